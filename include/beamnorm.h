@@ -1,0 +1,197 @@
+/*
+ * beamnorm.h -- C ABI of libbeamnorm: the arithmetic epilogue of a fused
+ * tensor-parallel all-reduce in an LLM decoder layer, on one GB300 GPU.
+ *
+ * The operation (sources):
+ *   "Fuse Beam's TP all-reduce with its sandwich norms" (vLLM pull request
+ *   62366), section "Claims", first bullet: an all-reduce followed by an FP32
+ *   norm-residual-norm epilogue, with an optional MoE top-k finalize before
+ *   the reduction that keeps each rank's local BF16 rounding; section
+ *   "Details", "Build" bullet: the FP32 epilogue is not contracted into FMAs;
+ *   the workspace "returns None" (declines) for shapes it does not serve.
+ *   sglang pull request 34134 (cute-dsl MNNVL all-reduce fusion backend),
+ *   description: the two fused patterns "AllReduce + residual + RMSNorm" and
+ *   "MoE finalize + shared-expert add + AllReduce + residual + RMSNorm", the
+ *   deferred finalize "materialized in place" when fusion declines, and the
+ *   rule that a decline must never drop the owed reduction.
+ *
+ * Here the R tensor-parallel shards are all resident on the calling GPU; the
+ * reduction is over a data dimension and nothing is communicated.
+ *
+ * Arithmetic, per token row t (all FP32 operations single IEEE operations,
+ * round to nearest even, no FMA contraction, no flush to zero):
+ *   finalize (finalize entries only), for each shard r:
+ *       acc = w[r,t,0] * x_0;  acc = acc + w[r,t,j] * x_j  for j = 1..k-1
+ *       (x_j = BF16 row perm[r,t,j] of expert_out[r], widened exactly)
+ *       acc = acc + shared[r,t]            (when shared is not NULL)
+ *       z[r,t] = bf16(acc)                 (local BF16 rounding per shard)
+ *   rank-ordered reduction:  s = p_0;  s = s + p_r  for r = 1..R-1
+ *       (p_r = partials[r,t] or z[r,t], widened exactly)
+ *   post-RMSNorm:  ss1 = sum_h s^2;  r1 = 1 / sqrt(ss1 / H + eps);
+ *                  y = (s * r1) * gamma_post
+ *   residual add:  h = residual[t] + y;  residual[t] = bf16(h)      (in place)
+ *   pre-RMSNorm:   ss2 = sum_h h^2;  r2 = 1 / sqrt(ss2 / H + eps);
+ *                  out[t] = bf16((h * r2) * gamma_pre)
+ * The sums of squares are the FP32 rounding of the exact sum (the kernels
+ * accumulate exact products in a compensated pair), so results do not depend
+ * on how the row is split across threads.
+ *
+ * Conventions for every entry point:
+ *   - BF16 tensors are passed as uint16_t bit patterns.  All tensors are dense,
+ *     row-major, contiguous.  Every pointer is a device pointer on the current
+ *     CUDA device, except where stated.
+ *   - BF16 and FP32 tensor pointers must be 16-byte aligned; perm and w must be
+ *     4-byte aligned.  H must be a multiple of 8 (16-byte rows).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without synchronising.  The caller owns
+ *     every buffer; the library allocates nothing.
+ *   - On any status other than BN_OK nothing was enqueued, except BN_ERR_CUDA
+ *     from a failed launch.  bn_last_error() describes the failure.
+ *   - Arguments are validated on the host before any CUDA call: a NULL
+ *     required pointer, R or k outside [1, 16], T < 0, H <= 0, H % 8 != 0, a
+ *     misaligned pointer, eps negative or not finite, or an output range that
+ *     overlaps an input range gives BN_ERR_INVALID.  A valid shape that is not
+ *     served (H > 32768, R * k > 256, T * k >= 2^31) gives BN_ERR_UNSUPPORTED;
+ *     bn_supports() predicts it, so the caller can fall back (decline) before
+ *     doing any work.  T == 0 returns BN_OK and enqueues nothing.
+ *   - dbg (nullable) asks for intermediate values, for testing:
+ *       dbg->sum [T,H] FP32 reduced sum s, dbg->ss [T,2] FP32 (ss1, ss2),
+ *       dbg->z [R,T,H] BF16 per-shard finalize results (finalize entries).
+ *     Any member may be NULL.  With dbg == NULL nothing extra is written.
+ */
+#ifndef BEAMNORM_H
+#define BEAMNORM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BN_API __attribute__((visibility("default")))
+#else
+#define BN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BN_OK = 0,
+    BN_ERR_INVALID = 1,      /* bad argument; nothing enqueued */
+    BN_ERR_UNSUPPORTED = 2,  /* valid shape that is declined; nothing enqueued */
+    BN_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    BN_ERR_DEVICE = 4        /* bn_check_device_error found a device-side error bit */
+} bn_status;
+
+/* Device-side error bits (see bn_check_device_error). */
+#define BN_DEVERR_PERM_RANGE 1u  /* a perm value outside [0, T*k): clamped to 0, never trapped */
+#define BN_DEVERR_TIMEOUT 2u     /* a pipeline wait gave up after its time limit */
+
+typedef struct {
+    float *sum;    /* [T, H] FP32, or NULL */
+    float *ss;     /* [T, 2] FP32 (post-norm, pre-norm sum of squares), or NULL */
+    uint16_t *z;   /* [R, T, H] BF16 per-shard finalize results, or NULL */
+} bn_debug;
+
+/* ---- fused entry points ------------------------------------------------ */
+
+/* Sandwich epilogue after a tensor-parallel all-reduce.
+ *   partials   [R, T, H] BF16   one partial output per shard (rank r = row block r)
+ *   residual   [T, H]    BF16   read, then overwritten with bf16(h)
+ *   gamma_post [H]       FP32   post-RMSNorm weight (applied to the reduced sum)
+ *   gamma_pre  [H]       FP32   next layer's input-RMSNorm weight
+ *   out        [T, H]    BF16   written; must not overlap any input
+ * Source: "Fuse Beam's TP all-reduce with its sandwich norms", "Claims". */
+BN_API bn_status bn_reduce_norm(const uint16_t *partials, int R, int T, int H,
+                         uint16_t *residual, const float *gamma_post,
+                         const float *gamma_pre, float eps, uint16_t *out,
+                         const bn_debug *dbg, void *stream);
+
+/* MoE top-k finalize per shard, then the sandwich epilogue.
+ *   expert_out [R, T*k, H] BF16  permuted expert-output rows of each shard
+ *   perm       [R, T, k]   int32 gather index: slot j of token t reads row
+ *                                perm[r,t,j] of expert_out[r]; values outside
+ *                                [0, T*k) set BN_DEVERR_PERM_RANGE and read row 0
+ *   w          [R, T, k]   FP32  top-k weights of each shard
+ *   shared     [R, T, H]   BF16  shared-expert output of each shard, or NULL (zeros)
+ *   residual, gamma_post, gamma_pre, out: as bn_reduce_norm
+ * Sources: "Fuse Beam's TP all-reduce with its sandwich norms", "Claims";
+ * sglang pull request 34134, description. */
+BN_API bn_status bn_finalize_reduce_norm(const uint16_t *expert_out, const int32_t *perm,
+                                  const float *w, const uint16_t *shared,
+                                  int R, int T, int k, int H,
+                                  uint16_t *residual, const float *gamma_post,
+                                  const float *gamma_pre, float eps, uint16_t *out,
+                                  const bn_debug *dbg, void *stream);
+
+/* The single-norm pattern "AllReduce + residual + RMSNorm": no post-norm,
+ * h = residual + s, then the RMSNorm with weight gamma.  dbg->ss[:,0] is 0.
+ * Source: sglang pull request 34134, description (first fused pattern). */
+BN_API bn_status bn_reduce_residual_norm(const uint16_t *partials, int R, int T, int H,
+                                  uint16_t *residual, const float *gamma, float eps,
+                                  uint16_t *out, const bn_debug *dbg, void *stream);
+
+/* "MoE finalize + shared-expert add + AllReduce + residual + RMSNorm".
+ * Source: sglang pull request 34134, description (second fused pattern). */
+BN_API bn_status bn_finalize_reduce_residual_norm(const uint16_t *expert_out, const int32_t *perm,
+                                           const float *w, const uint16_t *shared,
+                                           int R, int T, int k, int H,
+                                           uint16_t *residual, const float *gamma, float eps,
+                                           uint16_t *out, const bn_debug *dbg, void *stream);
+
+/* ---- unfused pieces (the decline / fallback path and its measurement) --- */
+
+/* Rank-ordered FP32 sum only: sum_out [T, H] FP32 = s. */
+BN_API bn_status bn_reduce_only(const uint16_t *partials, int R, int T, int H,
+                         float *sum_out, void *stream);
+
+/* Per-shard finalize rounded to BF16, then the rank-ordered FP32 sum only. */
+BN_API bn_status bn_finalize_reduce_only(const uint16_t *expert_out, const int32_t *perm,
+                                  const float *w, const uint16_t *shared,
+                                  int R, int T, int k, int H, float *sum_out,
+                                  void *stream);
+
+/* The sandwich epilogue given the FP32 sum [T, H] (post-norm, residual add,
+ * pre-norm).  Together with bn_reduce_only / bn_finalize_reduce_only it gives
+ * the same bits as the fused entry points. */
+BN_API bn_status bn_norm_only(const float *sum, int T, int H, uint16_t *residual,
+                       const float *gamma_post, const float *gamma_pre, float eps,
+                       uint16_t *out, const bn_debug *dbg, void *stream);
+
+/* The deferred finalize materialised on its own: z_out [R, T, H] BF16 =
+ * bf16(sum_j w*x_j + shared) per shard, with no reduction.
+ * Source: sglang pull request 34134, description ("a deferred finalize that
+ * reaches a non-fusing path is materialized in place"). */
+BN_API bn_status bn_finalize_only(const uint16_t *expert_out, const int32_t *perm,
+                           const float *w, const uint16_t *shared,
+                           int R, int T, int k, int H, uint16_t *z_out, void *stream);
+
+/* ---- queries and errors ------------------------------------------------ */
+
+/* 1 if the fused entry points serve this shape (k = 0 for the reduce-only
+ * entries), 0 if the caller must fall back.  Pure host logic. */
+BN_API int bn_supports(int R, int T, int k, int H);
+
+/* Synchronises `stream`, reads the device-side error bits of the current
+ * device into *bits (nullable), clears them, and returns BN_ERR_DEVICE if any
+ * bit was set, BN_ERR_CUDA if the synchronisation failed, else BN_OK. */
+BN_API bn_status bn_check_device_error(void *stream, unsigned *bits);
+
+/* Message describing the last failure on the calling thread ("" if none). */
+BN_API const char *bn_last_error(void);
+
+/* Name of a status code. */
+BN_API const char *bn_status_string(bn_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+BN_API int bn_version(void);
+
+/* Launch-shape overrides for measurement sweeps (process-wide; 0 = automatic):
+ * cluster_size in {1,2,4,8,16} CTAs per token row, stages = pipeline depth,
+ * threads = consumer threads per CTA (a multiple of 32, at most 512). */
+BN_API bn_status bn_set_tuning(int cluster_size, int stages, int threads);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BEAMNORM_H */

@@ -1,0 +1,134 @@
+"""GPU-vs-oracle comparison helpers for the parity tests and the smoke check.
+
+Inputs come from the seeded generator (on the GPU for large cases); the
+oracle gets host copies of the same bytes.  For large T the oracle computes a
+sample of token rows: the sampled rows' operands (their shard rows, or their
+gathered expert rows with the perm renumbered) are copied into a compact input
+set, which the oracle processes exactly as it would the full one, since every
+token row depends only on its own operands.
+
+Acceptance (per element): the FP32 reduced sum and the per-shard BF16
+finalize results bit-exact; the sums of squares within 1e-5 relative; the BF16
+output and updated residual within 1 BF16 ulp (+0 == -0, NaN == NaN).
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+import oracle
+from tests.helpers import assert_bf16_close, assert_bits_equal, assert_rel_close, bf16_ulp_diff
+from tp_reduce_residual_gb300 import beamnorm as bn
+from tp_reduce_residual_gb300 import inputs
+
+SS_RTOL = 1e-5
+MAX_ULP = 1
+NAN_BF16 = 0x7FC0
+
+
+def gpu_inputs(wl, T, seed=None, with_shared=True):
+    return inputs.make_inputs(wl, T, device="cuda", seed=seed, with_shared=with_shared)
+
+
+def _nan_like(shape, dtype):
+    if dtype == torch.bfloat16:
+        return torch.full(shape, NAN_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    return torch.full(shape, float("nan"), dtype=dtype, device="cuda")
+
+
+def run_fused(d, single: bool = False, debug: bool = True, stream=None) -> dict:
+    """One fused call on a copy of the residual; outputs prefilled with NaN."""
+    op, R, T, H, k = d["op"], d["R"], d["T"], d["H"], d["k"]
+    fin = op == "finalize_reduce_norm"
+    res = d["residual"].clone()
+    out = _nan_like((T, H), torch.bfloat16)
+    dbg = None
+    if debug:
+        dbg = bn.Debug(sum=_nan_like((T, H), torch.float32), ss=_nan_like((T, 2), torch.float32),
+                       z=_nan_like((R, T, H), torch.bfloat16) if fin else None)
+    if not fin:
+        if single:
+            bn.reduce_residual_norm(d["partials"], res, d["gamma_pre"], d["eps"], out=out, debug=dbg,
+                                    stream=stream)
+        else:
+            bn.reduce_norm(d["partials"], res, d["gamma_post"], d["gamma_pre"], d["eps"], out=out,
+                           debug=dbg, stream=stream)
+    else:
+        if single:
+            bn.finalize_reduce_residual_norm(d["expert_out"], d["perm"], d["w"], d["shared"], res,
+                                             d["gamma_pre"], d["eps"], out=out, debug=dbg,
+                                             stream=stream)
+        else:
+            bn.finalize_reduce_norm(d["expert_out"], d["perm"], d["w"], d["shared"], res,
+                                    d["gamma_post"], d["gamma_pre"], d["eps"], out=out, debug=dbg,
+                                    stream=stream)
+    bits = bn.check_device_error(stream=stream)
+    assert bits == 0, bits
+    r = {"out": inputs.u16(out), "residual_out": inputs.u16(res)}
+    if debug:
+        r["sum"] = dbg.sum.cpu().numpy()
+        r["ss"] = dbg.ss.cpu().numpy()
+        if fin:
+            r["z"] = inputs.u16(dbg.z)
+    return r
+
+
+def compact(d, rows: Sequence[int]) -> dict:
+    """The operands of the selected token rows as a self-contained input set."""
+    idx = torch.as_tensor(list(rows), dtype=torch.long, device=d["residual"].device)
+    n = idx.numel()
+    c = {key: d[key] for key in ("op", "R", "H", "k", "eps", "gamma_post", "gamma_pre")}
+    c["T"] = n
+    c["residual"] = d["residual"][idx].contiguous()
+    if d["op"] == "reduce_norm":
+        c["partials"] = d["partials"][:, idx].contiguous()
+    else:
+        R, k = d["R"], d["k"]
+        rows_used = d["perm"][:, idx, :].long().reshape(R, n * k)
+        c["expert_out"] = torch.stack([d["expert_out"][r][rows_used[r]] for r in range(R)]).contiguous()
+        c["perm"] = torch.arange(n * k, dtype=torch.int32, device=idx.device).reshape(1, n, k).repeat(R, 1, 1)
+        c["w"] = d["w"][:, idx].contiguous()
+        c["shared"] = None if d["shared"] is None else d["shared"][:, idx].contiguous()
+    return c
+
+
+def run_oracle(d, rows: Optional[Sequence[int]] = None, single: bool = False) -> dict:
+    """Oracle results for all rows, or for ``rows`` (in that order)."""
+    src = d if rows is None else compact(d, rows)
+    h = inputs.to_numpy(src)
+    flags = oracle.SINGLE_NORM if single else 0
+    if h["op"] == "reduce_norm":
+        return oracle.reduce_norm(h["partials"], h["residual"], h["gamma_post"], h["gamma_pre"],
+                                  h["eps"], flags=flags)
+    return oracle.finalize_reduce_norm(h["expert_out"], h["perm"], h["w"], h.get("shared"),
+                                       h["residual"], h["gamma_post"], h["gamma_pre"], h["eps"],
+                                       flags=flags, want_z=True)
+
+
+def compare(g: dict, ref: dict, rows: Optional[Sequence[int]] = None, what: str = "") -> dict:
+    """Assert the acceptance bar; return exact-match statistics."""
+    sel = slice(None) if rows is None else np.asarray(rows)
+    stats = {}
+    if "sum" in g:
+        assert_bits_equal(g["sum"][sel], ref["sum"], f"{what} sum")
+    if "z" in g and "z" in ref:
+        assert_bits_equal(g["z"][:, sel], ref["z"], f"{what} z")
+    if "ss" in g:
+        assert_rel_close(g["ss"][sel], ref["ss"], SS_RTOL, f"{what} ss")
+        stats["ss_exact"] = float(np.mean(g["ss"][sel].view(np.uint32) == ref["ss"].view(np.uint32)))
+    assert_bf16_close(g["residual_out"][sel], ref["residual_out"], MAX_ULP, f"{what} residual_out")
+    assert_bf16_close(g["out"][sel], ref["out"], MAX_ULP, f"{what} out")
+    stats["out_exact"] = float(np.mean(bf16_ulp_diff(g["out"][sel], ref["out"]) == 0))
+    stats["residual_exact"] = float(np.mean(bf16_ulp_diff(g["residual_out"][sel], ref["residual_out"]) == 0))
+    return stats
+
+
+def sample_rows(T: int, n: int, seed: int = 0) -> list:
+    """First, last and evenly spread random rows (sorted, unique)."""
+    if T <= n:
+        return list(range(T))
+    rng = np.random.default_rng(seed)
+    rows = set([0, T - 1, T // 2]) | set(rng.choice(T, size=n - 3, replace=False).tolist())
+    return sorted(rows)[:n]

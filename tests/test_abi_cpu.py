@@ -1,0 +1,155 @@
+"""Host-side tests of the C ABI (no GPU needed, no compute call made).
+
+The library is loaded on a machine without a GPU; every call here is rejected
+by host-side validation before any CUDA runtime call, or is pure host logic.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from tp_reduce_residual_gb300 import beamnorm as bn
+from tp_reduce_residual_gb300 import build as nbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "beamnorm.h")
+
+A16 = 0x10000      # a 16-byte aligned fake device address (never dereferenced)
+MIS = 0x10004      # 4-byte aligned, not 16-byte aligned
+
+
+@pytest.fixture(scope="module")
+def L():
+    nbuild.build()
+    return bn.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"BN_API\s+[\w\s\*]+?\b(bn_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_symbols()
+    assert len(names) == len(bn.EXPORTS) and set(names) == set(bn.EXPORTS), names
+    for name in names:
+        assert hasattr(L, name), name
+
+
+def test_library_is_built_for_sm103a():
+    # the build passes exactly one -gencode, for sm_103a
+    assert nbuild.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert "-fmad=false" in nbuild.NVCC_FLAGS
+
+
+def test_version_and_status_strings(L):
+    assert L.bn_version() == 10000
+    assert L.bn_status_string(0) == b"BN_OK"
+    assert L.bn_status_string(2) == b"BN_ERR_UNSUPPORTED"
+    assert L.bn_status_string(99) == b"unknown status"
+
+
+@pytest.mark.parametrize("R,T,k,H,expect", [
+    (2, 8, 0, 256, 1), (4, 4096, 0, 5120, 1), (8, 4096, 0, 8192, 1), (8, 1024, 8, 6144, 1),
+    (8, 4096, 10, 8192, 1), (16, 1, 16, 32768, 1), (1, 0, 0, 8, 1),
+    (0, 8, 0, 256, 0), (17, 8, 0, 256, 0), (2, -1, 0, 256, 0), (2, 8, 0, 0, 0), (2, 8, 0, 100, 0),
+    (2, 8, 0, 32776, 0), (16, 8, 17, 256, 0), (8, 2 ** 28, 10, 256, 0),
+])
+def test_supports(L, R, T, k, H, expect):
+    assert L.bn_supports(R, T, k, H) == expect
+
+
+def _reduce(L, partials=A16, R=2, T=8, H=256, residual=A16 * 2, gp=A16 * 3, gq=A16 * 4,
+            eps=1e-6, out=A16 * 5):
+    return L.bn_reduce_norm(partials, R, T, H, residual, gp, gq, eps, out, None, None)
+
+
+@pytest.mark.parametrize("kw,needle", [
+    (dict(partials=None), "partials is NULL"),
+    (dict(residual=None), "residual is NULL"),
+    (dict(out=None), "out is NULL"),
+    (dict(gp=None), "gamma_post is NULL"),
+    (dict(R=0), "R=0"),
+    (dict(R=17), "R=17"),
+    (dict(T=-3), "T=-3"),
+    (dict(H=250), "multiple of 8"),
+    (dict(H=0), "H=0"),
+    (dict(partials=MIS), "partials is not 16-byte aligned"),
+    (dict(out=MIS), "out is not 16-byte aligned"),
+    (dict(eps=-1.0), "eps"),
+    (dict(eps=float("nan")), "eps"),
+    (dict(eps=float("inf")), "eps"),
+    (dict(out=A16 * 2), "overlaps"),           # out == residual
+    (dict(out=A16 + 64), "overlaps"),          # out inside partials
+    (dict(residual=A16 + 16), "overlaps"),     # residual inside partials
+])
+def test_reduce_norm_rejects_bad_arguments(L, kw, needle):
+    assert _reduce(L, **kw) == bn.ERR_INVALID
+    assert needle in L.bn_last_error().decode()
+
+
+def test_unsupported_shape_is_declined_before_any_work(L):
+    # valid arguments, H above the served maximum: declined, nothing enqueued
+    st = _reduce(L, H=40960, residual=A16 * 1000, gp=A16 * 2000, gq=A16 * 2100, out=A16 * 3000)
+    assert st == bn.ERR_UNSUPPORTED
+    assert "H=40960" in L.bn_last_error().decode()
+
+
+def test_zero_tokens_is_a_no_op(L):
+    assert _reduce(L, T=0) == bn.OK
+    assert L.bn_last_error() == b""
+
+
+def test_finalize_rejects_bad_arguments(L):
+    f = L.bn_finalize_reduce_norm
+    args = dict(x=A16, perm=A16 * 10, w=A16 * 20, sh=A16 * 30, R=2, T=4, k=3, H=64,
+                res=A16 * 40, gp=A16 * 50, gq=A16 * 60, eps=1e-6, out=A16 * 70)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(a["x"], a["perm"], a["w"], a["sh"], a["R"], a["T"], a["k"], a["H"], a["res"],
+                 a["gp"], a["gq"], a["eps"], a["out"], None, None)
+
+    assert call(k=0) == bn.ERR_INVALID
+    assert call(k=17) == bn.ERR_INVALID
+    assert call(perm=None) == bn.ERR_INVALID
+    assert call(perm=A16 * 10 + 2) == bn.ERR_INVALID       # perm needs 4-byte alignment
+    assert call(w=None) == bn.ERR_INVALID
+    assert call(sh=A16 * 30 + 8) == bn.ERR_INVALID         # shared misaligned
+    assert call(out=A16 * 10) == bn.ERR_INVALID            # out overlaps perm
+    assert call(R=16, k=16, T=0) == bn.OK                  # nothing to do
+    assert call(T=0) == bn.OK
+
+
+def test_split_and_finalize_only_reject_bad_arguments(L):
+    assert L.bn_reduce_only(A16, 2, 4, 64, None, None) == bn.ERR_INVALID
+    assert L.bn_reduce_only(A16, 2, 4, 64, A16 + 32, None) == bn.ERR_INVALID   # sum overlaps
+    assert L.bn_norm_only(None, 4, 64, A16, A16 * 2, A16 * 3, 1e-6, A16 * 4, None, None) == bn.ERR_INVALID
+    assert L.bn_finalize_only(A16, A16 * 10, A16 * 20, None, 2, 4, 3, 64, None, None) == bn.ERR_INVALID
+    assert L.bn_finalize_reduce_only(A16, A16 * 10, A16 * 20, None, 2, 4, 3, 63, A16 * 40,
+                                     None) == bn.ERR_INVALID
+
+
+def test_set_tuning_validates(L):
+    assert L.bn_set_tuning(3, 0, 0) == bn.ERR_INVALID
+    assert L.bn_set_tuning(0, 1, 0) == bn.ERR_INVALID
+    assert L.bn_set_tuning(0, 65, 0) == bn.ERR_INVALID
+    assert L.bn_set_tuning(0, 0, 48) == bn.ERR_INVALID
+    assert L.bn_set_tuning(16, 8, 256) == bn.OK
+    assert L.bn_set_tuning(0, 0, 0) == bn.OK
+
+
+def test_python_binding_checks_before_calling(L):
+    cpu = torch.zeros(2, 8, 256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        bn.reduce_norm(cpu, torch.zeros(8, 256, dtype=torch.bfloat16), torch.zeros(256),
+                       torch.zeros(256), 1e-6)
+
+
+def test_binding_fails_loudly_without_library(monkeypatch):
+    monkeypatch.setattr(bn, "_lib", None)
+    monkeypatch.setattr(bn, "LIB_PATH", "/nonexistent/libbeamnorm.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        bn.load()

@@ -1,0 +1,325 @@
+"""GPU parity of libbeamnorm's kernels against the CPU oracle (GB300, sm_103a).
+
+Every call goes through the C ABI (via the ctypes binding).  The bar: the FP32
+reduced sum and the per-shard BF16 finalize bit-exact; sums of squares within
+1e-5 relative; BF16 outputs and the updated residual within 1 BF16 ulp.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import parity
+from tests.helpers import assert_bits_equal
+from tp_reduce_residual_gb300 import beamnorm as bn
+from tp_reduce_residual_gb300 import build as nbuild
+from tp_reduce_residual_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "the GPU tests need a CUDA device"
+    nbuild.build()
+    bn.load()
+    bn.set_tuning(0, 0, 0)
+    yield
+    bn.set_tuning(0, 0, 0)
+    torch.cuda.empty_cache()
+
+
+def _free():
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+# ---- small shapes: several tiles, ragged tails, extremes ----------------------------
+
+REDUCE_SMALL = [
+    # (R, T, H, row_scale, partial_std)
+    (2, 8, 256, False, 1.0),
+    (4, 37, 5120, False, 0.5),
+    (8, 70, 8192, True, 0.5),
+    (3, 5, 1000, False, 0.5),      # 125 chunks: ragged against 32-thread warps
+    (1, 3, 8, False, 0.5),         # one chunk per row
+    (16, 2, 32768, False, 0.5),    # largest served R and H
+    (5, 153, 6144, True, 0.5),     # more rows than SMs
+]
+
+
+@pytest.mark.parametrize("R,T,H,row_scale,std", REDUCE_SMALL)
+def test_reduce_norm_small(R, T, H, row_scale, std):
+    wl = inputs.custom("reduce_norm", R, H, partial_std=std, row_scale=row_scale)
+    d = parity.gpu_inputs(wl, T, seed=1000 + R * 7 + T)
+    g = parity.run_fused(d)
+    parity.compare(g, parity.run_oracle(d), what=f"reduce R={R} T={T} H={H}")
+
+
+FIN_SMALL = [
+    # (R, T, k, H)
+    (8, 19, 8, 6144),
+    (8, 13, 10, 8192),
+    (2, 7, 3, 1000),
+    (1, 5, 1, 64),
+    (16, 3, 16, 4096),             # R*k = 256, the served maximum
+]
+
+
+@pytest.mark.parametrize("with_shared", [True, False])
+@pytest.mark.parametrize("R,T,k,H", FIN_SMALL)
+def test_finalize_reduce_norm_small(R, T, k, H, with_shared):
+    wl = inputs.custom("finalize_reduce_norm", R, H, k, partial_std=0.3, shared_std=0.3)
+    d = parity.gpu_inputs(wl, T, seed=2000 + R * 11 + T, with_shared=with_shared)
+    g = parity.run_fused(d)
+    parity.compare(g, parity.run_oracle(d), what=f"finalize R={R} T={T} k={k} H={H}")
+
+
+@pytest.mark.parametrize("op", ["reduce_norm", "finalize_reduce_norm"])
+def test_single_norm_variants(op):
+    if op == "reduce_norm":
+        wl = inputs.custom(op, 4, 5120)
+        d = parity.gpu_inputs(wl, 29, seed=31)
+    else:
+        wl = inputs.custom(op, 8, 6144, 8, partial_std=0.3)
+        d = parity.gpu_inputs(wl, 11, seed=32)
+    g = parity.run_fused(d, single=True)
+    ref = parity.run_oracle(d, single=True)
+    parity.compare(g, ref, what=f"{op} single norm")
+    assert np.all(g["ss"][:, 0] == 0.0)
+
+
+# ---- the five workloads at their full sizes ------------------------------------------
+
+SWEEP = [(wl.index, T) for wl in inputs.WORKLOADS for T in wl.tokens]
+FULL_ORACLE_LIMIT = 256    # tokens up to which the oracle checks every row
+SAMPLE = 48                # rows the oracle checks above that
+
+
+@pytest.mark.parametrize("idx,T", SWEEP, ids=[f"C{i}-T{T}" for i, T in SWEEP])
+def test_workload_parity(idx, T):
+    wl = inputs.WORKLOADS[idx]
+    d = parity.gpu_inputs(wl, T)
+    g = parity.run_fused(d)
+    rows = None if T <= FULL_ORACLE_LIMIT else parity.sample_rows(T, SAMPLE, seed=T)
+    stats = parity.compare(g, parity.run_oracle(d, rows=rows), rows=rows, what=wl.describe(T))
+    # the compensated sums of squares are the correctly rounded exact sums:
+    # nearly all match the oracle's double accumulation bit for bit
+    assert stats["ss_exact"] >= 0.99, stats
+    del d, g
+    _free()
+
+
+# ---- unfused split and the materialised finalize ---------------------------------------
+
+def test_reduce_split_equals_fused():
+    wl = inputs.WORKLOADS[2]
+    d = parity.gpu_inputs(wl, 64)
+    fused = parity.run_fused(d)
+    s = bn.reduce_only(d["partials"])
+    res = d["residual"].clone()
+    ss = torch.zeros(64, 2, device="cuda")
+    out = bn.norm_only(s, res, d["gamma_post"], d["gamma_pre"], d["eps"], debug=bn.Debug(ss=ss))
+    torch.cuda.synchronize()
+    assert_bits_equal(s.cpu().numpy(), fused["sum"], "sum")
+    assert_bits_equal(inputs.u16(res), fused["residual_out"], "residual_out")
+    assert_bits_equal(inputs.u16(out), fused["out"], "out")
+    assert_bits_equal(ss.cpu().numpy(), fused["ss"], "ss")
+
+
+@pytest.mark.parametrize("with_shared", [True, False])
+def test_finalize_split_equals_fused(with_shared):
+    wl = inputs.WORKLOADS[4]
+    d = parity.gpu_inputs(wl, 16, with_shared=with_shared)
+    fused = parity.run_fused(d)
+    s = bn.finalize_reduce_only(d["expert_out"], d["perm"], d["w"], d["shared"])
+    res = d["residual"].clone()
+    out = bn.norm_only(s, res, d["gamma_post"], d["gamma_pre"], d["eps"])
+    torch.cuda.synchronize()
+    assert_bits_equal(s.cpu().numpy(), fused["sum"], "sum")
+    assert_bits_equal(inputs.u16(res), fused["residual_out"], "residual_out")
+    assert_bits_equal(inputs.u16(out), fused["out"], "out")
+
+
+def test_finalize_only_matches_oracle():
+    wl = inputs.WORKLOADS[3]
+    d = parity.gpu_inputs(wl, 16)
+    z = bn.finalize_only(d["expert_out"], d["perm"], d["w"], d["shared"])
+    torch.cuda.synchronize()
+    ref = parity.run_oracle(d)
+    assert_bits_equal(inputs.u16(z), ref["z"], "z")
+
+
+def test_decline_then_fallback_gives_the_same_bits():
+    """When the fused op declines, a caller that materialises the finalize and
+    then reduces and normalises gets exactly the fused result: nothing owed is
+    dropped on the fallback path."""
+    wl = inputs.WORKLOADS[4]
+    d = parity.gpu_inputs(wl, 8)
+    fused = parity.run_fused(d)
+    z = bn.finalize_only(d["expert_out"], d["perm"], d["w"], d["shared"])
+    res = d["residual"].clone()
+    out = bn.reduce_norm(z, res, d["gamma_post"], d["gamma_pre"], d["eps"])
+    torch.cuda.synchronize()
+    assert_bits_equal(inputs.u16(res), fused["residual_out"], "residual_out")
+    assert_bits_equal(inputs.u16(out), fused["out"], "out")
+
+
+# ---- launch shapes, streams, graphs ------------------------------------------------------
+
+@pytest.mark.parametrize("cluster,stages,threads", [
+    (1, 0, 0), (2, 0, 0), (4, 3, 0), (8, 0, 0), (16, 2, 0), (1, 2, 0), (1, 7, 0),
+    (1, 0, 256), (1, 0, 128), (2, 5, 64),
+])
+def test_launch_shapes_give_identical_bits(cluster, stages, threads):
+    wl = inputs.custom("finalize_reduce_norm", 8, 8192, 10, partial_std=0.3)
+    d = parity.gpu_inputs(wl, 21, seed=77)
+    try:
+        bn.set_tuning(cluster, stages, threads)
+        g = parity.run_fused(d)
+    finally:
+        bn.set_tuning(0, 0, 0)
+    base = parity.run_fused(d)
+    for key in ("sum", "ss", "z", "out", "residual_out"):
+        assert_bits_equal(g[key], base[key], key)
+    parity.compare(g, parity.run_oracle(d), what=f"cluster={cluster} stages={stages}")
+
+
+def test_reduce_launch_shapes_give_identical_bits():
+    wl = inputs.custom("reduce_norm", 8, 5120, row_scale=True)
+    d = parity.gpu_inputs(wl, 45, seed=78)
+    base = parity.run_fused(d)
+    for cluster in (2, 4, 16):
+        try:
+            bn.set_tuning(cluster, 0, 0)
+            g = parity.run_fused(d)
+        finally:
+            bn.set_tuning(0, 0, 0)
+        for key in ("sum", "ss", "out", "residual_out"):
+            assert_bits_equal(g[key], base[key], f"cluster={cluster} {key}")
+
+
+def test_side_stream_and_graph_replay():
+    wl = inputs.WORKLOADS[3]
+    d = parity.gpu_inputs(wl, 64)
+    eager = parity.run_fused(d, debug=False)
+    s = torch.cuda.Stream()
+    res = d["residual"].clone()
+    res0 = res.clone()
+    out = torch.empty_like(res)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        bn.finalize_reduce_norm(d["expert_out"], d["perm"], d["w"], d["shared"], res,
+                                d["gamma_post"], d["gamma_pre"], d["eps"], out=out)
+    s.synchronize()
+    assert_bits_equal(inputs.u16(out), eager["out"], "side stream out")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        bn.finalize_reduce_norm(d["expert_out"], d["perm"], d["w"], d["shared"], res,
+                                d["gamma_post"], d["gamma_pre"], d["eps"], out=out)
+    res.copy_(res0)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert_bits_equal(inputs.u16(out), eager["out"], "graph out")
+    assert_bits_equal(inputs.u16(res), eager["residual_out"], "graph residual")
+
+
+def test_two_calls_update_the_residual_twice():
+    wl = inputs.WORKLOADS[1]
+    d = parity.gpu_inputs(wl, 8)
+    res = d["residual"].clone()
+    bn.reduce_norm(d["partials"], res, d["gamma_post"], d["gamma_pre"], d["eps"])
+    out2 = bn.reduce_norm(d["partials"], res, d["gamma_post"], d["gamma_pre"], d["eps"])
+    torch.cuda.synchronize()
+    h = inputs.to_numpy(d)
+    r1 = oracle.reduce_norm(h["partials"], h["residual"], h["gamma_post"], h["gamma_pre"], h["eps"])
+    r2 = oracle.reduce_norm(h["partials"], r1["residual_out"], h["gamma_post"], h["gamma_pre"],
+                            h["eps"])
+    parity.compare({"out": inputs.u16(out2), "residual_out": inputs.u16(res)}, r2, what="second call")
+
+
+# ---- memory safety substitutes (guard bands, NaN prefill) --------------------------------
+
+def _guarded(n, dtype, guard=4096):
+    """A tensor of n elements inside a NaN-filled buffer with guard bands."""
+    esz = torch.tensor([], dtype=dtype).element_size()
+    g = guard // esz
+    buf = parity._nan_like((g + n + g,), dtype)
+    return buf, buf[g:g + n], g
+
+
+def _guard_intact(buf, g, n):
+    bits = buf.view(torch.int16) if buf.dtype == torch.bfloat16 else buf.view(torch.int32)
+    ref = parity.NAN_BF16 if buf.dtype == torch.bfloat16 else None
+    head, tail = bits[:g], bits[g + n:]
+    if ref is not None:
+        return bool((head == ref).all() and (tail == ref).all())
+    return bool(torch.isnan(buf[:g]).all() and torch.isnan(buf[g + n:]).all())
+
+
+@pytest.mark.parametrize("cluster", [1, 16])
+def test_outputs_stay_inside_their_buffers(cluster):
+    wl = inputs.custom("finalize_reduce_norm", 4, 1000, 3, partial_std=0.3)
+    R, T, k, H = 4, 9, 3, 1000
+    d = parity.gpu_inputs(wl, T, seed=5)
+    ob, out, og = _guarded(T * H, torch.bfloat16)
+    sb, s, sg = _guarded(T * H, torch.float32)
+    qb, ss, qg = _guarded(T * 2, torch.float32)
+    zb, z, zg = _guarded(R * T * H, torch.bfloat16)
+    rb, res, rg = _guarded(T * H, torch.bfloat16)
+    res.copy_(d["residual"].reshape(-1))
+    try:
+        bn.set_tuning(cluster, 0, 0)
+        bn.finalize_reduce_norm(d["expert_out"], d["perm"], d["w"], d["shared"], res.view(T, H),
+                                d["gamma_post"], d["gamma_pre"], d["eps"], out=out.view(T, H),
+                                debug=bn.Debug(sum=s.view(T, H), ss=ss.view(T, 2), z=z.view(R, T, H)))
+        torch.cuda.synchronize()
+    finally:
+        bn.set_tuning(0, 0, 0)
+    for buf, g, n in ((ob, og, T * H), (sb, sg, T * H), (qb, qg, T * 2), (zb, zg, R * T * H),
+                      (rb, rg, T * H)):
+        assert _guard_intact(buf, g, n)
+    # every element written (no NaN left from the prefill)
+    assert not torch.isnan(out.float()).any() and not torch.isnan(s).any()
+    assert not torch.isnan(ss).any() and not torch.isnan(z.float()).any()
+
+
+# ---- errors --------------------------------------------------------------------------------
+
+def test_perm_out_of_range_sets_the_device_flag_without_trapping():
+    wl = inputs.custom("finalize_reduce_norm", 2, 256, 4, partial_std=0.3)
+    d = parity.gpu_inputs(wl, 6, seed=9)
+    bad = d["perm"].clone()
+    bad[1, 2, 3] = 6 * 4 + 5
+    bad[0, 0, 0] = -1
+    res = d["residual"].clone()
+    bn.finalize_reduce_norm(d["expert_out"], bad, d["w"], d["shared"], res, d["gamma_post"],
+                            d["gamma_pre"], d["eps"])
+    bits = bn.check_device_error(raise_on_error=False)
+    assert bits == bn.DEVERR_PERM_RANGE
+    assert bn.check_device_error() == 0          # cleared
+    # the context is still usable
+    g = parity.run_fused(d)
+    parity.compare(g, parity.run_oracle(d), what="after the flagged call")
+
+
+def test_zero_tokens_and_declined_shapes_touch_nothing():
+    R, H = 2, 64
+    p = torch.randn(R, 0, H, device="cuda").to(torch.bfloat16)
+    res = torch.empty(0, H, dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(H, device="cuda")
+    out = bn.reduce_norm(p, res, g, g, 1e-6)
+    assert out.shape == (0, H)
+    # a valid but unserved shape is declined before any work
+    Hb = 40960
+    pb = torch.zeros(1, 1, Hb, dtype=torch.bfloat16, device="cuda")
+    rb = torch.zeros(1, Hb, dtype=torch.bfloat16, device="cuda")
+    gb = torch.ones(Hb, device="cuda")
+    ob = torch.full((1, Hb), 3.0, device="cuda").to(torch.bfloat16)
+    assert not bn.supports(1, 1, 0, Hb)
+    with pytest.raises(bn.BeamNormError) as e:
+        bn.reduce_norm(pb, rb, gb, gb, 1e-6, out=ob)
+    assert e.value.status == bn.ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert bool((ob.float() == 3.0).all())

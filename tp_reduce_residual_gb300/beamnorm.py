@@ -1,0 +1,332 @@
+"""Python binding of libbeamnorm (argument marshalling only).
+
+Every function here checks dtypes, shapes, devices and contiguity, then calls
+the C entry point of the same name with raw device pointers and the current
+CUDA stream.  All arithmetic runs in the library's CUDA kernels; there is no
+fallback.  If the library is missing the call raises.
+
+BF16 tensors are ``torch.bfloat16``; perm is ``torch.int32``; w, gammas and
+FP32 sums are ``torch.float32``.  Shapes: partials [R,T,H], expert_out
+[R,T*k,H], perm and w [R,T,k], shared [R,T,H] (or None), residual and out
+[T,H], gammas [H].  The residual is updated in place.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libbeamnorm.so")
+
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE = 0, 1, 2, 3, 4
+DEVERR_PERM_RANGE, DEVERR_TIMEOUT = 1, 2
+
+# Every symbol declared in include/beamnorm.h.
+EXPORTS = (
+    "bn_reduce_norm", "bn_finalize_reduce_norm", "bn_reduce_residual_norm",
+    "bn_finalize_reduce_residual_norm", "bn_reduce_only", "bn_finalize_reduce_only",
+    "bn_norm_only", "bn_finalize_only", "bn_supports", "bn_check_device_error",
+    "bn_last_error", "bn_status_string", "bn_version", "bn_set_tuning",
+)
+
+
+class BeamNormError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_STATUS_NAMES = {OK: "BN_OK", ERR_INVALID: "BN_ERR_INVALID", ERR_UNSUPPORTED: "BN_ERR_UNSUPPORTED",
+                 ERR_CUDA: "BN_ERR_CUDA", ERR_DEVICE: "BN_ERR_DEVICE"}
+
+
+class _Debug(ctypes.Structure):
+    _fields_ = [("sum", ctypes.c_void_p), ("ss", ctypes.c_void_p), ("z", ctypes.c_void_p)]
+
+
+@dataclass
+class Debug:
+    """Optional intermediate outputs: sum [T,H] FP32, ss [T,2] FP32, z [R,T,H] BF16."""
+    sum: Optional[torch.Tensor] = None
+    ss: Optional[torch.Tensor] = None
+    z: Optional[torch.Tensor] = None
+
+
+_lib = None
+_lock = threading.Lock()
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+
+
+def load() -> ctypes.CDLL:
+    """Load libbeamnorm.so (built by ``tp_reduce_residual_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libbeamnorm is not built ({LIB_PATH} missing); run "
+                               "`python -m tp_reduce_residual_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        dbgp = ctypes.POINTER(_Debug)
+        sig = {
+            "bn_reduce_norm": [_P, _I, _I, _I, _P, _P, _P, _F, _P, dbgp, _P],
+            "bn_finalize_reduce_norm": [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _F, _P, dbgp, _P],
+            "bn_reduce_residual_norm": [_P, _I, _I, _I, _P, _P, _F, _P, dbgp, _P],
+            "bn_finalize_reduce_residual_norm": [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _F, _P,
+                                                 dbgp, _P],
+            "bn_reduce_only": [_P, _I, _I, _I, _P, _P],
+            "bn_finalize_reduce_only": [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P],
+            "bn_norm_only": [_P, _I, _I, _P, _P, _P, _F, _P, dbgp, _P],
+            "bn_finalize_only": [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P],
+            "bn_supports": [_I, _I, _I, _I],
+            "bn_check_device_error": [_P, ctypes.POINTER(ctypes.c_uint)],
+            "bn_last_error": [],
+            "bn_status_string": [_I],
+            "bn_version": [],
+            "bn_set_tuning": [_I, _I, _I],
+        }
+        for name, args in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = _I
+        L.bn_last_error.restype = ctypes.c_char_p
+        L.bn_status_string.restype = ctypes.c_char_p
+        _lib = L
+        return L
+
+
+def _check(status: int):
+    if status != OK:
+        msg = load().bn_last_error().decode(errors="replace")
+        raise BeamNormError(status, msg)
+
+
+def _stream(t: torch.Tensor, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t: Optional[torch.Tensor], name: str, dtype, shape, device) -> int:
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _opt(t, name, dtype, shape, device) -> Optional[int]:
+    return None if t is None else _need(t, name, dtype, shape, device)
+
+
+def _debug(dbg: Optional[Debug], R, T, H, device, fin: bool):
+    if dbg is None:
+        return None
+    s = _Debug(_opt(dbg.sum, "debug.sum", torch.float32, (T, H), device),
+               _opt(dbg.ss, "debug.ss", torch.float32, (T, 2), device),
+               _opt(dbg.z, "debug.z", torch.bfloat16, (R, T, H), device) if fin else None)
+    return ctypes.byref(s), s
+
+
+def _with_device(t: torch.Tensor):
+    return torch.cuda.device(t.device)
+
+
+def reduce_norm(partials, residual, gamma_post, gamma_pre, eps: float, out=None,
+                debug: Optional[Debug] = None, stream=None) -> torch.Tensor:
+    """Rank-ordered FP32 sum of the shards, post-RMSNorm, residual add (in
+    place), pre-RMSNorm.  Returns ``out`` (BF16 [T,H])."""
+    L = load()
+    R, T, H = partials.shape
+    dev = partials.device
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    args = (_need(partials, "partials", torch.bfloat16, (R, T, H), dev), R, T, H,
+            _need(residual, "residual", torch.bfloat16, (T, H), dev),
+            _need(gamma_post, "gamma_post", torch.float32, (H,), dev),
+            _need(gamma_pre, "gamma_pre", torch.float32, (H,), dev), float(eps),
+            _need(out, "out", torch.bfloat16, (T, H), dev))
+    d = _debug(debug, R, T, H, dev, False)
+    with _with_device(partials):
+        _check(L.bn_reduce_norm(*args, d[0] if d else None, _stream(partials, stream)))
+    return out
+
+
+def finalize_reduce_norm(expert_out, perm, w, shared, residual, gamma_post, gamma_pre, eps: float,
+                         out=None, debug: Optional[Debug] = None, stream=None) -> torch.Tensor:
+    """Per-shard MoE top-k finalize (rounded to BF16), rank-ordered FP32 sum,
+    post-RMSNorm, residual add (in place), pre-RMSNorm.  Returns ``out``."""
+    L = load()
+    R, T, k = perm.shape
+    H = expert_out.shape[-1]
+    dev = expert_out.device
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    args = (_need(expert_out, "expert_out", torch.bfloat16, (R, T * k, H), dev),
+            _need(perm, "perm", torch.int32, (R, T, k), dev),
+            _need(w, "w", torch.float32, (R, T, k), dev),
+            _opt(shared, "shared", torch.bfloat16, (R, T, H), dev), R, T, k, H,
+            _need(residual, "residual", torch.bfloat16, (T, H), dev),
+            _need(gamma_post, "gamma_post", torch.float32, (H,), dev),
+            _need(gamma_pre, "gamma_pre", torch.float32, (H,), dev), float(eps),
+            _need(out, "out", torch.bfloat16, (T, H), dev))
+    d = _debug(debug, R, T, H, dev, True)
+    with _with_device(expert_out):
+        _check(L.bn_finalize_reduce_norm(*args, d[0] if d else None, _stream(expert_out, stream)))
+    return out
+
+
+def reduce_residual_norm(partials, residual, gamma, eps: float, out=None,
+                         debug: Optional[Debug] = None, stream=None) -> torch.Tensor:
+    """AllReduce + residual + RMSNorm (no post-norm)."""
+    L = load()
+    R, T, H = partials.shape
+    dev = partials.device
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    args = (_need(partials, "partials", torch.bfloat16, (R, T, H), dev), R, T, H,
+            _need(residual, "residual", torch.bfloat16, (T, H), dev),
+            _need(gamma, "gamma", torch.float32, (H,), dev), float(eps),
+            _need(out, "out", torch.bfloat16, (T, H), dev))
+    d = _debug(debug, R, T, H, dev, False)
+    with _with_device(partials):
+        _check(L.bn_reduce_residual_norm(*args, d[0] if d else None, _stream(partials, stream)))
+    return out
+
+
+def finalize_reduce_residual_norm(expert_out, perm, w, shared, residual, gamma, eps: float,
+                                  out=None, debug: Optional[Debug] = None,
+                                  stream=None) -> torch.Tensor:
+    """MoE finalize + shared-expert add + AllReduce + residual + RMSNorm."""
+    L = load()
+    R, T, k = perm.shape
+    H = expert_out.shape[-1]
+    dev = expert_out.device
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    args = (_need(expert_out, "expert_out", torch.bfloat16, (R, T * k, H), dev),
+            _need(perm, "perm", torch.int32, (R, T, k), dev),
+            _need(w, "w", torch.float32, (R, T, k), dev),
+            _opt(shared, "shared", torch.bfloat16, (R, T, H), dev), R, T, k, H,
+            _need(residual, "residual", torch.bfloat16, (T, H), dev),
+            _need(gamma, "gamma", torch.float32, (H,), dev), float(eps),
+            _need(out, "out", torch.bfloat16, (T, H), dev))
+    d = _debug(debug, R, T, H, dev, True)
+    with _with_device(expert_out):
+        _check(L.bn_finalize_reduce_residual_norm(*args, d[0] if d else None,
+                                                  _stream(expert_out, stream)))
+    return out
+
+
+def reduce_only(partials, sum_out=None, stream=None) -> torch.Tensor:
+    """Rank-ordered FP32 sum only (first half of the unfused split)."""
+    L = load()
+    R, T, H = partials.shape
+    dev = partials.device
+    if sum_out is None:
+        sum_out = torch.empty((T, H), dtype=torch.float32, device=dev)
+    with _with_device(partials):
+        _check(L.bn_reduce_only(_need(partials, "partials", torch.bfloat16, (R, T, H), dev), R, T, H,
+                                _need(sum_out, "sum_out", torch.float32, (T, H), dev),
+                                _stream(partials, stream)))
+    return sum_out
+
+
+def finalize_reduce_only(expert_out, perm, w, shared, sum_out=None, stream=None) -> torch.Tensor:
+    """Per-shard finalize rounded to BF16, then the rank-ordered FP32 sum only."""
+    L = load()
+    R, T, k = perm.shape
+    H = expert_out.shape[-1]
+    dev = expert_out.device
+    if sum_out is None:
+        sum_out = torch.empty((T, H), dtype=torch.float32, device=dev)
+    with _with_device(expert_out):
+        _check(L.bn_finalize_reduce_only(
+            _need(expert_out, "expert_out", torch.bfloat16, (R, T * k, H), dev),
+            _need(perm, "perm", torch.int32, (R, T, k), dev),
+            _need(w, "w", torch.float32, (R, T, k), dev),
+            _opt(shared, "shared", torch.bfloat16, (R, T, H), dev), R, T, k, H,
+            _need(sum_out, "sum_out", torch.float32, (T, H), dev), _stream(expert_out, stream)))
+    return sum_out
+
+
+def norm_only(sum_, residual, gamma_post, gamma_pre, eps: float, out=None,
+              debug: Optional[Debug] = None, stream=None) -> torch.Tensor:
+    """The sandwich epilogue given the FP32 sum [T,H] (second half of the split)."""
+    L = load()
+    T, H = sum_.shape
+    dev = sum_.device
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    args = (_need(sum_, "sum", torch.float32, (T, H), dev), T, H,
+            _need(residual, "residual", torch.bfloat16, (T, H), dev),
+            _need(gamma_post, "gamma_post", torch.float32, (H,), dev),
+            _need(gamma_pre, "gamma_pre", torch.float32, (H,), dev), float(eps),
+            _need(out, "out", torch.bfloat16, (T, H), dev))
+    d = _debug(debug, 1, T, H, dev, False)
+    with _with_device(sum_):
+        _check(L.bn_norm_only(*args, d[0] if d else None, _stream(sum_, stream)))
+    return out
+
+
+def finalize_only(expert_out, perm, w, shared, z_out=None, stream=None) -> torch.Tensor:
+    """The deferred finalize materialised: z [R,T,H] BF16 per shard, no reduction."""
+    L = load()
+    R, T, k = perm.shape
+    H = expert_out.shape[-1]
+    dev = expert_out.device
+    if z_out is None:
+        z_out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
+    with _with_device(expert_out):
+        _check(L.bn_finalize_only(
+            _need(expert_out, "expert_out", torch.bfloat16, (R, T * k, H), dev),
+            _need(perm, "perm", torch.int32, (R, T, k), dev),
+            _need(w, "w", torch.float32, (R, T, k), dev),
+            _opt(shared, "shared", torch.bfloat16, (R, T, H), dev), R, T, k, H,
+            _need(z_out, "z_out", torch.bfloat16, (R, T, H), dev), _stream(expert_out, stream)))
+    return z_out
+
+
+def supports(R: int, T: int, k: int, H: int) -> bool:
+    """True if the fused entry points serve this shape (k = 0: reduce entries)."""
+    return bool(load().bn_supports(int(R), int(T), int(k), int(H)))
+
+
+def check_device_error(stream=None, raise_on_error: bool = True) -> int:
+    """Synchronise ``stream``, read and clear the device error bits."""
+    L = load()
+    bits = ctypes.c_uint(0)
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    st = L.bn_check_device_error(int(stream.cuda_stream) if hasattr(stream, "cuda_stream")
+                                 else int(stream), ctypes.byref(bits))
+    if st not in (OK, ERR_DEVICE) or (raise_on_error and st != OK):
+        _check(st)
+    return int(bits.value)
+
+
+def set_tuning(cluster_size: int = 0, stages: int = 0, threads: int = 0) -> None:
+    """Override the launch shape for measurement sweeps (0 = automatic)."""
+    _check(load().bn_set_tuning(int(cluster_size), int(stages), int(threads)))
+
+
+def version() -> int:
+    return int(load().bn_version())

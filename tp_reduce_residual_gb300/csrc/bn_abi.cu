@@ -1,0 +1,664 @@
+// bn_abi.cu -- the C ABI of libbeamnorm: host-side validation, the choice of
+// launch shape, launches, and the device error word.
+//
+// Every entry point validates its arguments on the host before any CUDA call
+// and either enqueues exactly one kernel on the caller's stream or enqueues
+// nothing.  Declining a valid shape (BN_ERR_UNSUPPORTED) never does part of
+// the work: the caller falls back to an unfused path and owes the whole
+// reduction (sglang pull request 34134, description: a decline must not skip
+// the owed all-reduce).
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include <atomic>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/beamnorm.h"
+#include "bn_internal.h"
+
+// The device error word: one per device that loads the library.  Kernels
+// receive its address; they set bits with atomicOr and never trap.
+__device__ unsigned g_bn_device_error;
+
+namespace bn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kVersion = 10000;  // 1.0.0
+
+thread_local char g_msg[512] = "";
+
+bn_status fail(bn_status st, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+bn_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(BN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ---- tuning overrides (process-wide) -------------------------------------------
+
+std::atomic<int> g_tune_cluster{0}, g_tune_stages{0}, g_tune_threads{0};
+
+// ---- per-device state ------------------------------------------------------------
+
+struct DeviceInfo {
+    int sms = 0;
+    int smem_optin = 0;
+    unsigned *err = nullptr;  // address of g_bn_device_error on this device
+};
+
+std::once_flag g_dev_once[kMaxDevices];
+DeviceInfo g_dev[kMaxDevices];
+cudaError_t g_dev_status[kMaxDevices];
+
+bn_status device_info(const DeviceInfo **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(BN_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::call_once(g_dev_once[dev], [dev]() {
+        DeviceInfo &d = g_dev[dev];
+        cudaError_t st = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (st == cudaSuccess)
+            st = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (st == cudaSuccess)
+            st = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_bn_device_error);
+        g_dev_status[dev] = st;
+    });
+    if (g_dev_status[dev] != cudaSuccess) return cuda_fail(g_dev_status[dev], "device setup");
+    *out = &g_dev[dev];
+    return BN_OK;
+}
+
+// ---- validation helpers ----------------------------------------------------------
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Range {
+    const void *p;
+    size_t bytes;
+    const char *name;
+};
+
+bool overlaps(const Range &x, const Range &y)
+{
+    if (!x.p || !y.p || x.bytes == 0 || y.bytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(x.p), a1 = a0 + x.bytes;
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(y.p), b1 = b0 + y.bytes;
+    return a0 < b1 && b0 < a1;
+}
+
+// Each written range must not overlap any other range in the list (the
+// residual is read and written through one pointer, which is intended).
+bn_status check_overlaps(const Range *writes, int nw, const Range *reads, int nr)
+{
+    for (int i = 0; i < nw; ++i) {
+        for (int j = 0; j < nr; ++j)
+            if (overlaps(writes[i], reads[j]))
+                return fail(BN_ERR_INVALID, "%s overlaps %s", writes[i].name, reads[j].name);
+        for (int j = i + 1; j < nw; ++j)
+            if (overlaps(writes[i], writes[j]))
+                return fail(BN_ERR_INVALID, "%s overlaps %s", writes[i].name, writes[j].name);
+    }
+    return BN_OK;
+}
+
+bn_status check_shape(int R, int T, int k, int H, bool fin)
+{
+    if (R < 1 || R > kMaxR) return fail(BN_ERR_INVALID, "R=%d outside [1, %d]", R, kMaxR);
+    if (fin && (k < 1 || k > kMaxK)) return fail(BN_ERR_INVALID, "k=%d outside [1, %d]", k, kMaxK);
+    if (T < 0) return fail(BN_ERR_INVALID, "T=%d is negative", T);
+    if (H <= 0) return fail(BN_ERR_INVALID, "H=%d is not positive", H);
+    if (H % 8 != 0) return fail(BN_ERR_INVALID, "H=%d is not a multiple of 8", H);
+    return BN_OK;
+}
+
+bn_status check_served(int R, int T, int k, int H, bool fin)
+{
+    if (H > kMaxH) return fail(BN_ERR_UNSUPPORTED, "H=%d above the served maximum %d", H, kMaxH);
+    if (fin && R * k > kMaxMeta)
+        return fail(BN_ERR_UNSUPPORTED, "R*k=%d above the served maximum %d", R * k, kMaxMeta);
+    if (fin && (long long)T * k >= (1LL << 31))
+        return fail(BN_ERR_UNSUPPORTED, "T*k=%lld does not fit int32 row indices", (long long)T * k);
+    (void)R;
+    return BN_OK;
+}
+
+bn_status check_eps(float eps)
+{
+    if (!(eps >= 0.0f) || !std::isfinite(eps))
+        return fail(BN_ERR_INVALID, "eps must be finite and non-negative");
+    return BN_OK;
+}
+
+#define BN_REQUIRE(cond, ...)                                      \
+    do {                                                           \
+        if (!(cond)) return fail(BN_ERR_INVALID, __VA_ARGS__);     \
+    } while (0)
+#define BN_TRY(expr)                         \
+    do {                                     \
+        bn_status _st = (expr);              \
+        if (_st != BN_OK) return _st;        \
+    } while (0)
+
+bn_status check_ptr16(const void *p, const char *name, bool required = true)
+{
+    if (!p) {
+        if (required) return fail(BN_ERR_INVALID, "%s is NULL", name);
+        return BN_OK;
+    }
+    if (!aligned(p, 16)) return fail(BN_ERR_INVALID, "%s is not 16-byte aligned", name);
+    return BN_OK;
+}
+
+bn_status check_ptr4(const void *p, const char *name)
+{
+    if (!p) return fail(BN_ERR_INVALID, "%s is NULL", name);
+    if (!aligned(p, 4)) return fail(BN_ERR_INVALID, "%s is not 4-byte aligned", name);
+    return BN_OK;
+}
+
+// ---- launch shape ----------------------------------------------------------------
+
+using LaunchFn = cudaError_t (*)(const Args &, const Launch &, cudaStream_t);
+using OccFn = int (*)(const Launch &, cudaError_t *);
+
+struct ModeOps {
+    int mode;
+    LaunchFn launch;
+    OccFn occupancy;
+    const char *name;
+};
+
+const ModeOps kOps[] = {
+    {kModeReduceNorm, launch_reduce_norm, occupancy_reduce_norm, "reduce_norm"},
+    {kModeFinReduceNorm, launch_fin_reduce_norm, occupancy_fin_reduce_norm, "finalize_reduce_norm"},
+    {kModeReduceResNorm, launch_reduce_resnorm, occupancy_reduce_resnorm, "reduce_residual_norm"},
+    {kModeFinReduceResNorm, launch_fin_reduce_resnorm, occupancy_fin_reduce_resnorm,
+     "finalize_reduce_residual_norm"},
+    {kModeReduceOnly, launch_reduce_only, occupancy_reduce_only, "reduce_only"},
+    {kModeFinReduceOnly, launch_fin_reduce_only, occupancy_fin_reduce_only, "finalize_reduce_only"},
+    {kModeNormOnly, launch_norm_only, occupancy_norm_only, "norm_only"},
+    {kModeFinOnly, launch_fin_only, occupancy_fin_only, "finalize_only"},
+};
+
+const ModeOps &ops_for(int mode)
+{
+    for (const ModeOps &o : kOps)
+        if (o.mode == mode) return o;
+    return kOps[0];
+}
+
+// Occupancy answers are cached: (device, mode, shape) -> resident clusters.
+struct OccEntry {
+    int dev, mode, cluster, consumers, cpt;
+    size_t smem;
+    int clusters;
+};
+constexpr int kOccCache = 256;
+OccEntry g_occ[kOccCache];
+int g_occ_n = 0;
+std::mutex g_occ_mu;
+
+bn_status resident_clusters(int mode, const Launch &l, int *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    {
+        std::lock_guard<std::mutex> g(g_occ_mu);
+        for (int i = 0; i < g_occ_n; ++i) {
+            const OccEntry &o = g_occ[i];
+            if (o.dev == dev && o.mode == mode && o.cluster == l.cluster &&
+                o.consumers == l.consumers && o.cpt == l.cpt && o.smem == l.smem) {
+                *out = o.clusters;
+                return BN_OK;
+            }
+        }
+    }
+    int n = ops_for(mode).occupancy(l, &e);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // occupancy queries leave no sticky error; clear the last one
+        n = 0;
+    }
+    {
+        std::lock_guard<std::mutex> g(g_occ_mu);
+        if (g_occ_n < kOccCache) g_occ[g_occ_n++] = OccEntry{dev, mode, l.cluster, l.consumers, l.cpt, l.smem, n};
+    }
+    *out = n;
+    return BN_OK;
+}
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// CTAs per token row: split rows over a cluster while the rows alone would
+// leave SMs idle, keeping at least 32 chunks (one warp's worth) per CTA.
+int auto_cluster(int T, int nchunks, int sms)
+{
+    int cs = 1;
+    while (cs < kMaxCluster && (long long)T * cs < sms && nchunks / (cs * 2) >= 32) cs *= 2;
+    return cs;
+}
+
+bn_status plan(int mode, int T, int H, Launch *l, Args *a)
+{
+    const DeviceInfo *d = nullptr;
+    BN_TRY(device_info(&d));
+    const bool sum_in = (mode & F_SUM_IN) != 0;
+    const int nchunks = H / 8;
+    int cs = g_tune_cluster.load();
+    if (cs <= 0) cs = auto_cluster(T, nchunks, d->sms);
+    if (cs > nchunks) cs = 1;
+    const int cap = g_tune_threads.load() > 0 ? g_tune_threads.load() : kMaxConsumers;
+    const int want_stages = g_tune_stages.load();
+
+    for (;; cs /= 2) {
+        const int nch_max = (nchunks + cs - 1) / cs;
+        int cpt = 1;
+        while (cpt < 8 && (nch_max + cpt - 1) / cpt > cap) cpt *= 2;
+        const int consumers = round_up((nch_max + cpt - 1) / cpt, 32);
+        if (consumers > kMaxConsumers)
+            return fail(BN_ERR_UNSUPPORTED, "row of %d chunks needs %d consumer threads", nch_max, consumers);
+        const int stage_bytes = round_up(nch_max * 16 * (sum_in ? 2 : 1), 128);
+        // pipeline depth: ~144 KB in flight unless overridden, within the
+        // opt-in shared memory of one CTA
+        int stages = want_stages > 0 ? want_stages : (144 * 1024) / stage_bytes;
+        if (stages > kMaxStages) stages = kMaxStages;
+        if (stages < 2) stages = 2;
+        const int budget = d->smem_optin - 1024;  // room for the kernel's static shared memory
+        while (stages > 2 && (int)SmemLayout::make(stages, stage_bytes).total > budget) --stages;
+        if ((int)SmemLayout::make(stages, stage_bytes).total > budget)
+            return fail(BN_ERR_UNSUPPORTED, "stage of %d bytes does not fit shared memory", stage_bytes);
+
+        Launch L;
+        L.cluster = cs;
+        L.consumers = consumers;
+        L.cpt = cpt;
+        L.smem = SmemLayout::make(stages, stage_bytes).total;
+        int resident = 0;
+        BN_TRY(resident_clusters(mode, L, &resident));
+        if (resident <= 0) {
+            if (cs > 1) continue;  // this cluster size cannot be resident: halve it
+            return fail(BN_ERR_UNSUPPORTED, "no resident CTA for this shape");
+        }
+        const int ncl = T < resident ? T : resident;
+        L.grid = ncl * cs;
+        *l = L;
+        a->stages = stages;
+        a->stage_bytes = stage_bytes;
+        a->nchunks = nchunks;
+        a->err = d->err;
+        return BN_OK;
+    }
+}
+
+bn_status run(int mode, Args &a, void *stream)
+{
+    if (a.T == 0) return BN_OK;
+    Launch l;
+    BN_TRY(plan(mode, a.T, a.H, &l, &a));
+    cudaError_t e = ops_for(mode).launch(a, l, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, ops_for(mode).name);
+    return BN_OK;
+}
+
+Args base_args(int R, int T, int k, int H, float eps)
+{
+    Args a;
+    std::memset(&a, 0, sizeof a);
+    a.R = R;
+    a.T = T;
+    a.k = k;
+    a.H = H;
+    a.eps = eps;
+    return a;
+}
+
+void apply_debug(Args &a, const bn_debug *dbg)
+{
+    if (!dbg) return;
+    a.sum_out = dbg->sum;
+    a.ss_out = dbg->ss;
+    a.z_out = dbg->z;
+}
+
+bn_status check_debug(const bn_debug *dbg, bool fin)
+{
+    if (!dbg) return BN_OK;
+    BN_TRY(check_ptr16(dbg->sum, "dbg->sum", false));
+    BN_TRY(check_ptr16(dbg->ss, "dbg->ss", false));  // 8-byte pairs; 16 keeps one rule
+    if (fin) BN_TRY(check_ptr16(dbg->z, "dbg->z", false));
+    return BN_OK;
+}
+
+void debug_ranges(const bn_debug *dbg, int R, int T, int H, bool fin, Range *w, int *nw)
+{
+    if (!dbg) return;
+    const size_t th = (size_t)T * H;
+    if (dbg->sum) w[(*nw)++] = Range{dbg->sum, th * 4, "dbg->sum"};
+    if (dbg->ss) w[(*nw)++] = Range{dbg->ss, (size_t)T * 8, "dbg->ss"};
+    if (fin && dbg->z) w[(*nw)++] = Range{dbg->z, (size_t)R * th * 2, "dbg->z"};
+}
+
+// ---- shared validation of the two source kinds ------------------------------------
+
+bn_status check_reduce_sources(const uint16_t *partials, int R, int T, int H, Range *reads, int *nr)
+{
+    BN_TRY(check_ptr16(partials, "partials"));
+    reads[(*nr)++] = Range{partials, (size_t)R * T * H * 2, "partials"};
+    return BN_OK;
+}
+
+bn_status check_fin_sources(const uint16_t *expert_out, const int32_t *perm, const float *w,
+                            const uint16_t *shared, int R, int T, int k, int H, Range *reads, int *nr)
+{
+    BN_TRY(check_ptr16(expert_out, "expert_out"));
+    BN_TRY(check_ptr4(perm, "perm"));
+    BN_TRY(check_ptr4(w, "w"));
+    BN_TRY(check_ptr16(shared, "shared", false));
+    const size_t rtk = (size_t)R * T * k;
+    reads[(*nr)++] = Range{expert_out, rtk * H * 2, "expert_out"};
+    reads[(*nr)++] = Range{perm, rtk * 4, "perm"};
+    reads[(*nr)++] = Range{w, rtk * 4, "w"};
+    if (shared) reads[(*nr)++] = Range{shared, (size_t)R * T * H * 2, "shared"};
+    return BN_OK;
+}
+
+bn_status check_epilogue(uint16_t *residual, const float *gp, const float *gq, uint16_t *out,
+                         float eps, int T, int H, Range *reads, int *nr, Range *writes, int *nw)
+{
+    BN_TRY(check_ptr16(residual, "residual"));
+    BN_TRY(check_ptr16(gp, "gamma_post"));
+    BN_TRY(check_ptr16(gq, "gamma_pre"));
+    BN_TRY(check_ptr16(out, "out"));
+    BN_TRY(check_eps(eps));
+    const size_t th = (size_t)T * H;
+    reads[(*nr)++] = Range{gp, (size_t)H * 4, "gamma_post"};
+    if (gq != gp) reads[(*nr)++] = Range{gq, (size_t)H * 4, "gamma_pre"};
+    writes[(*nw)++] = Range{residual, th * 2, "residual"};
+    writes[(*nw)++] = Range{out, th * 2, "out"};
+    return BN_OK;
+}
+
+}  // namespace
+}  // namespace bn
+
+using namespace bn;
+
+// ================================ C ABI ===========================================
+
+extern "C" {
+
+bn_status bn_reduce_norm(const uint16_t *partials, int R, int T, int H, uint16_t *residual,
+                         const float *gamma_post, const float *gamma_pre, float eps, uint16_t *out,
+                         const bn_debug *dbg, void *stream)
+{
+    g_msg[0] = '\0';
+    BN_TRY(check_shape(R, T, 1, H, false));
+    Range reads[8], writes[8];
+    int nr = 0, nw = 0;
+    BN_TRY(check_reduce_sources(partials, R, T, H, reads, &nr));
+    BN_TRY(check_epilogue(residual, gamma_post, gamma_pre, out, eps, T, H, reads, &nr, writes, &nw));
+    BN_TRY(check_debug(dbg, false));
+    debug_ranges(dbg, R, T, H, false, writes, &nw);
+    BN_TRY(check_overlaps(writes, nw, reads, nr));
+    BN_TRY(check_served(R, T, 1, H, false));
+    Args a = base_args(R, T, 0, H, eps);
+    a.src = partials;
+    a.residual = residual;
+    a.gamma_post = gamma_post;
+    a.gamma_pre = gamma_pre;
+    a.out = out;
+    apply_debug(a, dbg);
+    return run(kModeReduceNorm, a, stream);
+}
+
+bn_status bn_finalize_reduce_norm(const uint16_t *expert_out, const int32_t *perm, const float *w,
+                                  const uint16_t *shared, int R, int T, int k, int H,
+                                  uint16_t *residual, const float *gamma_post,
+                                  const float *gamma_pre, float eps, uint16_t *out,
+                                  const bn_debug *dbg, void *stream)
+{
+    g_msg[0] = '\0';
+    BN_TRY(check_shape(R, T, k, H, true));
+    Range reads[8], writes[8];
+    int nr = 0, nw = 0;
+    BN_TRY(check_fin_sources(expert_out, perm, w, shared, R, T, k, H, reads, &nr));
+    BN_TRY(check_epilogue(residual, gamma_post, gamma_pre, out, eps, T, H, reads, &nr, writes, &nw));
+    BN_TRY(check_debug(dbg, true));
+    debug_ranges(dbg, R, T, H, true, writes, &nw);
+    BN_TRY(check_overlaps(writes, nw, reads, nr));
+    BN_TRY(check_served(R, T, k, H, true));
+    Args a = base_args(R, T, k, H, eps);
+    a.src = expert_out;
+    a.perm = perm;
+    a.w = w;
+    a.shared = shared;
+    a.residual = residual;
+    a.gamma_post = gamma_post;
+    a.gamma_pre = gamma_pre;
+    a.out = out;
+    apply_debug(a, dbg);
+    return run(kModeFinReduceNorm, a, stream);
+}
+
+bn_status bn_reduce_residual_norm(const uint16_t *partials, int R, int T, int H, uint16_t *residual,
+                                  const float *gamma, float eps, uint16_t *out, const bn_debug *dbg,
+                                  void *stream)
+{
+    g_msg[0] = '\0';
+    BN_TRY(check_shape(R, T, 1, H, false));
+    Range reads[8], writes[8];
+    int nr = 0, nw = 0;
+    BN_TRY(check_reduce_sources(partials, R, T, H, reads, &nr));
+    BN_TRY(check_epilogue(residual, gamma, gamma, out, eps, T, H, reads, &nr, writes, &nw));
+    BN_TRY(check_debug(dbg, false));
+    debug_ranges(dbg, R, T, H, false, writes, &nw);
+    BN_TRY(check_overlaps(writes, nw, reads, nr));
+    BN_TRY(check_served(R, T, 1, H, false));
+    Args a = base_args(R, T, 0, H, eps);
+    a.src = partials;
+    a.residual = residual;
+    a.gamma_post = gamma;
+    a.gamma_pre = gamma;
+    a.out = out;
+    apply_debug(a, dbg);
+    return run(kModeReduceResNorm, a, stream);
+}
+
+bn_status bn_finalize_reduce_residual_norm(const uint16_t *expert_out, const int32_t *perm,
+                                           const float *w, const uint16_t *shared, int R, int T,
+                                           int k, int H, uint16_t *residual, const float *gamma,
+                                           float eps, uint16_t *out, const bn_debug *dbg,
+                                           void *stream)
+{
+    g_msg[0] = '\0';
+    BN_TRY(check_shape(R, T, k, H, true));
+    Range reads[8], writes[8];
+    int nr = 0, nw = 0;
+    BN_TRY(check_fin_sources(expert_out, perm, w, shared, R, T, k, H, reads, &nr));
+    BN_TRY(check_epilogue(residual, gamma, gamma, out, eps, T, H, reads, &nr, writes, &nw));
+    BN_TRY(check_debug(dbg, true));
+    debug_ranges(dbg, R, T, H, true, writes, &nw);
+    BN_TRY(check_overlaps(writes, nw, reads, nr));
+    BN_TRY(check_served(R, T, k, H, true));
+    Args a = base_args(R, T, k, H, eps);
+    a.src = expert_out;
+    a.perm = perm;
+    a.w = w;
+    a.shared = shared;
+    a.residual = residual;
+    a.gamma_post = gamma;
+    a.gamma_pre = gamma;
+    a.out = out;
+    apply_debug(a, dbg);
+    return run(kModeFinReduceResNorm, a, stream);
+}
+
+bn_status bn_reduce_only(const uint16_t *partials, int R, int T, int H, float *sum_out, void *stream)
+{
+    g_msg[0] = '\0';
+    BN_TRY(check_shape(R, T, 1, H, false));
+    Range reads[4], writes[2];
+    int nr = 0, nw = 0;
+    BN_TRY(check_reduce_sources(partials, R, T, H, reads, &nr));
+    BN_TRY(check_ptr16(sum_out, "sum_out"));
+    writes[nw++] = Range{sum_out, (size_t)T * H * 4, "sum_out"};
+    BN_TRY(check_overlaps(writes, nw, reads, nr));
+    BN_TRY(check_served(R, T, 1, H, false));
+    Args a = base_args(R, T, 0, H, 0.f);
+    a.src = partials;
+    a.sum_out = sum_out;
+    return run(kModeReduceOnly, a, stream);
+}
+
+bn_status bn_finalize_reduce_only(const uint16_t *expert_out, const int32_t *perm, const float *w,
+                                  const uint16_t *shared, int R, int T, int k, int H, float *sum_out,
+                                  void *stream)
+{
+    g_msg[0] = '\0';
+    BN_TRY(check_shape(R, T, k, H, true));
+    Range reads[8], writes[2];
+    int nr = 0, nw = 0;
+    BN_TRY(check_fin_sources(expert_out, perm, w, shared, R, T, k, H, reads, &nr));
+    BN_TRY(check_ptr16(sum_out, "sum_out"));
+    writes[nw++] = Range{sum_out, (size_t)T * H * 4, "sum_out"};
+    BN_TRY(check_overlaps(writes, nw, reads, nr));
+    BN_TRY(check_served(R, T, k, H, true));
+    Args a = base_args(R, T, k, H, 0.f);
+    a.src = expert_out;
+    a.perm = perm;
+    a.w = w;
+    a.shared = shared;
+    a.sum_out = sum_out;
+    return run(kModeFinReduceOnly, a, stream);
+}
+
+bn_status bn_norm_only(const float *sum, int T, int H, uint16_t *residual, const float *gamma_post,
+                       const float *gamma_pre, float eps, uint16_t *out, const bn_debug *dbg,
+                       void *stream)
+{
+    g_msg[0] = '\0';
+    BN_TRY(check_shape(1, T, 1, H, false));
+    Range reads[8], writes[8];
+    int nr = 0, nw = 0;
+    BN_TRY(check_ptr16(sum, "sum"));
+    reads[nr++] = Range{sum, (size_t)T * H * 4, "sum"};
+    BN_TRY(check_epilogue(residual, gamma_post, gamma_pre, out, eps, T, H, reads, &nr, writes, &nw));
+    if (dbg && dbg->ss) {
+        BN_TRY(check_ptr16(dbg->ss, "dbg->ss"));
+        writes[nw++] = Range{dbg->ss, (size_t)T * 8, "dbg->ss"};
+    }
+    BN_TRY(check_overlaps(writes, nw, reads, nr));
+    BN_TRY(check_served(1, T, 1, H, false));
+    Args a = base_args(1, T, 0, H, eps);
+    a.sum_in = sum;
+    a.residual = residual;
+    a.gamma_post = gamma_post;
+    a.gamma_pre = gamma_pre;
+    a.out = out;
+    if (dbg) a.ss_out = dbg->ss;
+    return run(kModeNormOnly, a, stream);
+}
+
+bn_status bn_finalize_only(const uint16_t *expert_out, const int32_t *perm, const float *w,
+                           const uint16_t *shared, int R, int T, int k, int H, uint16_t *z_out,
+                           void *stream)
+{
+    g_msg[0] = '\0';
+    BN_TRY(check_shape(R, T, k, H, true));
+    Range reads[8], writes[2];
+    int nr = 0, nw = 0;
+    BN_TRY(check_fin_sources(expert_out, perm, w, shared, R, T, k, H, reads, &nr));
+    BN_TRY(check_ptr16(z_out, "z_out"));
+    writes[nw++] = Range{z_out, (size_t)R * T * H * 2, "z_out"};
+    BN_TRY(check_overlaps(writes, nw, reads, nr));
+    BN_TRY(check_served(R, T, k, H, true));
+    Args a = base_args(R, T, k, H, 0.f);
+    a.src = expert_out;
+    a.perm = perm;
+    a.w = w;
+    a.shared = shared;
+    a.z_out = z_out;
+    return run(kModeFinOnly, a, stream);
+}
+
+int bn_supports(int R, int T, int k, int H)
+{
+    const bool fin = k > 0;
+    if (check_shape(R, T, fin ? k : 1, H, fin) != BN_OK) return 0;
+    if (check_served(R, T, fin ? k : 1, H, fin) != BN_OK) return 0;
+    g_msg[0] = '\0';
+    return 1;
+}
+
+bn_status bn_check_device_error(void *stream, unsigned *bits)
+{
+    g_msg[0] = '\0';
+    if (bits) *bits = 0;
+    const DeviceInfo *d = nullptr;
+    BN_TRY(device_info(&d));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned v = 0;
+    e = cudaMemcpy(&v, d->err, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (v != 0) {
+        const unsigned zero = 0;
+        e = cudaMemcpy(d->err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+    }
+    if (bits) *bits = v;
+    if (v != 0)
+        return fail(BN_ERR_DEVICE, "device error bits 0x%x%s%s", v,
+                    (v & BN_DEVERR_PERM_RANGE) ? " (perm index out of range)" : "",
+                    (v & BN_DEVERR_TIMEOUT) ? " (pipeline wait timed out)" : "");
+    return BN_OK;
+}
+
+const char *bn_last_error(void) { return g_msg; }
+
+const char *bn_status_string(bn_status status)
+{
+    switch (status) {
+    case BN_OK: return "BN_OK";
+    case BN_ERR_INVALID: return "BN_ERR_INVALID";
+    case BN_ERR_UNSUPPORTED: return "BN_ERR_UNSUPPORTED";
+    case BN_ERR_CUDA: return "BN_ERR_CUDA";
+    case BN_ERR_DEVICE: return "BN_ERR_DEVICE";
+    }
+    return "unknown status";
+}
+
+int bn_version(void) { return kVersion; }
+
+bn_status bn_set_tuning(int cluster_size, int stages, int threads)
+{
+    g_msg[0] = '\0';
+    if (cluster_size != 0 && cluster_size != 1 && cluster_size != 2 && cluster_size != 4 &&
+        cluster_size != 8 && cluster_size != 16)
+        return fail(BN_ERR_INVALID, "cluster_size must be 0, 1, 2, 4, 8 or 16");
+    if (stages < 0 || stages > kMaxStages || stages == 1)
+        return fail(BN_ERR_INVALID, "stages must be 0 or in [2, %d]", kMaxStages);
+    if (threads < 0 || threads > kMaxConsumers || threads % 32 != 0)
+        return fail(BN_ERR_INVALID, "threads must be 0 or a multiple of 32 up to %d", kMaxConsumers);
+    g_tune_cluster.store(cluster_size);
+    g_tune_stages.store(stages);
+    g_tune_threads.store(threads);
+    return BN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,702 @@
+// bn_device.cuh -- the one kernel template of libbeamnorm (sm_103a).
+//
+// Operation: the arithmetic epilogue of a fused tensor-parallel all-reduce
+// ("Fuse Beam's TP all-reduce with its sandwich norms", vLLM pull request
+// 62366, "Claims": FP32 norm-residual-norm epilogue, optional MoE finalize
+// before the reduction keeping the local BF16 rounding; "Details": no FMA
+// contraction of the FP32 epilogue, so this file is compiled with
+// -fmad=false), and its variants from sglang pull request 34134 (description:
+// "AllReduce + residual + RMSNorm" and "MoE finalize + shared-expert add +
+// AllReduce + residual + RMSNorm").
+//
+// Design (GB300):
+//   * One token row is owned by one CTA, or by a thread-block cluster of up to
+//     16 CTAs that split the row into contiguous 16-byte-chunk slices (small T,
+//     so that many SMs pull one row).  Clusters are persistent and grid-stride
+//     over rows.
+//   * A producer warp streams every row the CTA needs (R shard rows, or R*k
+//     gathered expert rows plus R shared rows, then the residual row) from HBM
+//     into a ring of shared-memory stages with 1-D TMA bulk copies
+//     (cp.async.bulk, completion counted on an mbarrier).  The ring keeps
+//     ~100-200 KB in flight per SM and runs ahead across row boundaries, so the
+//     two row-wide reductions of one row overlap the loads of the next.
+//   * Consumer warps own 16-byte chunks of the slice, read them from shared
+//     memory, and do all arithmetic in registers: exact BF16 widening, the
+//     rank-ordered FP32 sum, the per-shard finalize, both RMSNorms, and 16-byte
+//     coalesced stores of the BF16 outputs.
+//   * A sum of squares is accumulated as a compensated pair (exact products via
+//     one explicit fma for the error term, two-sum for the additions), combined
+//     in a fixed warp/block/cluster tree, and rounded once: the result is the
+//     FP32 rounding of the exact sum, independent of the row's split.
+//   * Cluster partial sums travel through distributed shared memory (remote
+//     st.shared::cluster plus a remote mbarrier arrive) -- no global scratch.
+//   * Every wait is bounded in time; on expiry the kernel records an error bit,
+//     stops issuing copies, drains the copies it has in flight, runs the rest of
+//     its control flow without waiting and without storing, and returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "bn_internal.h"
+
+namespace bn {
+namespace dev {
+
+constexpr unsigned long long kWaitLimitNs = 250ull * 1000ull * 1000ull;  // 250 ms
+constexpr uint32_t kMaxSpins = 1u << 26;
+constexpr unsigned kErrPerm = 1u;
+constexpr unsigned kErrTimeout = 2u;
+
+// ---- PTX wrappers -------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t ncluster_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Acquire at cluster scope: pairs with the remote release-arrive of the
+// partial-sum exchange.
+__device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f2(uint32_t addr, float x, float y)
+{
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(x), "f"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_remote_arrive(uint32_t bar_cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                     bar_cluster_addr)
+                 : "memory");
+}
+// 1-D TMA bulk copy global -> this CTA's shared memory, completion counted in
+// bytes on the mbarrier.  dst, src and bytes are multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ void fence_mbarrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// Named barrier among the consumer warps only (the producer warp runs free).
+__device__ __forceinline__ void consumer_sync(int nthreads)
+{
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// ---- bounded waits --------------------------------------------------------------
+
+struct Ctl {
+    volatile int *abort;  // shared flag: set once any wait of this CTA expired
+    unsigned *err;        // device error word
+};
+
+// Wait for the phase of `bar` with parity `parity` to complete.  Returns false
+// (without waiting) once the CTA is aborting, or after the time limit, in
+// which case it records the timeout and starts the abort.
+template <bool CLUSTER_ACQUIRE, bool HONOR_ABORT>
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl &c)
+{
+    if (HONOR_ABORT && *c.abort) return false;
+    if (CLUSTER_ACQUIRE ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1; i < kMaxSpins; ++i) {
+        if (CLUSTER_ACQUIRE ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
+        if ((i & 15u) == 0u) {
+            if (HONOR_ABORT && *c.abort) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) break;
+        }
+    }
+    atomicOr(c.err, kErrTimeout);
+    *c.abort = 1;
+    return false;
+}
+
+// ---- arithmetic helpers ----------------------------------------------------------
+
+// Exact widening of eight BF16 values packed in 16 bytes (element 2i is the low
+// half of word i).
+__device__ __forceinline__ void unpack8(const uint4 &v, float *f)
+{
+    f[0] = __uint_as_float(v.x << 16);
+    f[1] = __uint_as_float(v.x & 0xffff0000u);
+    f[2] = __uint_as_float(v.y << 16);
+    f[3] = __uint_as_float(v.y & 0xffff0000u);
+    f[4] = __uint_as_float(v.z << 16);
+    f[5] = __uint_as_float(v.z & 0xffff0000u);
+    f[6] = __uint_as_float(v.w << 16);
+    f[7] = __uint_as_float(v.w & 0xffff0000u);
+}
+
+// Round two FP32 values to BF16 (nearest even) and pack them, lo in the low half.
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&b);
+}
+
+__device__ __forceinline__ uint4 pack8(const float *f)
+{
+    return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+}
+
+// s + e == a + b exactly (Knuth's two-sum; no ordering assumption).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
+{
+    s = a + b;
+    const float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+// (S, E) += x*x with the product's rounding error and the addition's error
+// both carried in E.  The explicit fma only computes the exact error of the
+// rounded product; no result value is contracted.
+__device__ __forceinline__ void acc_square(float &S, float &E, float x)
+{
+    const float p = x * x;
+    const float pe = __fmaf_rn(x, x, -p);
+    float s, e;
+    two_sum(S, p, s, e);
+    S = s;
+    E = E + (e + pe);
+}
+
+__device__ __forceinline__ void combine(float &S, float &E, float S2, float E2)
+{
+    float s, e;
+    two_sum(S, S2, s, e);
+    S = s;
+    E = (E + E2) + e;
+}
+
+__device__ __forceinline__ void warp_tree(float &S, float &E)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float S2 = __shfl_down_sync(0xffffffffu, S, off);
+        const float E2 = __shfl_down_sync(0xffffffffu, E, off);
+        combine(S, E, S2, E2);
+    }
+}
+
+// 1 / sqrt(ss / H + eps): three correctly rounded FP32 operations
+// (-prec-div and -prec-sqrt are left at their IEEE defaults).
+__device__ __forceinline__ float rms_factor(float ss, int H, float eps)
+{
+    const float mean = ss / (float)H;
+    return 1.0f / sqrtf(mean + eps);
+}
+
+// ---- the kernel ------------------------------------------------------------------
+
+struct Smem {
+    uint8_t *stages;
+    uint32_t stages_u32;
+    uint32_t full0, empty0, mfull0, mempty0, ex0;  // mbarrier addresses (8 bytes apart)
+    float2 *red;                                   // [2][32]
+    float2 *xslot;                                 // [2][kMaxCluster]
+    int32_t *mperm;                                // [2][kMaxMeta]
+    float *mw;                                     // [2][kMaxMeta]
+};
+
+// Row-wide sum of squares: compensated pairs reduced over the warp, the
+// consumer warps of the CTA, then the CTAs of the cluster, in a fixed order;
+// every consumer thread of every CTA of the cluster gets the same value.
+__device__ __forceinline__ float row_sum_squares(float S, float E, int &nred, const Smem &sm,
+                                                 uint32_t cs, uint32_t q, int NT, int NW,
+                                                 int warp, int lane, int tid, const Ctl &ctl,
+                                                 bool &live)
+{
+    warp_tree(S, E);
+    const int b = nred & 1;
+    if (lane == 0) sm.red[b * 32 + warp] = make_float2(S, E);
+    consumer_sync(NT);
+    const float2 v = (lane < NW) ? sm.red[b * 32 + lane] : make_float2(0.f, 0.f);
+    S = v.x;
+    E = v.y;
+    warp_tree(S, E);
+    S = __shfl_sync(0xffffffffu, S, 0);
+    E = __shfl_sync(0xffffffffu, E, 0);
+    if (cs > 1) {
+        float2 *slots = sm.xslot + b * kMaxCluster;
+        const uint32_t bar = sm.ex0 + 8u * (uint32_t)b;
+        if (tid == 0) {
+            const uint32_t mine = smem_addr(slots + q);
+            for (uint32_t d = 0; d < cs; ++d) {
+                st_cluster_f2(mapa(mine, d), S, E);
+                mbar_remote_arrive(mapa(bar, d));
+            }
+        }
+        if (!wait_phase<true, true>(bar, (uint32_t)(nred >> 1) & 1u, ctl)) live = false;
+        S = slots[0].x;
+        E = slots[0].y;
+        for (uint32_t c = 1; c < cs; ++c) combine(S, E, slots[c].x, slots[c].y);
+    }
+    ++nred;
+    return S + E;
+}
+
+template <int MODE, int CPT>
+__global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
+{
+    constexpr bool FIN = (MODE & F_FIN) != 0;
+    constexpr bool SUM_IN = (MODE & F_SUM_IN) != 0;
+    constexpr bool POSTNORM = (MODE & F_POSTNORM) != 0;
+    constexpr bool RESNORM = (MODE & F_RESNORM) != 0;
+    constexpr bool SUM_OUT = (MODE & F_SUM_OUT) != 0;
+    constexpr bool Z_OUT = (MODE & F_Z_OUT) != 0;
+    constexpr bool REDUCE = !Z_OUT;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int s_abort;
+
+    const SmemLayout L = SmemLayout::make(a.stages, a.stage_bytes);
+    Smem sm;
+    sm.stages = smem + L.stages_off;
+    sm.stages_u32 = smem_addr(sm.stages);
+    sm.full0 = smem_addr(smem + L.bars_off);
+    sm.empty0 = sm.full0 + 8u * (uint32_t)a.stages;
+    sm.mfull0 = sm.empty0 + 8u * (uint32_t)a.stages;
+    sm.mempty0 = sm.mfull0 + 16u;
+    sm.ex0 = sm.mempty0 + 16u;
+    sm.red = reinterpret_cast<float2 *>(smem + L.red_off);
+    sm.xslot = reinterpret_cast<float2 *>(smem + L.xslot_off);
+    sm.mperm = reinterpret_cast<int32_t *>(smem + L.meta_off);
+    sm.mw = reinterpret_cast<float *>(smem + L.meta_off + 2u * kMaxMeta * 4u);
+
+    const int NT = (int)blockDim.x - 32;  // consumer threads
+    const int NW = NT >> 5;
+    const int tid = (int)threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const uint32_t cs = cluster_nctarank();
+    const uint32_t q = cluster_ctarank();
+    const int cl = (int)cluster_id_x();
+    const int ncl = (int)ncluster_x();
+    // this CTA's slice of the row: chunks [c0, c0 + nch)
+    const int c0 = (int)(((long long)q * a.nchunks) / (long long)cs);
+    const int nch = (int)(((long long)(q + 1) * a.nchunks) / (long long)cs) - c0;
+    const int S = a.stages;
+    const size_t H = (size_t)a.H;
+    const bool has_shared = FIN && a.shared != nullptr;
+
+    if (tid == 0) {
+        s_abort = 0;
+        for (int i = 0; i < S; ++i) {
+            mbar_init(sm.full0 + 8u * i, 1u);
+            mbar_init(sm.empty0 + 8u * i, (uint32_t)NW);
+        }
+        mbar_init(sm.mfull0, 32u);
+        mbar_init(sm.mfull0 + 8u, 32u);
+        mbar_init(sm.mempty0, (uint32_t)NW);
+        mbar_init(sm.mempty0 + 8u, (uint32_t)NW);
+        mbar_init(sm.ex0, cs);
+        mbar_init(sm.ex0 + 8u, cs);
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    if (cs > 1) cluster_sync_all();
+    const Ctl ctl{&s_abort, a.err};
+
+    if (warp == NW) {
+        // ================= producer warp =================
+        uint32_t stage = 0, phase = 0, issued = 0;
+        bool ok = true;
+        for (int t = cl, it = 0; t < a.T && ok; t += ncl, ++it) {
+            const int slot = it & 1;
+            if constexpr (FIN) {
+                // stage this row's gather indices and weights (all lanes)
+                bool got = true;
+                if (lane == 0)
+                    got = wait_phase<false, true>(sm.mempty0 + 8u * slot,
+                                                  (((uint32_t)it >> 1) & 1u) ^ 1u, ctl);
+                got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                const int nm = a.R * a.k;
+                const long long lim = (long long)a.T * a.k;
+                for (int i = lane; i < nm; i += 32) {
+                    const int r = i / a.k;
+                    const int j = i - r * a.k;
+                    const size_t mi = ((size_t)r * a.T + t) * a.k + j;
+                    int p = __ldg(a.perm + mi);
+                    if (p < 0 || (long long)p >= lim) {
+                        atomicOr(a.err, kErrPerm);
+                        p = 0;
+                    }
+                    sm.mperm[slot * kMaxMeta + i] = p;
+                    sm.mw[slot * kMaxMeta + i] = __ldg(a.w + mi);
+                }
+                mbar_arrive(sm.mfull0 + 8u * slot);
+                __syncwarp();
+            }
+            if (lane == 0) {
+                auto issue = [&](const void *src, uint32_t bytes) -> bool {
+                    if (!wait_phase<false, true>(sm.empty0 + 8u * stage, phase ^ 1u, ctl)) return false;
+                    const uint32_t fb = sm.full0 + 8u * stage;
+                    mbar_arrive_expect_tx(fb, bytes);
+                    bulk_g2s(sm.stages_u32 + stage * (uint32_t)a.stage_bytes, src, bytes, fb);
+                    ++issued;
+                    if (++stage == (uint32_t)S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    return true;
+                };
+                const uint32_t bytes16 = (uint32_t)nch * 16u;
+                const size_t col = (size_t)c0 * 8u;
+                if constexpr (SUM_IN) {
+                    ok = issue(a.sum_in + (size_t)t * H + col, bytes16 * 2u);
+                } else if constexpr (FIN) {
+                    const int32_t *mp = sm.mperm + slot * kMaxMeta;
+                    for (int r = 0; r < a.R && ok; ++r) {
+                        const uint16_t *xr = a.src + (size_t)r * a.T * a.k * H;
+                        for (int j = 0; j < a.k && ok; ++j)
+                            ok = issue(xr + (size_t)mp[r * a.k + j] * H + col, bytes16);
+                        if (ok && has_shared)
+                            ok = issue(a.shared + ((size_t)r * a.T + t) * H + col, bytes16);
+                    }
+                } else {
+                    for (int r = 0; r < a.R && ok; ++r)
+                        ok = issue(a.src + ((size_t)r * a.T + t) * H + col, bytes16);
+                }
+                if constexpr (RESNORM) {
+                    if (ok) ok = issue(a.residual + (size_t)t * H + col, bytes16);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        }
+        // drain: wait (bounded, even when aborting) for every copy still in flight
+        if (lane == 0) {
+            const uint32_t n = issued < (uint32_t)S ? issued : (uint32_t)S;
+            uint32_t st = stage, ph = phase;
+            for (uint32_t i = 0; i < n; ++i) {
+                if (st == 0) {
+                    st = (uint32_t)S - 1u;
+                    ph ^= 1u;
+                } else {
+                    --st;
+                }
+                wait_phase<false, false>(sm.full0 + 8u * st, ph, ctl);
+            }
+        }
+    } else {
+        // ================= consumer warps =================
+        uint32_t stage = 0, phase = 0;
+        int nred = 0;
+        bool live = true;  // false once a wait failed: keep the control flow, store nothing
+        auto take = [&]() -> const uint8_t * {
+            if (!wait_phase<false, true>(sm.full0 + 8u * stage, phase, ctl)) live = false;
+            return sm.stages + (size_t)stage * (size_t)a.stage_bytes;
+        };
+        auto release = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.empty0 + 8u * stage);
+            if (++stage == (uint32_t)S) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        };
+
+        for (int t = cl, it = 0; t < a.T; t += ncl, ++it) {
+            const int slot = it & 1;
+            float s[CPT][8];
+#pragma unroll
+            for (int i = 0; i < CPT; ++i)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s[i][e] = 0.f;
+
+            // ---- the reduced sum s (or the per-shard finalize results) ----
+            if constexpr (SUM_IN) {
+                const uint8_t *p = take();
+#pragma unroll
+                for (int i = 0; i < CPT; ++i) {
+                    const int lc = tid + i * NT;
+                    if (lc < nch) {
+                        const float4 u = *reinterpret_cast<const float4 *>(p + (size_t)lc * 32);
+                        const float4 v = *reinterpret_cast<const float4 *>(p + (size_t)lc * 32 + 16);
+                        s[i][0] = u.x; s[i][1] = u.y; s[i][2] = u.z; s[i][3] = u.w;
+                        s[i][4] = v.x; s[i][5] = v.y; s[i][6] = v.z; s[i][7] = v.w;
+                    }
+                }
+                release();
+            } else if constexpr (FIN) {
+                if (!wait_phase<false, true>(sm.mfull0 + 8u * slot, ((uint32_t)it >> 1) & 1u, ctl))
+                    live = false;
+                const float *wrow = sm.mw + slot * kMaxMeta;
+                for (int r = 0; r < a.R; ++r) {
+                    float acc[CPT][8];
+                    // slot 0: acc = w0 * x0
+                    {
+                        const float w0 = wrow[r * a.k];
+                        const uint8_t *p = take();
+#pragma unroll
+                        for (int i = 0; i < CPT; ++i) {
+                            const int lc = tid + i * NT;
+                            float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                            if (lc < nch) unpack8(*reinterpret_cast<const uint4 *>(p + (size_t)lc * 16), x);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[i][e] = w0 * x[e];
+                        }
+                        release();
+                    }
+                    // slots 1..k-1: acc = acc + wj * xj
+                    for (int j = 1; j < a.k; ++j) {
+                        const float wj = wrow[r * a.k + j];
+                        const uint8_t *p = take();
+#pragma unroll
+                        for (int i = 0; i < CPT; ++i) {
+                            const int lc = tid + i * NT;
+                            if (lc < nch) {
+                                float x[8];
+                                unpack8(*reinterpret_cast<const uint4 *>(p + (size_t)lc * 16), x);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) acc[i][e] = acc[i][e] + wj * x[e];
+                            }
+                        }
+                        release();
+                    }
+                    // shared-expert add
+                    if (has_shared) {
+                        const uint8_t *p = take();
+#pragma unroll
+                        for (int i = 0; i < CPT; ++i) {
+                            const int lc = tid + i * NT;
+                            if (lc < nch) {
+                                float x[8];
+                                unpack8(*reinterpret_cast<const uint4 *>(p + (size_t)lc * 16), x);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) acc[i][e] = acc[i][e] + x[e];
+                            }
+                        }
+                        release();
+                    }
+                    // local BF16 rounding, then the rank-ordered sum
+#pragma unroll
+                    for (int i = 0; i < CPT; ++i) {
+                        const int lc = tid + i * NT;
+                        if (lc < nch) {
+                            const uint4 z = pack8(acc[i]);
+                            if ((Z_OUT || a.z_out != nullptr) && live)
+                                *reinterpret_cast<uint4 *>(a.z_out + ((size_t)r * a.T + t) * H +
+                                                           (size_t)(c0 + lc) * 8) = z;
+                            if constexpr (REDUCE) {
+                                float zf[8];
+                                unpack8(z, zf);
+                                if (r == 0) {
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) s[i][e] = zf[e];
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) s[i][e] = s[i][e] + zf[e];
+                                }
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sm.mempty0 + 8u * slot);
+            } else {
+                for (int r = 0; r < a.R; ++r) {
+                    const uint8_t *p = take();
+#pragma unroll
+                    for (int i = 0; i < CPT; ++i) {
+                        const int lc = tid + i * NT;
+                        if (lc < nch) {
+                            float x[8];
+                            unpack8(*reinterpret_cast<const uint4 *>(p + (size_t)lc * 16), x);
+                            if (r == 0) {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) s[i][e] = x[e];
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) s[i][e] = s[i][e] + x[e];
+                            }
+                        }
+                    }
+                    release();
+                }
+            }
+
+            // ---- FP32 sum out (split path) or debug copy ----
+            if constexpr (REDUCE && !SUM_IN) {
+                if ((SUM_OUT || a.sum_out != nullptr) && live) {
+#pragma unroll
+                    for (int i = 0; i < CPT; ++i) {
+                        const int lc = tid + i * NT;
+                        if (lc < nch) {
+                            float4 *dst = reinterpret_cast<float4 *>(a.sum_out + (size_t)t * H +
+                                                                     (size_t)(c0 + lc) * 8);
+                            dst[0] = make_float4(s[i][0], s[i][1], s[i][2], s[i][3]);
+                            dst[1] = make_float4(s[i][4], s[i][5], s[i][6], s[i][7]);
+                        }
+                    }
+                }
+            }
+
+            // ---- norm-residual-norm ----
+            if constexpr (RESNORM) {
+                float ss1 = 0.f;
+                if constexpr (POSTNORM) {
+                    float S1 = 0.f, E1 = 0.f;
+#pragma unroll
+                    for (int i = 0; i < CPT; ++i) {
+                        const int lc = tid + i * NT;
+                        if (lc < nch) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc_square(S1, E1, s[i][e]);
+                        }
+                    }
+                    ss1 = row_sum_squares(S1, E1, nred, sm, cs, q, NT, NW, warp, lane, tid, ctl, live);
+                    const float r1 = rms_factor(ss1, a.H, a.eps);
+#pragma unroll
+                    for (int i = 0; i < CPT; ++i) {
+                        const int lc = tid + i * NT;
+                        if (lc < nch) {
+                            const float4 *g = reinterpret_cast<const float4 *>(a.gamma_post +
+                                                                               (size_t)(c0 + lc) * 8);
+                            const float4 g0 = __ldg(g), g1 = __ldg(g + 1);
+                            const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) s[i][e] = (s[i][e] * r1) * gg[e];
+                        }
+                    }
+                }
+                // residual add and write-back (s now holds y, or the sum itself)
+                float S2 = 0.f, E2 = 0.f;
+                {
+                    const uint8_t *p = take();
+#pragma unroll
+                    for (int i = 0; i < CPT; ++i) {
+                        const int lc = tid + i * NT;
+                        if (lc < nch) {
+                            float rf[8];
+                            unpack8(*reinterpret_cast<const uint4 *>(p + (size_t)lc * 16), rf);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                s[i][e] = rf[e] + s[i][e];
+                                acc_square(S2, E2, s[i][e]);
+                            }
+                            if (live)
+                                *reinterpret_cast<uint4 *>(a.residual + (size_t)t * H +
+                                                           (size_t)(c0 + lc) * 8) = pack8(s[i]);
+                        }
+                    }
+                    release();
+                }
+                const float ss2 = row_sum_squares(S2, E2, nred, sm, cs, q, NT, NW, warp, lane, tid, ctl, live);
+                const float r2 = rms_factor(ss2, a.H, a.eps);
+#pragma unroll
+                for (int i = 0; i < CPT; ++i) {
+                    const int lc = tid + i * NT;
+                    if (lc < nch) {
+                        const float4 *g = reinterpret_cast<const float4 *>(a.gamma_pre +
+                                                                           (size_t)(c0 + lc) * 8);
+                        const float4 g0 = __ldg(g), g1 = __ldg(g + 1);
+                        const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                        float o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[e] = (s[i][e] * r2) * gg[e];
+                        if (live)
+                            *reinterpret_cast<uint4 *>(a.out + (size_t)t * H + (size_t)(c0 + lc) * 8) =
+                                pack8(o);
+                    }
+                }
+                if (a.ss_out != nullptr && q == 0 && tid == 0 && live) {
+                    a.ss_out[2 * (size_t)t] = ss1;
+                    a.ss_out[2 * (size_t)t + 1] = ss2;
+                }
+            }
+        }
+    }
+    if (cs > 1) cluster_sync_all();
+}
+
+}  // namespace dev
+}  // namespace bn

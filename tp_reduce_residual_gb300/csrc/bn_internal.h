@@ -1,0 +1,104 @@
+// bn_internal.h -- shared between the C-ABI translation unit and the kernel
+// translation units of libbeamnorm (not installed, not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace bn {
+
+// Mode bits of the one kernel template.  Each served entry point is one mode.
+enum : int {
+    F_FIN = 1,        // sources are gathered expert rows, finalized per shard
+    F_SUM_IN = 2,     // the source is one FP32 reduced-sum row (epilogue only)
+    F_POSTNORM = 4,   // post-RMSNorm of the reduced sum before the residual add
+    F_RESNORM = 8,    // residual add, residual write-back, pre-RMSNorm -> out
+    F_SUM_OUT = 16,   // write the FP32 reduced sum (first half of the split)
+    F_Z_OUT = 32,     // write the per-shard BF16 finalize results only
+};
+
+constexpr int kModeReduceNorm = F_POSTNORM | F_RESNORM;
+constexpr int kModeFinReduceNorm = F_FIN | F_POSTNORM | F_RESNORM;
+constexpr int kModeReduceResNorm = F_RESNORM;
+constexpr int kModeFinReduceResNorm = F_FIN | F_RESNORM;
+constexpr int kModeReduceOnly = F_SUM_OUT;
+constexpr int kModeFinReduceOnly = F_FIN | F_SUM_OUT;
+constexpr int kModeNormOnly = F_SUM_IN | F_POSTNORM | F_RESNORM;
+constexpr int kModeFinOnly = F_FIN | F_Z_OUT;
+
+constexpr int kMaxR = 16;
+constexpr int kMaxK = 16;
+constexpr int kMaxMeta = 256;        // R * k slots staged per token row
+constexpr int kMaxH = 32768;
+constexpr int kMaxConsumers = 512;   // consumer threads per CTA
+constexpr int kMaxStages = 64;
+constexpr int kMaxCluster = 16;
+
+// Kernel arguments (passed by value).
+struct Args {
+    const uint16_t *src;      // partials [R,T,H] or expert_out [R,T*k,H]
+    const float *sum_in;      // [T,H] FP32 (F_SUM_IN)
+    const int32_t *perm;      // [R,T,k]
+    const float *w;           // [R,T,k]
+    const uint16_t *shared;   // [R,T,H] or null
+    uint16_t *residual;       // [T,H] read, then written
+    const float *gamma_post;  // [H]
+    const float *gamma_pre;   // [H]
+    uint16_t *out;            // [T,H]
+    float *sum_out;           // [T,H] (F_SUM_OUT, or debug)
+    float *ss_out;            // [T,2] debug
+    uint16_t *z_out;          // [R,T,H] (F_Z_OUT, or debug)
+    unsigned *err;            // device error word
+    int R, T, H, k;
+    int nchunks;              // H / 8 sixteen-byte chunks per row
+    int stages;               // pipeline depth
+    int stage_bytes;          // bytes of one stage (multiple of 128)
+    float eps;
+};
+
+// Launch shape chosen on the host.
+struct Launch {
+    int cluster;     // CTAs per token row (thread-block cluster size)
+    int consumers;   // consumer threads per CTA (multiple of 32)
+    int cpt;         // 16-byte chunks per consumer thread: 1, 2, 4 or 8
+    int grid;        // CTAs (a multiple of cluster)
+    size_t smem;     // dynamic shared memory bytes
+};
+
+// Dynamic shared-memory layout, identical on host and device.
+struct SmemLayout {
+    uint32_t stages_off, bars_off, red_off, xslot_off, meta_off, total;
+    __host__ __device__ static SmemLayout make(int stages, int stage_bytes) {
+        SmemLayout L;
+        L.stages_off = 0;
+        L.bars_off = (uint32_t)stages * (uint32_t)stage_bytes;            // 128-aligned
+        uint32_t nbars = 2u * (uint32_t)stages + 6u;                      // full, empty, meta x2 x2, exchange x2
+        L.red_off = L.bars_off + ((nbars * 8u + 15u) & ~15u);
+        L.xslot_off = L.red_off + 2u * 32u * 8u;                          // float2 [2][32]
+        L.meta_off = L.xslot_off + 2u * (uint32_t)kMaxCluster * 8u;       // float2 [2][16]
+        L.total = L.meta_off + 2u * (uint32_t)kMaxMeta * 8u;              // int32 + float [2][256]
+        return L;
+    }
+};
+
+// Per-mode host entry points, defined in the kernel translation units:
+//   launch_<mode>     enqueue the kernel with the given launch shape;
+//   occupancy_<mode>  resident clusters on the whole current device for that
+//                     shape (0 if it cannot be resident); sets the kernel's
+//                     shared-memory and cluster attributes for the device first.
+#define BN_DECLARE_MODE(name)                                                   \
+    cudaError_t launch_##name(const Args &, const Launch &, cudaStream_t);      \
+    int occupancy_##name(const Launch &, cudaError_t *);
+BN_DECLARE_MODE(reduce_norm)
+BN_DECLARE_MODE(fin_reduce_norm)
+BN_DECLARE_MODE(reduce_resnorm)
+BN_DECLARE_MODE(fin_reduce_resnorm)
+BN_DECLARE_MODE(reduce_only)
+BN_DECLARE_MODE(fin_reduce_only)
+BN_DECLARE_MODE(norm_only)
+BN_DECLARE_MODE(fin_only)
+#undef BN_DECLARE_MODE
+
+}  // namespace bn

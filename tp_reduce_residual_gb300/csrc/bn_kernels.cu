@@ -1,0 +1,129 @@
+// bn_kernels.cu -- instantiates the kernel template for one mode.
+//
+// Compiled once per mode with -DBN_MODE_NAME=<name> -DBN_MODE_VALUE=<bits>
+// (the build compiles the eight modes as eight objects in parallel), always
+// with -fmad=false: the FP32 epilogue must not be contracted into FMAs
+// ("Fuse Beam's TP all-reduce with its sandwich norms", "Details", "Build").
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "bn_device.cuh"
+
+#if !defined(BN_MODE_NAME) || !defined(BN_MODE_VALUE)
+#error "compile with -DBN_MODE_NAME=<name> -DBN_MODE_VALUE=<mode bits>"
+#endif
+
+#define BN_CAT2(a, b) a##b
+#define BN_CAT(a, b) BN_CAT2(a, b)
+
+namespace bn {
+namespace {
+
+constexpr int kMode = BN_MODE_VALUE;
+constexpr int kMaxDevices = 64;
+
+const void *kernel_for(int cpt)
+{
+    switch (cpt) {
+    case 1: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 1>);
+    case 2: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 2>);
+    case 4: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 4>);
+    case 8: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 8>);
+    default: return nullptr;
+    }
+}
+
+int cpt_index(int cpt) { return cpt == 1 ? 0 : cpt == 2 ? 1 : cpt == 4 ? 2 : 3; }
+
+// Function attributes are per device: set them once per (device, cpt).
+std::atomic<unsigned> g_prepared[kMaxDevices];
+
+cudaError_t prepare(const void *fn, int cpt)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    const unsigned bit = 1u << cpt_index(cpt);
+    if (g_prepared[dev].load(std::memory_order_acquire) & bit) return cudaSuccess;
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - (int)fa.sharedSizeBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    g_prepared[dev].fetch_or(bit, std::memory_order_acq_rel);
+    return cudaSuccess;
+}
+
+void fill_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, const Launch &l, int grid,
+                 cudaStream_t st)
+{
+    cfg = cudaLaunchConfig_t{};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)(l.consumers + 32), 1, 1);
+    cfg.dynamicSmemBytes = l.smem;
+    cfg.stream = st;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    if (l.cluster > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)l.cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+}
+
+}  // namespace
+
+cudaError_t BN_CAT(launch_, BN_MODE_NAME)(const Args &a, const Launch &l, cudaStream_t st)
+{
+    const void *fn = kernel_for(l.cpt);
+    if (!fn) return cudaErrorInvalidValue;
+    cudaError_t e = prepare(fn, l.cpt);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    fill_config(cfg, attr, l, l.grid, st);
+    void *args[] = {const_cast<Args *>(&a)};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+int BN_CAT(occupancy_, BN_MODE_NAME)(const Launch &l, cudaError_t *err)
+{
+    const void *fn = kernel_for(l.cpt);
+    if (!fn) {
+        *err = cudaErrorInvalidValue;
+        return 0;
+    }
+    cudaError_t e = prepare(fn, l.cpt);
+    if (e != cudaSuccess) {
+        *err = e;
+        return 0;
+    }
+    if (l.cluster <= 1) {
+        int per_sm = 0, dev = 0, sms = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, l.consumers + 32, l.smem);
+        if (e == cudaSuccess) e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        *err = e;
+        return e == cudaSuccess ? per_sm * sms : 0;
+    }
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    fill_config(cfg, attr, l, l.cluster, nullptr);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+    *err = e;
+    return e == cudaSuccess ? n : 0;
+}
+
+}  // namespace bn
