@@ -53,7 +53,8 @@
  *     overlaps an input range gives BN_ERR_INVALID.  A valid shape that is not
  *     served (H > 32768, R * k > 256, T * k >= 2^31) gives BN_ERR_UNSUPPORTED;
  *     bn_supports() predicts it, so the caller can fall back (decline) before
- *     doing any work.  T == 0 returns BN_OK and enqueues nothing.
+ *     doing any work.  T == 0 returns BN_OK after the shape checks, enqueues
+ *     nothing and does not examine the pointers (empty tensors may be NULL).
  *   - dbg (nullable) asks for intermediate values, for testing:
  *       dbg->sum [T,H] FP32 reduced sum s, dbg->ss [T,2] FP32 (ss1, ss2),
  *       dbg->z [R,T,H] BF16 per-shard finalize results (finalize entries).

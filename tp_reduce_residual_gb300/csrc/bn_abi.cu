@@ -407,6 +407,7 @@ bn_status bn_reduce_norm(const uint16_t *partials, int R, int T, int H, uint16_t
 {
     g_msg[0] = '\0';
     BN_TRY(check_shape(R, T, 1, H, false));
+    if (T == 0) return BN_OK;  // nothing is read or written; pointers are not examined
     Range reads[8], writes[8];
     int nr = 0, nw = 0;
     BN_TRY(check_reduce_sources(partials, R, T, H, reads, &nr));
@@ -433,6 +434,7 @@ bn_status bn_finalize_reduce_norm(const uint16_t *expert_out, const int32_t *per
 {
     g_msg[0] = '\0';
     BN_TRY(check_shape(R, T, k, H, true));
+    if (T == 0) return BN_OK;  // nothing is read or written; pointers are not examined
     Range reads[8], writes[8];
     int nr = 0, nw = 0;
     BN_TRY(check_fin_sources(expert_out, perm, w, shared, R, T, k, H, reads, &nr));
@@ -460,6 +462,7 @@ bn_status bn_reduce_residual_norm(const uint16_t *partials, int R, int T, int H,
 {
     g_msg[0] = '\0';
     BN_TRY(check_shape(R, T, 1, H, false));
+    if (T == 0) return BN_OK;  // nothing is read or written; pointers are not examined
     Range reads[8], writes[8];
     int nr = 0, nw = 0;
     BN_TRY(check_reduce_sources(partials, R, T, H, reads, &nr));
@@ -486,6 +489,7 @@ bn_status bn_finalize_reduce_residual_norm(const uint16_t *expert_out, const int
 {
     g_msg[0] = '\0';
     BN_TRY(check_shape(R, T, k, H, true));
+    if (T == 0) return BN_OK;  // nothing is read or written; pointers are not examined
     Range reads[8], writes[8];
     int nr = 0, nw = 0;
     BN_TRY(check_fin_sources(expert_out, perm, w, shared, R, T, k, H, reads, &nr));
@@ -511,6 +515,7 @@ bn_status bn_reduce_only(const uint16_t *partials, int R, int T, int H, float *s
 {
     g_msg[0] = '\0';
     BN_TRY(check_shape(R, T, 1, H, false));
+    if (T == 0) return BN_OK;  // nothing is read or written; pointers are not examined
     Range reads[4], writes[2];
     int nr = 0, nw = 0;
     BN_TRY(check_reduce_sources(partials, R, T, H, reads, &nr));
@@ -530,6 +535,7 @@ bn_status bn_finalize_reduce_only(const uint16_t *expert_out, const int32_t *per
 {
     g_msg[0] = '\0';
     BN_TRY(check_shape(R, T, k, H, true));
+    if (T == 0) return BN_OK;  // nothing is read or written; pointers are not examined
     Range reads[8], writes[2];
     int nr = 0, nw = 0;
     BN_TRY(check_fin_sources(expert_out, perm, w, shared, R, T, k, H, reads, &nr));
@@ -552,6 +558,7 @@ bn_status bn_norm_only(const float *sum, int T, int H, uint16_t *residual, const
 {
     g_msg[0] = '\0';
     BN_TRY(check_shape(1, T, 1, H, false));
+    if (T == 0) return BN_OK;  // nothing is read or written; pointers are not examined
     Range reads[8], writes[8];
     int nr = 0, nw = 0;
     BN_TRY(check_ptr16(sum, "sum"));
@@ -579,6 +586,7 @@ bn_status bn_finalize_only(const uint16_t *expert_out, const int32_t *perm, cons
 {
     g_msg[0] = '\0';
     BN_TRY(check_shape(R, T, k, H, true));
+    if (T == 0) return BN_OK;  // nothing is read or written; pointers are not examined
     Range reads[8], writes[2];
     int nr = 0, nw = 0;
     BN_TRY(check_fin_sources(expert_out, perm, w, shared, R, T, k, H, reads, &nr));
