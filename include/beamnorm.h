@@ -8,12 +8,13 @@
  *   norm-residual-norm epilogue, with an optional MoE top-k finalize before
  *   the reduction that keeps each rank's local BF16 rounding; section
  *   "Details", "Build" bullet: the FP32 epilogue is not contracted into FMAs;
- *   the workspace "returns None" (declines) for shapes it does not serve.
+ *   the workspace declines (returns nothing) for shapes it does not serve.
  *   sglang pull request 34134 (cute-dsl MNNVL all-reduce fusion backend),
- *   description: the two fused patterns "AllReduce + residual + RMSNorm" and
- *   "MoE finalize + shared-expert add + AllReduce + residual + RMSNorm", the
- *   deferred finalize "materialized in place" when fusion declines, and the
- *   rule that a decline must never drop the owed reduction.
+ *   description: two fused patterns, the plain one (all-reduce, residual add,
+ *   RMSNorm) and the MoE one (finalize and shared-expert add folded in ahead
+ *   of the all-reduce, residual add and RMSNorm); a deferred finalize that
+ *   meets a path which does not fuse is written out on its own; a decline
+ *   must never drop the reduction that is still owed.
  *
  * Here the R tensor-parallel shards are all resident on the calling GPU; the
  * reduction is over a data dimension and nothing is communicated.
@@ -124,14 +125,15 @@ BN_API bn_status bn_finalize_reduce_norm(const uint16_t *expert_out, const int32
                                   const float *gamma_pre, float eps, uint16_t *out,
                                   const bn_debug *dbg, void *stream);
 
-/* The single-norm pattern "AllReduce + residual + RMSNorm": no post-norm,
+/* The plain single-norm pattern (all-reduce, residual add, RMSNorm): no post-norm,
  * h = residual + s, then the RMSNorm with weight gamma.  dbg->ss[:,0] is 0.
  * Source: sglang pull request 34134, description (first fused pattern). */
 BN_API bn_status bn_reduce_residual_norm(const uint16_t *partials, int R, int T, int H,
                                   uint16_t *residual, const float *gamma, float eps,
                                   uint16_t *out, const bn_debug *dbg, void *stream);
 
-/* "MoE finalize + shared-expert add + AllReduce + residual + RMSNorm".
+/* The MoE single-norm pattern: per-shard finalize with the shared-expert add,
+ * then all-reduce, residual add and RMSNorm (no post-norm).
  * Source: sglang pull request 34134, description (second fused pattern). */
 BN_API bn_status bn_finalize_reduce_residual_norm(const uint16_t *expert_out, const int32_t *perm,
                                            const float *w, const uint16_t *shared,
@@ -160,8 +162,8 @@ BN_API bn_status bn_norm_only(const float *sum, int T, int H, uint16_t *residual
 
 /* The deferred finalize materialised on its own: z_out [R, T, H] BF16 =
  * bf16(sum_j w*x_j + shared) per shard, with no reduction.
- * Source: sglang pull request 34134, description ("a deferred finalize that
- * reaches a non-fusing path is materialized in place"). */
+ * Source: sglang pull request 34134, description (the deferred finalize written
+ * out on its own when the fused path declines). */
 BN_API bn_status bn_finalize_only(const uint16_t *expert_out, const int32_t *perm,
                            const float *w, const uint16_t *shared,
                            int R, int T, int k, int H, uint16_t *z_out, void *stream);

@@ -196,7 +196,7 @@ def finalize_reduce_norm(expert_out, perm, w, shared, residual, gamma_post, gamm
 
 def reduce_residual_norm(partials, residual, gamma, eps: float, out=None,
                          debug: Optional[Debug] = None, stream=None) -> torch.Tensor:
-    """AllReduce + residual + RMSNorm (no post-norm)."""
+    """Rank-ordered sum, residual add (in place), RMSNorm; no post-norm."""
     L = load()
     R, T, H = partials.shape
     dev = partials.device
@@ -215,7 +215,7 @@ def reduce_residual_norm(partials, residual, gamma, eps: float, out=None,
 def finalize_reduce_residual_norm(expert_out, perm, w, shared, residual, gamma, eps: float,
                                   out=None, debug: Optional[Debug] = None,
                                   stream=None) -> torch.Tensor:
-    """MoE finalize + shared-expert add + AllReduce + residual + RMSNorm."""
+    """Per-shard finalize, rank-ordered sum, residual add (in place), RMSNorm."""
     L = load()
     R, T, k = perm.shape
     H = expert_out.shape[-1]

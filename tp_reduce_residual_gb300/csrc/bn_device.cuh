@@ -2,12 +2,12 @@
 //
 // Operation: the arithmetic epilogue of a fused tensor-parallel all-reduce
 // ("Fuse Beam's TP all-reduce with its sandwich norms", vLLM pull request
-// 62366, "Claims": FP32 norm-residual-norm epilogue, optional MoE finalize
-// before the reduction keeping the local BF16 rounding; "Details": no FMA
-// contraction of the FP32 epilogue, so this file is compiled with
-// -fmad=false), and its variants from sglang pull request 34134 (description:
-// "AllReduce + residual + RMSNorm" and "MoE finalize + shared-expert add +
-// AllReduce + residual + RMSNorm").
+// 62366, section Claims: FP32 norm-residual-norm epilogue, optional MoE
+// finalize before the reduction keeping the local BF16 rounding; section
+// Details: no FMA contraction of the FP32 epilogue, so this file is compiled
+// with -fmad=false), and its variants from sglang pull request 34134 (description:
+// the plain all-reduce / residual / RMSNorm pattern and the MoE pattern with
+// the finalize and shared-expert add folded in ahead of it).
 //
 // Design (GB300):
 //   * One token row is owned by one CTA, or by a thread-block cluster of up to
