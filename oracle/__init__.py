@@ -43,7 +43,10 @@ def lib() -> ctypes.CDLL:
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.build()
+            # A test may point the wrapper at a deliberately broken copy of the
+            # oracle (tests/test_oracle_mutations.py); otherwise build and load
+            # the real one.
+            path = os.environ.get("BEAMNORM_ORACLE_LIB") or _build.build()
             L = ctypes.CDLL(path)
             L.oracle_reduce_norm.argtypes = [_u16p, _int, _int, _int, _u16p, _f32p, _f32p, _f32,
                                              _int, _i32p, _int, _u16p, _u16p, _f32p, _f32p]
