@@ -190,8 +190,10 @@ BN_API int bn_version(void);
 
 /* Launch-shape overrides for measurement sweeps (process-wide; 0 = automatic):
  * cluster_size in {1,2,4,8,16} CTAs per token row, stages = pipeline depth,
- * threads = consumer threads per CTA (a multiple of 32, at most 512). */
-BN_API bn_status bn_set_tuning(int cluster_size, int stages, int threads);
+ * threads = consumer threads per CTA (a multiple of 32, at most 512),
+ * ctas_per_sm = CTAs sharing one SM (at most 8; capped by what registers
+ * allow).  Results do not depend on the launch shape, only speed does. */
+BN_API bn_status bn_set_tuning(int cluster_size, int stages, int threads, int ctas_per_sm);
 
 #ifdef __cplusplus
 }

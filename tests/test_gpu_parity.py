@@ -23,9 +23,9 @@ def _gpu():
     assert torch.cuda.is_available(), "the GPU tests need a CUDA device"
     nbuild.build()
     bn.load()
-    bn.set_tuning(0, 0, 0)
+    bn.set_tuning()
     yield
-    bn.set_tuning(0, 0, 0)
+    bn.set_tuning()
     torch.cuda.empty_cache()
 
 
@@ -167,36 +167,36 @@ def test_decline_then_fallback_gives_the_same_bits():
 
 # ---- launch shapes, streams, graphs ------------------------------------------------------
 
-@pytest.mark.parametrize("cluster,stages,threads", [
-    (1, 0, 0), (2, 0, 0), (4, 3, 0), (8, 0, 0), (16, 2, 0), (1, 2, 0), (1, 7, 0),
-    (1, 0, 256), (1, 0, 128), (2, 5, 64),
+@pytest.mark.parametrize("cluster,stages,threads,ctas", [
+    (1, 0, 0, 0), (2, 0, 0, 0), (4, 3, 0, 0), (8, 0, 0, 0), (16, 2, 0, 0), (1, 2, 0, 0),
+    (1, 7, 0, 0), (1, 0, 256, 0), (1, 0, 128, 0), (2, 5, 64, 0), (1, 0, 128, 3), (1, 4, 64, 4),
 ])
-def test_launch_shapes_give_identical_bits(cluster, stages, threads):
+def test_launch_shapes_give_identical_bits(cluster, stages, threads, ctas):
     wl = inputs.custom("finalize_reduce_norm", 8, 8192, 10, partial_std=0.3)
     d = parity.gpu_inputs(wl, 21, seed=77)
     try:
-        bn.set_tuning(cluster, stages, threads)
+        bn.set_tuning(cluster, stages, threads, ctas)
         g = parity.run_fused(d)
     finally:
-        bn.set_tuning(0, 0, 0)
+        bn.set_tuning()
     base = parity.run_fused(d)
     for key in ("sum", "ss", "z", "out", "residual_out"):
         assert_bits_equal(g[key], base[key], key)
-    parity.compare(g, parity.run_oracle(d), what=f"cluster={cluster} stages={stages}")
+    parity.compare(g, parity.run_oracle(d), what=f"cluster={cluster} stages={stages} ctas={ctas}")
 
 
 def test_reduce_launch_shapes_give_identical_bits():
     wl = inputs.custom("reduce_norm", 8, 5120, row_scale=True)
     d = parity.gpu_inputs(wl, 45, seed=78)
     base = parity.run_fused(d)
-    for cluster in (2, 4, 16):
+    for cluster, threads, ctas in ((2, 0, 0), (4, 0, 0), (16, 0, 0), (1, 512, 1), (1, 64, 4)):
         try:
-            bn.set_tuning(cluster, 0, 0)
+            bn.set_tuning(cluster, 0, threads, ctas)
             g = parity.run_fused(d)
         finally:
-            bn.set_tuning(0, 0, 0)
+            bn.set_tuning()
         for key in ("sum", "ss", "out", "residual_out"):
-            assert_bits_equal(g[key], base[key], f"cluster={cluster} {key}")
+            assert_bits_equal(g[key], base[key], f"cluster={cluster} threads={threads} {key}")
 
 
 def test_side_stream_and_graph_replay():
@@ -270,13 +270,13 @@ def test_outputs_stay_inside_their_buffers(cluster):
     rb, res, rg = _guarded(T * H, torch.bfloat16)
     res.copy_(d["residual"].reshape(-1))
     try:
-        bn.set_tuning(cluster, 0, 0)
+        bn.set_tuning(cluster)
         bn.finalize_reduce_norm(d["expert_out"], d["perm"], d["w"], d["shared"], res.view(T, H),
                                 d["gamma_post"], d["gamma_pre"], d["eps"], out=out.view(T, H),
                                 debug=bn.Debug(sum=s.view(T, H), ss=ss.view(T, 2), z=z.view(R, T, H)))
         torch.cuda.synchronize()
     finally:
-        bn.set_tuning(0, 0, 0)
+        bn.set_tuning()
     for buf, g, n in ((ob, og, T * H), (sb, sg, T * H), (qb, qg, T * 2), (zb, zg, R * T * H),
                       (rb, rg, T * H)):
         assert _guard_intact(buf, g, n)

@@ -48,13 +48,15 @@ bn_status cuda_fail(cudaError_t e, const char *what)
 
 // ---- tuning overrides (process-wide) -------------------------------------------
 
-std::atomic<int> g_tune_cluster{0}, g_tune_stages{0}, g_tune_threads{0};
+std::atomic<int> g_tune_cluster{0}, g_tune_stages{0}, g_tune_threads{0}, g_tune_ctas{0};
 
 // ---- per-device state ------------------------------------------------------------
 
 struct DeviceInfo {
     int sms = 0;
-    int smem_optin = 0;
+    int smem_optin = 0;      // dynamic + static shared memory one CTA may use
+    int smem_per_sm = 0;     // shared memory of one SM
+    int smem_reserved = 0;   // shared memory the system reserves per CTA
     unsigned *err = nullptr;  // address of g_bn_device_error on this device
 };
 
@@ -73,6 +75,10 @@ bn_status device_info(const DeviceInfo **out)
         cudaError_t st = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
         if (st == cudaSuccess)
             st = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (st == cudaSuccess)
+            st = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        if (st == cudaSuccess)
+            st = cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
         if (st == cudaSuccess)
             st = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_bn_device_error);
         g_dev_status[dev] = st;
@@ -252,17 +258,38 @@ int auto_cluster(int T, int nchunks, int sms)
     return cs;
 }
 
-bn_status plan(int mode, int T, int H, Launch *l, Args *a)
+// Copies the producer issues per token row.
+int loads_per_row(int mode, const Args &a)
+{
+    if (mode & F_SUM_IN) return 2;
+    int n = (mode & F_FIN) ? a.R * (a.k + (a.shared ? 1 : 0)) : a.R;
+    if (mode & F_RESNORM) n += 1;
+    return n;
+}
+
+// Launch shape:
+//   cluster   CTAs per row (automatic: split rows while rows alone leave SMs idle);
+//   consumers up to 256 threads (reduce modes) or 512 (finalize modes) per CTA,
+//             each owning CPT 16-byte chunks of the CTA's slice;
+//   CTAs/SM   as many as registers and threads allow (at most 4), so that the
+//             per-row reductions of one CTA overlap another CTA's streaming;
+//   stages    the SM's shared memory split over those CTAs, capped at two rows
+//             of copies ahead.
+bn_status plan(int mode, Args *a, Launch *l)
 {
     const DeviceInfo *d = nullptr;
     BN_TRY(device_info(&d));
+    const int T = a->T, H = a->H;
     const bool sum_in = (mode & F_SUM_IN) != 0;
+    const bool fin = (mode & F_FIN) != 0;
     const int nchunks = H / 8;
     int cs = g_tune_cluster.load();
     if (cs <= 0) cs = auto_cluster(T, nchunks, d->sms);
     if (cs > nchunks) cs = 1;
-    const int cap = g_tune_threads.load() > 0 ? g_tune_threads.load() : kMaxConsumers;
+    const int cap = g_tune_threads.load() > 0 ? g_tune_threads.load() : (fin ? kMaxConsumers : 256);
     const int want_stages = g_tune_stages.load();
+    const int want_ctas = g_tune_ctas.load();
+    const int per_row = loads_per_row(mode, *a);
 
     for (;; cs /= 2) {
         const int nch_max = (nchunks + cs - 1) / cs;
@@ -272,21 +299,41 @@ bn_status plan(int mode, int T, int H, Launch *l, Args *a)
         if (consumers > kMaxConsumers)
             return fail(BN_ERR_UNSUPPORTED, "row of %d chunks needs %d consumer threads", nch_max, consumers);
         const int stage_bytes = round_up(nch_max * 16 * (sum_in ? 2 : 1), 128);
-        // pipeline depth: ~144 KB in flight unless overridden, within the
-        // opt-in shared memory of one CTA
-        int stages = want_stages > 0 ? want_stages : (144 * 1024) / stage_bytes;
-        if (stages > kMaxStages) stages = kMaxStages;
-        if (stages < 2) stages = 2;
-        const int budget = d->smem_optin - 1024;  // room for the kernel's static shared memory
-        while (stages > 2 && (int)SmemLayout::make(stages, stage_bytes).total > budget) --stages;
-        if ((int)SmemLayout::make(stages, stage_bytes).total > budget)
-            return fail(BN_ERR_UNSUPPORTED, "stage of %d bytes does not fit shared memory", stage_bytes);
+        const int overhead = (int)SmemLayout::make(0, stage_bytes).total + 2 * 16;
+        const int cta_max = d->smem_optin - 1024;  // room for the kernel's static shared memory
 
         Launch L;
         L.cluster = cs;
         L.consumers = consumers;
         L.cpt = cpt;
+        // CTAs per SM that registers and threads allow (probe with a 2-stage ring)
+        Launch probe = L;
+        probe.cluster = 1;
+        probe.smem = SmemLayout::make(2, stage_bytes).total;
+        int resident_probe = 0;
+        BN_TRY(resident_clusters(mode, probe, &resident_probe));
+        int by_regs = resident_probe / (d->sms > 0 ? d->sms : 1);
+        if (by_regs < 1) by_regs = 1;
+        int ctas = want_ctas > 0 ? want_ctas : (by_regs < 4 ? by_regs : 4);
+        if (ctas > by_regs) ctas = by_regs;
+        int per_cta = d->smem_per_sm / ctas - d->smem_reserved - 1024;
+        if (per_cta > cta_max) per_cta = cta_max;
+
+        int stages;
+        if (want_stages > 0) {
+            stages = want_stages;
+        } else {
+            stages = (per_cta - overhead) / stage_bytes;
+            const int ahead = 2 * per_row + 2;
+            if (stages > ahead) stages = ahead;
+        }
+        if (stages > kMaxStages) stages = kMaxStages;
+        if (stages < 2) stages = 2;
+        while (stages > 2 && (int)SmemLayout::make(stages, stage_bytes).total > cta_max) --stages;
+        if ((int)SmemLayout::make(stages, stage_bytes).total > cta_max)
+            return fail(BN_ERR_UNSUPPORTED, "stage of %d bytes does not fit shared memory", stage_bytes);
         L.smem = SmemLayout::make(stages, stage_bytes).total;
+
         int resident = 0;
         BN_TRY(resident_clusters(mode, L, &resident));
         if (resident <= 0) {
@@ -308,7 +355,7 @@ bn_status run(int mode, Args &a, void *stream)
 {
     if (a.T == 0) return BN_OK;
     Launch l;
-    BN_TRY(plan(mode, a.T, a.H, &l, &a));
+    BN_TRY(plan(mode, &a, &l));
     cudaError_t e = ops_for(mode).launch(a, l, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, ops_for(mode).name);
     return BN_OK;
@@ -653,7 +700,7 @@ const char *bn_status_string(bn_status status)
 
 int bn_version(void) { return kVersion; }
 
-bn_status bn_set_tuning(int cluster_size, int stages, int threads)
+bn_status bn_set_tuning(int cluster_size, int stages, int threads, int ctas_per_sm)
 {
     g_msg[0] = '\0';
     if (cluster_size != 0 && cluster_size != 1 && cluster_size != 2 && cluster_size != 4 &&
@@ -663,7 +710,10 @@ bn_status bn_set_tuning(int cluster_size, int stages, int threads)
         return fail(BN_ERR_INVALID, "stages must be 0 or in [2, %d]", kMaxStages);
     if (threads < 0 || threads > kMaxConsumers || threads % 32 != 0)
         return fail(BN_ERR_INVALID, "threads must be 0 or a multiple of 32 up to %d", kMaxConsumers);
+    if (ctas_per_sm < 0 || ctas_per_sm > 8)
+        return fail(BN_ERR_INVALID, "ctas_per_sm must be in [0, 8]");
     g_tune_cluster.store(cluster_size);
+    g_tune_ctas.store(ctas_per_sm);
     g_tune_stages.store(stages);
     g_tune_threads.store(threads);
     return BN_OK;

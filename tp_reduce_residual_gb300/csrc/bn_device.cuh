@@ -197,31 +197,87 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 }
 
 // ---- arithmetic helpers ----------------------------------------------------------
+//
+// The consumers work on packed FP32 pairs (f2): Blackwell's add/sub/mul .f32x2
+// round each lane to nearest even exactly like the scalar instructions, so the
+// results are those of the scalar definition while half as many instructions
+// issue.  Element 2i of a 16-byte chunk is the low lane of pair i.
 
-// Exact widening of eight BF16 values packed in 16 bytes (element 2i is the low
-// half of word i).
-__device__ __forceinline__ void unpack8(const uint4 &v, float *f)
+typedef unsigned long long f2;
+
+__device__ __forceinline__ f2 f2_make(float lo, float hi)
 {
-    f[0] = __uint_as_float(v.x << 16);
-    f[1] = __uint_as_float(v.x & 0xffff0000u);
-    f[2] = __uint_as_float(v.y << 16);
-    f[3] = __uint_as_float(v.y & 0xffff0000u);
-    f[4] = __uint_as_float(v.z << 16);
-    f[5] = __uint_as_float(v.z & 0xffff0000u);
-    f[6] = __uint_as_float(v.w << 16);
-    f[7] = __uint_as_float(v.w & 0xffff0000u);
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(f2 v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b)
+{
+    f2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b)
+{
+    f2 r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b)
+{
+    f2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// Only used to obtain the exact rounding error of a product (see acc_square2).
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c)
+{
+    f2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ f2 neg2(f2 a) { return a ^ 0x8000000080000000ull; }
+
+// Exact widening of a word holding two BF16 values (low half -> low lane).
+__device__ __forceinline__ f2 widen2(uint32_t w)
+{
+    return f2_make(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-// Round two FP32 values to BF16 (nearest even) and pack them, lo in the low half.
-__device__ __forceinline__ uint32_t pack2(float lo, float hi)
+__device__ __forceinline__ void widen8(const uint4 &v, f2 *x)
 {
+    x[0] = widen2(v.x);
+    x[1] = widen2(v.y);
+    x[2] = widen2(v.z);
+    x[3] = widen2(v.w);
+}
+
+// Round a pair to BF16 (nearest even) and pack it, low lane in the low half.
+__device__ __forceinline__ uint32_t round2(f2 v)
+{
+    float lo, hi;
+    f2_split(v, lo, hi);
     __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&b);
 }
 
-__device__ __forceinline__ uint4 pack8(const float *f)
+__device__ __forceinline__ uint4 round8(const f2 *v)
 {
-    return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+    return make_uint4(round2(v[0]), round2(v[1]), round2(v[2]), round2(v[3]));
+}
+
+__device__ __forceinline__ void load_gamma8(const float *g, f2 *out)
+{
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(g));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(g) + 1);
+    out[0] = f2_make(a.x, a.y);
+    out[1] = f2_make(a.z, a.w);
+    out[2] = f2_make(b.x, b.y);
+    out[3] = f2_make(b.z, b.w);
 }
 
 // s + e == a + b exactly (Knuth's two-sum; no ordering assumption).
@@ -232,17 +288,19 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
     e = (a - (s - bb)) + (b - bb);
 }
 
-// (S, E) += x*x with the product's rounding error and the addition's error
-// both carried in E.  The explicit fma only computes the exact error of the
-// rounded product; no result value is contracted.
-__device__ __forceinline__ void acc_square(float &S, float &E, float x)
+// Two independent compensated accumulators (one per lane): (S, E) += x*x.
+// The product's rounding error comes from one explicit fma (it only measures
+// the error of the rounded product; no result value is contracted) and the
+// addition's error from two-sum; both are carried in E.
+__device__ __forceinline__ void acc_square2(f2 &S, f2 &E, f2 x)
 {
-    const float p = x * x;
-    const float pe = __fmaf_rn(x, x, -p);
-    float s, e;
-    two_sum(S, p, s, e);
+    const f2 p = mul2(x, x);
+    const f2 pe = fma2(x, x, neg2(p));
+    const f2 s = add2(S, p);
+    const f2 bb = sub2(s, S);
+    const f2 e = add2(sub2(S, sub2(s, bb)), sub2(p, bb));
     S = s;
-    E = E + (e + pe);
+    E = add2(E, add2(e, pe));
 }
 
 __device__ __forceinline__ void combine(float &S, float &E, float S2, float E2)
@@ -251,6 +309,17 @@ __device__ __forceinline__ void combine(float &S, float &E, float S2, float E2)
     two_sum(S, S2, s, e);
     S = s;
     E = (E + E2) + e;
+}
+
+// Fold the two lanes of a packed accumulator into one (S, E), low lane first.
+__device__ __forceinline__ void fold2(f2 S2, f2 E2, float &S, float &E)
+{
+    float s0, s1, e0, e1;
+    f2_split(S2, s0, s1);
+    f2_split(E2, e0, e1);
+    S = s0;
+    E = e0;
+    combine(S, E, s1, e1);
 }
 
 __device__ __forceinline__ void warp_tree(float &S, float &E)
@@ -286,11 +355,13 @@ struct Smem {
 // Row-wide sum of squares: compensated pairs reduced over the warp, the
 // consumer warps of the CTA, then the CTAs of the cluster, in a fixed order;
 // every consumer thread of every CTA of the cluster gets the same value.
-__device__ __forceinline__ float row_sum_squares(float S, float E, int &nred, const Smem &sm,
+__device__ __forceinline__ float row_sum_squares(f2 S2, f2 E2, int &nred, const Smem &sm,
                                                  uint32_t cs, uint32_t q, int NT, int NW,
                                                  int warp, int lane, int tid, const Ctl &ctl,
                                                  bool &live)
 {
+    float S, E;
+    fold2(S2, E2, S, E);
     warp_tree(S, E);
     const int b = nred & 1;
     if (lane == 0) sm.red[b * 32 + warp] = make_float2(S, E);
@@ -364,20 +435,19 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
     const size_t H = (size_t)a.H;
     const bool has_shared = FIN && a.shared != nullptr;
 
-    if (tid == 0) {
-        s_abort = 0;
-        for (int i = 0; i < S; ++i) {
-            mbar_init(sm.full0 + 8u * i, 1u);
-            mbar_init(sm.empty0 + 8u * i, (uint32_t)NW);
-        }
-        mbar_init(sm.mfull0, 32u);
-        mbar_init(sm.mfull0 + 8u, 32u);
-        mbar_init(sm.mempty0, (uint32_t)NW);
-        mbar_init(sm.mempty0 + 8u, (uint32_t)NW);
-        mbar_init(sm.ex0, cs);
-        mbar_init(sm.ex0 + 8u, cs);
-        fence_mbarrier_init();
+    // barriers: full[S], empty[S], meta_full[2], meta_empty[2], exchange[2]
+    const int nbars = 2 * S + 6;
+    for (int i = tid; i < nbars; i += (int)blockDim.x) {
+        uint32_t count;
+        if (i < S) count = 1u;                      // full: the producer's expect-tx arrive
+        else if (i < 2 * S) count = (uint32_t)NW;   // empty: one arrive per consumer warp
+        else if (i < 2 * S + 2) count = 32u;        // meta_full: every producer lane
+        else if (i < 2 * S + 4) count = (uint32_t)NW;  // meta_empty
+        else count = cs;                            // exchange: one arrive per CTA
+        mbar_init(sm.full0 + 8u * (uint32_t)i, count);
     }
+    if (tid == 0) s_abort = 0;
+    fence_mbarrier_init();
     __syncthreads();
     if (cs > 1) cluster_sync_all();
     const Ctl ctl{&s_abort, a.err};
@@ -483,14 +553,17 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                 phase ^= 1u;
             }
         };
+        auto chunk = [&](const uint8_t *p, int lc) -> uint4 {
+            return *reinterpret_cast<const uint4 *>(p + (size_t)lc * 16);
+        };
 
         for (int t = cl, it = 0; t < a.T; t += ncl, ++it) {
             const int slot = it & 1;
-            float s[CPT][8];
+            f2 s[CPT][4];
 #pragma unroll
             for (int i = 0; i < CPT; ++i)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) s[i][e] = 0.f;
+                for (int m = 0; m < 4; ++m) s[i][m] = 0ull;
 
             // ---- the reduced sum s (or the per-shard finalize results) ----
             if constexpr (SUM_IN) {
@@ -499,10 +572,12 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                 for (int i = 0; i < CPT; ++i) {
                     const int lc = tid + i * NT;
                     if (lc < nch) {
-                        const float4 u = *reinterpret_cast<const float4 *>(p + (size_t)lc * 32);
-                        const float4 v = *reinterpret_cast<const float4 *>(p + (size_t)lc * 32 + 16);
-                        s[i][0] = u.x; s[i][1] = u.y; s[i][2] = u.z; s[i][3] = u.w;
-                        s[i][4] = v.x; s[i][5] = v.y; s[i][6] = v.z; s[i][7] = v.w;
+                        const uint4 u = *reinterpret_cast<const uint4 *>(p + (size_t)lc * 32);
+                        const uint4 v = *reinterpret_cast<const uint4 *>(p + (size_t)lc * 32 + 16);
+                        s[i][0] = ((f2)u.y << 32) | u.x;
+                        s[i][1] = ((f2)u.w << 32) | u.z;
+                        s[i][2] = ((f2)v.y << 32) | v.x;
+                        s[i][3] = ((f2)v.w << 32) | v.z;
                     }
                 }
                 release();
@@ -511,33 +586,35 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                     live = false;
                 const float *wrow = sm.mw + slot * kMaxMeta;
                 for (int r = 0; r < a.R; ++r) {
-                    float acc[CPT][8];
+                    f2 acc[CPT][4];
                     // slot 0: acc = w0 * x0
                     {
                         const float w0 = wrow[r * a.k];
+                        const f2 w2 = f2_make(w0, w0);
                         const uint8_t *p = take();
 #pragma unroll
                         for (int i = 0; i < CPT; ++i) {
                             const int lc = tid + i * NT;
-                            float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                            if (lc < nch) unpack8(*reinterpret_cast<const uint4 *>(p + (size_t)lc * 16), x);
+                            f2 x[4] = {0ull, 0ull, 0ull, 0ull};
+                            if (lc < nch) widen8(chunk(p, lc), x);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[i][e] = w0 * x[e];
+                            for (int m = 0; m < 4; ++m) acc[i][m] = mul2(w2, x[m]);
                         }
                         release();
                     }
                     // slots 1..k-1: acc = acc + wj * xj
                     for (int j = 1; j < a.k; ++j) {
                         const float wj = wrow[r * a.k + j];
+                        const f2 w2 = f2_make(wj, wj);
                         const uint8_t *p = take();
 #pragma unroll
                         for (int i = 0; i < CPT; ++i) {
                             const int lc = tid + i * NT;
                             if (lc < nch) {
-                                float x[8];
-                                unpack8(*reinterpret_cast<const uint4 *>(p + (size_t)lc * 16), x);
+                                f2 x[4];
+                                widen8(chunk(p, lc), x);
 #pragma unroll
-                                for (int e = 0; e < 8; ++e) acc[i][e] = acc[i][e] + wj * x[e];
+                                for (int m = 0; m < 4; ++m) acc[i][m] = add2(acc[i][m], mul2(w2, x[m]));
                             }
                         }
                         release();
@@ -549,10 +626,10 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                         for (int i = 0; i < CPT; ++i) {
                             const int lc = tid + i * NT;
                             if (lc < nch) {
-                                float x[8];
-                                unpack8(*reinterpret_cast<const uint4 *>(p + (size_t)lc * 16), x);
+                                f2 x[4];
+                                widen8(chunk(p, lc), x);
 #pragma unroll
-                                for (int e = 0; e < 8; ++e) acc[i][e] = acc[i][e] + x[e];
+                                for (int m = 0; m < 4; ++m) acc[i][m] = add2(acc[i][m], x[m]);
                             }
                         }
                         release();
@@ -562,19 +639,19 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
                         if (lc < nch) {
-                            const uint4 z = pack8(acc[i]);
+                            const uint4 z = round8(acc[i]);
                             if ((Z_OUT || a.z_out != nullptr) && live)
                                 *reinterpret_cast<uint4 *>(a.z_out + ((size_t)r * a.T + t) * H +
                                                            (size_t)(c0 + lc) * 8) = z;
                             if constexpr (REDUCE) {
-                                float zf[8];
-                                unpack8(z, zf);
+                                f2 zf[4];
+                                widen8(z, zf);
                                 if (r == 0) {
 #pragma unroll
-                                    for (int e = 0; e < 8; ++e) s[i][e] = zf[e];
+                                    for (int m = 0; m < 4; ++m) s[i][m] = zf[m];
                                 } else {
 #pragma unroll
-                                    for (int e = 0; e < 8; ++e) s[i][e] = s[i][e] + zf[e];
+                                    for (int m = 0; m < 4; ++m) s[i][m] = add2(s[i][m], zf[m]);
                                 }
                             }
                         }
@@ -583,21 +660,26 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sm.mempty0 + 8u * slot);
             } else {
-                for (int r = 0; r < a.R; ++r) {
+                // shard 0 initialises the sum, shards 1..R-1 add in rank order
+                {
+                    const uint8_t *p = take();
+#pragma unroll
+                    for (int i = 0; i < CPT; ++i) {
+                        const int lc = tid + i * NT;
+                        if (lc < nch) widen8(chunk(p, lc), s[i]);
+                    }
+                    release();
+                }
+                for (int r = 1; r < a.R; ++r) {
                     const uint8_t *p = take();
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
                         if (lc < nch) {
-                            float x[8];
-                            unpack8(*reinterpret_cast<const uint4 *>(p + (size_t)lc * 16), x);
-                            if (r == 0) {
+                            f2 x[4];
+                            widen8(chunk(p, lc), x);
 #pragma unroll
-                                for (int e = 0; e < 8; ++e) s[i][e] = x[e];
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) s[i][e] = s[i][e] + x[e];
-                            }
+                            for (int m = 0; m < 4; ++m) s[i][m] = add2(s[i][m], x[m]);
                         }
                     }
                     release();
@@ -611,10 +693,10 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
                         if (lc < nch) {
-                            float4 *dst = reinterpret_cast<float4 *>(a.sum_out + (size_t)t * H +
-                                                                     (size_t)(c0 + lc) * 8);
-                            dst[0] = make_float4(s[i][0], s[i][1], s[i][2], s[i][3]);
-                            dst[1] = make_float4(s[i][4], s[i][5], s[i][6], s[i][7]);
+                            f2 *dst = reinterpret_cast<f2 *>(a.sum_out + (size_t)t * H +
+                                                             (size_t)(c0 + lc) * 8);
+                            reinterpret_cast<ulonglong2 *>(dst)[0] = make_ulonglong2(s[i][0], s[i][1]);
+                            reinterpret_cast<ulonglong2 *>(dst)[1] = make_ulonglong2(s[i][2], s[i][3]);
                         }
                     }
                 }
@@ -624,68 +706,65 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
             if constexpr (RESNORM) {
                 float ss1 = 0.f;
                 if constexpr (POSTNORM) {
-                    float S1 = 0.f, E1 = 0.f;
+                    f2 S1 = 0ull, E1 = 0ull;
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
                         if (lc < nch) {
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) acc_square(S1, E1, s[i][e]);
+                            for (int m = 0; m < 4; ++m) acc_square2(S1, E1, s[i][m]);
                         }
                     }
                     ss1 = row_sum_squares(S1, E1, nred, sm, cs, q, NT, NW, warp, lane, tid, ctl, live);
                     const float r1 = rms_factor(ss1, a.H, a.eps);
+                    const f2 r1x2 = f2_make(r1, r1);
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
                         if (lc < nch) {
-                            const float4 *g = reinterpret_cast<const float4 *>(a.gamma_post +
-                                                                               (size_t)(c0 + lc) * 8);
-                            const float4 g0 = __ldg(g), g1 = __ldg(g + 1);
-                            const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                            f2 g[4];
+                            load_gamma8(a.gamma_post + (size_t)(c0 + lc) * 8, g);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) s[i][e] = (s[i][e] * r1) * gg[e];
+                            for (int m = 0; m < 4; ++m) s[i][m] = mul2(mul2(s[i][m], r1x2), g[m]);
                         }
                     }
                 }
                 // residual add and write-back (s now holds y, or the sum itself)
-                float S2 = 0.f, E2 = 0.f;
+                f2 S2 = 0ull, E2 = 0ull;
                 {
                     const uint8_t *p = take();
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
                         if (lc < nch) {
-                            float rf[8];
-                            unpack8(*reinterpret_cast<const uint4 *>(p + (size_t)lc * 16), rf);
+                            f2 rf[4];
+                            widen8(chunk(p, lc), rf);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                s[i][e] = rf[e] + s[i][e];
-                                acc_square(S2, E2, s[i][e]);
+                            for (int m = 0; m < 4; ++m) {
+                                s[i][m] = add2(rf[m], s[i][m]);
+                                acc_square2(S2, E2, s[i][m]);
                             }
                             if (live)
                                 *reinterpret_cast<uint4 *>(a.residual + (size_t)t * H +
-                                                           (size_t)(c0 + lc) * 8) = pack8(s[i]);
+                                                           (size_t)(c0 + lc) * 8) = round8(s[i]);
                         }
                     }
                     release();
                 }
                 const float ss2 = row_sum_squares(S2, E2, nred, sm, cs, q, NT, NW, warp, lane, tid, ctl, live);
                 const float r2 = rms_factor(ss2, a.H, a.eps);
+                const f2 r2x2 = f2_make(r2, r2);
 #pragma unroll
                 for (int i = 0; i < CPT; ++i) {
                     const int lc = tid + i * NT;
                     if (lc < nch) {
-                        const float4 *g = reinterpret_cast<const float4 *>(a.gamma_pre +
-                                                                           (size_t)(c0 + lc) * 8);
-                        const float4 g0 = __ldg(g), g1 = __ldg(g + 1);
-                        const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-                        float o[8];
+                        f2 g[4], o[4];
+                        load_gamma8(a.gamma_pre + (size_t)(c0 + lc) * 8, g);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) o[e] = (s[i][e] * r2) * gg[e];
+                        for (int m = 0; m < 4; ++m) o[m] = mul2(mul2(s[i][m], r2x2), g[m]);
                         if (live)
                             *reinterpret_cast<uint4 *>(a.out + (size_t)t * H + (size_t)(c0 + lc) * 8) =
-                                pack8(o);
+                                round8(o);
                     }
                 }
                 if (a.ss_out != nullptr && q == 0 && tid == 0 && live) {
