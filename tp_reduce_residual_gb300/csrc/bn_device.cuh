@@ -200,8 +200,16 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 //
 // The consumers work on packed FP32 pairs (f2): Blackwell's add/sub/mul .f32x2
 // round each lane to nearest even exactly like the scalar instructions, so the
-// results are those of the scalar definition while half as many instructions
-// issue.  Element 2i of a 16-byte chunk is the low lane of pair i.
+// results are those of the scalar definition while fewer instructions issue.
+// Element 2i of a 16-byte chunk is the low lane of pair i.
+//
+// One rule keeps the arithmetic uncontracted: ptxas fuses a packed multiply
+// that feeds a packed add into a packed fused multiply-add even under
+// --fmad=false (measured: every differing result matched the fused one),
+// while a scalar mul.rn.f32 feeding a packed add is left alone.  So every
+// product that is later added (finalize weights, squares, the post-norm
+// output before the residual add) is formed lane by lane with mul_sep2;
+// packed multiplies (mul2) only feed other multiplies or outputs.
 
 typedef unsigned long long f2;
 
@@ -232,6 +240,21 @@ __device__ __forceinline__ f2 mul2(f2 a, f2 b)
     f2 r;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
+}
+// A product that will be added to something: two scalar multiplies, which the
+// code generator keeps separate from the following addition.
+__device__ __forceinline__ float mul_sep(float a, float b)
+{
+    float r;
+    asm("mul.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ f2 mul_sep2(f2 a, f2 b)
+{
+    float a0, a1, b0, b1;
+    f2_split(a, a0, a1);
+    f2_split(b, b0, b1);
+    return f2_make(mul_sep(a0, b0), mul_sep(a1, b1));
 }
 // Only used to obtain the exact rounding error of a product (see acc_square2).
 __device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c)
@@ -294,7 +317,7 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
 // addition's error from two-sum; both are carried in E.
 __device__ __forceinline__ void acc_square2(f2 &S, f2 &E, f2 x)
 {
-    const f2 p = mul2(x, x);
+    const f2 p = mul_sep2(x, x);
     const f2 pe = fma2(x, x, neg2(p));
     const f2 s = add2(S, p);
     const f2 bb = sub2(s, S);
@@ -456,10 +479,31 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
         // ================= producer warp =================
         uint32_t stage = 0, phase = 0, issued = 0;
         bool ok = true;
+        // Gather indices and weights of a row are loaded into registers one row
+        // ahead (all lanes, up to 8 slots per lane), so their latency overlaps
+        // the copies of the current row.
+        constexpr int kMetaPerLane = kMaxMeta / 32;
+        int32_t pv[kMetaPerLane];
+        float wv[kMetaPerLane];
+        const int nm = FIN ? a.R * a.k : 0;
+        auto prefetch_meta = [&](int t) {
+#pragma unroll
+            for (int u = 0; u < kMetaPerLane; ++u) {
+                const int i = lane + 32 * u;
+                if (i < nm && t < a.T) {
+                    const int r = i / a.k;
+                    const int j = i - r * a.k;
+                    const size_t mi = ((size_t)r * a.T + t) * a.k + j;
+                    pv[u] = __ldg(a.perm + mi);
+                    wv[u] = __ldg(a.w + mi);
+                }
+            }
+        };
+        if constexpr (FIN) prefetch_meta(cl);
         for (int t = cl, it = 0; t < a.T && ok; t += ncl, ++it) {
             const int slot = it & 1;
             if constexpr (FIN) {
-                // stage this row's gather indices and weights (all lanes)
+                // publish this row's gather indices and weights (all lanes)
                 bool got = true;
                 if (lane == 0)
                     got = wait_phase<false, true>(sm.mempty0 + 8u * slot,
@@ -469,22 +513,23 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                     ok = false;
                     break;
                 }
-                const int nm = a.R * a.k;
                 const long long lim = (long long)a.T * a.k;
-                for (int i = lane; i < nm; i += 32) {
-                    const int r = i / a.k;
-                    const int j = i - r * a.k;
-                    const size_t mi = ((size_t)r * a.T + t) * a.k + j;
-                    int p = __ldg(a.perm + mi);
-                    if (p < 0 || (long long)p >= lim) {
-                        atomicOr(a.err, kErrPerm);
-                        p = 0;
+#pragma unroll
+                for (int u = 0; u < kMetaPerLane; ++u) {
+                    const int i = lane + 32 * u;
+                    if (i < nm) {
+                        int p = pv[u];
+                        if (p < 0 || (long long)p >= lim) {
+                            atomicOr(a.err, kErrPerm);
+                            p = 0;
+                        }
+                        sm.mperm[slot * kMaxMeta + i] = p;
+                        sm.mw[slot * kMaxMeta + i] = wv[u];
                     }
-                    sm.mperm[slot * kMaxMeta + i] = p;
-                    sm.mw[slot * kMaxMeta + i] = __ldg(a.w + mi);
                 }
                 mbar_arrive(sm.mfull0 + 8u * slot);
                 __syncwarp();
+                prefetch_meta(t + ncl);
             }
             if (lane == 0) {
                 auto issue = [&](const void *src, uint32_t bytes) -> bool {
@@ -598,7 +643,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                             f2 x[4] = {0ull, 0ull, 0ull, 0ull};
                             if (lc < nch) widen8(chunk(p, lc), x);
 #pragma unroll
-                            for (int m = 0; m < 4; ++m) acc[i][m] = mul2(w2, x[m]);
+                            for (int m = 0; m < 4; ++m) acc[i][m] = mul_sep2(w2, x[m]);
                         }
                         release();
                     }
@@ -614,7 +659,8 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                                 f2 x[4];
                                 widen8(chunk(p, lc), x);
 #pragma unroll
-                                for (int m = 0; m < 4; ++m) acc[i][m] = add2(acc[i][m], mul2(w2, x[m]));
+                                for (int m = 0; m < 4; ++m)
+                                    acc[i][m] = add2(acc[i][m], mul_sep2(w2, x[m]));
                             }
                         }
                         release();
@@ -725,7 +771,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                             f2 g[4];
                             load_gamma8(a.gamma_post + (size_t)(c0 + lc) * 8, g);
 #pragma unroll
-                            for (int m = 0; m < 4; ++m) s[i][m] = mul2(mul2(s[i][m], r1x2), g[m]);
+                            for (int m = 0; m < 4; ++m) s[i][m] = mul_sep2(mul2(s[i][m], r1x2), g[m]);
                         }
                     }
                 }
