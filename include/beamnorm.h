@@ -192,8 +192,11 @@ BN_API int bn_version(void);
  * cluster_size in {1,2,4,8,16} CTAs per token row, stages = pipeline depth,
  * threads = consumer threads per CTA (a multiple of 32, at most 512),
  * ctas_per_sm = CTAs sharing one SM (at most 8; capped by what registers
- * allow).  Results do not depend on the launch shape, only speed does. */
-BN_API bn_status bn_set_tuning(int cluster_size, int stages, int threads, int ctas_per_sm);
+ * allow), wait_mode = how threads wait for a pipeline stage (1: suspending
+ * try_wait, 2: polling test_wait).  Results do not depend on these settings,
+ * only speed does. */
+BN_API bn_status bn_set_tuning(int cluster_size, int stages, int threads, int ctas_per_sm,
+                               int wait_mode);
 
 #ifdef __cplusplus
 }

@@ -133,13 +133,14 @@ def test_split_and_finalize_only_reject_bad_arguments(L):
 
 
 def test_set_tuning_validates(L):
-    assert L.bn_set_tuning(3, 0, 0, 0) == bn.ERR_INVALID
-    assert L.bn_set_tuning(0, 1, 0, 0) == bn.ERR_INVALID
-    assert L.bn_set_tuning(0, 65, 0, 0) == bn.ERR_INVALID
-    assert L.bn_set_tuning(0, 0, 48, 0) == bn.ERR_INVALID
-    assert L.bn_set_tuning(0, 0, 0, 9) == bn.ERR_INVALID
-    assert L.bn_set_tuning(16, 8, 256, 2) == bn.OK
-    assert L.bn_set_tuning(0, 0, 0, 0) == bn.OK
+    assert L.bn_set_tuning(3, 0, 0, 0, 0) == bn.ERR_INVALID
+    assert L.bn_set_tuning(0, 1, 0, 0, 0) == bn.ERR_INVALID
+    assert L.bn_set_tuning(0, 65, 0, 0, 0) == bn.ERR_INVALID
+    assert L.bn_set_tuning(0, 0, 48, 0, 0) == bn.ERR_INVALID
+    assert L.bn_set_tuning(0, 0, 0, 9, 0) == bn.ERR_INVALID
+    assert L.bn_set_tuning(0, 0, 0, 0, 3) == bn.ERR_INVALID
+    assert L.bn_set_tuning(16, 8, 256, 2, 2) == bn.OK
+    assert L.bn_set_tuning(0, 0, 0, 0, 0) == bn.OK
 
 
 def test_python_binding_checks_before_calling(L):

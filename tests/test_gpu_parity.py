@@ -167,15 +167,16 @@ def test_decline_then_fallback_gives_the_same_bits():
 
 # ---- launch shapes, streams, graphs ------------------------------------------------------
 
-@pytest.mark.parametrize("cluster,stages,threads,ctas", [
-    (1, 0, 0, 0), (2, 0, 0, 0), (4, 3, 0, 0), (8, 0, 0, 0), (16, 2, 0, 0), (1, 2, 0, 0),
-    (1, 7, 0, 0), (1, 0, 256, 0), (1, 0, 128, 0), (2, 5, 64, 0), (1, 0, 128, 3), (1, 4, 64, 4),
+@pytest.mark.parametrize("cluster,stages,threads,ctas,wait", [
+    (1, 0, 0, 0, 0), (2, 0, 0, 0, 0), (4, 3, 0, 0, 2), (8, 0, 0, 0, 0), (16, 2, 0, 0, 2),
+    (1, 2, 0, 0, 1), (1, 7, 0, 0, 2), (1, 0, 256, 0, 0), (1, 0, 128, 0, 2), (2, 5, 64, 0, 0),
+    (1, 0, 128, 3, 0), (1, 4, 64, 4, 2),
 ])
-def test_launch_shapes_give_identical_bits(cluster, stages, threads, ctas):
+def test_launch_shapes_give_identical_bits(cluster, stages, threads, ctas, wait):
     wl = inputs.custom("finalize_reduce_norm", 8, 8192, 10, partial_std=0.3)
     d = parity.gpu_inputs(wl, 21, seed=77)
     try:
-        bn.set_tuning(cluster, stages, threads, ctas)
+        bn.set_tuning(cluster, stages, threads, ctas, wait)
         g = parity.run_fused(d)
     finally:
         bn.set_tuning()

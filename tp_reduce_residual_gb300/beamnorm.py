@@ -91,7 +91,7 @@ def load() -> ctypes.CDLL:
             "bn_last_error": [],
             "bn_status_string": [_I],
             "bn_version": [],
-            "bn_set_tuning": [_I, _I, _I, _I],
+            "bn_set_tuning": [_I, _I, _I, _I, _I],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -323,9 +323,11 @@ def check_device_error(stream=None, raise_on_error: bool = True) -> int:
     return int(bits.value)
 
 
-def set_tuning(cluster_size: int = 0, stages: int = 0, threads: int = 0, ctas_per_sm: int = 0) -> None:
+def set_tuning(cluster_size: int = 0, stages: int = 0, threads: int = 0, ctas_per_sm: int = 0,
+               wait_mode: int = 0) -> None:
     """Override the launch shape for measurement sweeps (0 = automatic)."""
-    _check(load().bn_set_tuning(int(cluster_size), int(stages), int(threads), int(ctas_per_sm)))
+    _check(load().bn_set_tuning(int(cluster_size), int(stages), int(threads), int(ctas_per_sm),
+                                int(wait_mode)))
 
 
 def version() -> int:

@@ -48,7 +48,8 @@ bn_status cuda_fail(cudaError_t e, const char *what)
 
 // ---- tuning overrides (process-wide) -------------------------------------------
 
-std::atomic<int> g_tune_cluster{0}, g_tune_stages{0}, g_tune_threads{0}, g_tune_ctas{0};
+std::atomic<int> g_tune_cluster{0}, g_tune_stages{0}, g_tune_threads{0}, g_tune_ctas{0},
+    g_tune_wait{0};
 
 // ---- per-device state ------------------------------------------------------------
 
@@ -249,12 +250,17 @@ bn_status resident_clusters(int mode, const Launch &l, int *out)
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
-// CTAs per token row: split rows over a cluster while the rows alone would
-// leave SMs idle, keeping at least 32 chunks (one warp's worth) per CTA.
-int auto_cluster(int T, int nchunks, int sms)
+// CTAs per token row.  A cluster splits a row only when the rows alone would
+// leave SMs idle and a row is heavy enough (about 192 KB of copies per CTA)
+// to repay the two cluster-wide exchanges; each CTA keeps at least 32 chunks.
+int auto_cluster(int T, int nchunks, int sms, long long row_bytes)
 {
-    int cs = 1;
-    while (cs < kMaxCluster && (long long)T * cs < sms && nchunks / (cs * 2) >= 32) cs *= 2;
+    int by_rows = 1;
+    while (by_rows < kMaxCluster && (long long)T * by_rows * 2 <= sms) by_rows *= 2;
+    int by_bytes = 1;
+    while (by_bytes < kMaxCluster && (long long)by_bytes * 2 * 192 * 1024 <= row_bytes) by_bytes *= 2;
+    int cs = by_rows < by_bytes ? by_rows : by_bytes;
+    while (cs > 1 && nchunks / cs < 32) cs /= 2;
     return cs;
 }
 
@@ -283,13 +289,14 @@ bn_status plan(int mode, Args *a, Launch *l)
     const bool sum_in = (mode & F_SUM_IN) != 0;
     const bool fin = (mode & F_FIN) != 0;
     const int nchunks = H / 8;
+    const int per_row = loads_per_row(mode, *a);
     int cs = g_tune_cluster.load();
-    if (cs <= 0) cs = auto_cluster(T, nchunks, d->sms);
+    if (cs <= 0) cs = auto_cluster(T, nchunks, d->sms, (long long)per_row * 2 * H);
     if (cs > nchunks) cs = 1;
-    const int cap = g_tune_threads.load() > 0 ? g_tune_threads.load() : (fin ? kMaxConsumers : 256);
+    const int cap = g_tune_threads.load() > 0 ? g_tune_threads.load() : kMaxConsumers;
     const int want_stages = g_tune_stages.load();
     const int want_ctas = g_tune_ctas.load();
-    const int per_row = loads_per_row(mode, *a);
+    (void)fin;
 
     for (;; cs /= 2) {
         const int nch_max = (nchunks + cs - 1) / cs;
@@ -299,7 +306,8 @@ bn_status plan(int mode, Args *a, Launch *l)
         if (consumers > kMaxConsumers)
             return fail(BN_ERR_UNSUPPORTED, "row of %d chunks needs %d consumer threads", nch_max, consumers);
         const int stage_bytes = round_up(nch_max * 16 * (sum_in ? 2 : 1), 128);
-        const int overhead = (int)SmemLayout::make(0, stage_bytes).total + 2 * 16;
+        const int gamma_bytes = gamma_slot_bytes(mode, cpt, consumers);
+        const int overhead = (int)SmemLayout::make(0, stage_bytes, gamma_bytes).total + 2 * 16;
         const int cta_max = d->smem_optin - 1024;  // room for the kernel's static shared memory
 
         Launch L;
@@ -309,7 +317,7 @@ bn_status plan(int mode, Args *a, Launch *l)
         // CTAs per SM that registers and threads allow (probe with a 2-stage ring)
         Launch probe = L;
         probe.cluster = 1;
-        probe.smem = SmemLayout::make(2, stage_bytes).total;
+        probe.smem = SmemLayout::make(2, stage_bytes, gamma_bytes).total;
         int resident_probe = 0;
         BN_TRY(resident_clusters(mode, probe, &resident_probe));
         int by_regs = resident_probe / (d->sms > 0 ? d->sms : 1);
@@ -329,10 +337,11 @@ bn_status plan(int mode, Args *a, Launch *l)
         }
         if (stages > kMaxStages) stages = kMaxStages;
         if (stages < 2) stages = 2;
-        while (stages > 2 && (int)SmemLayout::make(stages, stage_bytes).total > cta_max) --stages;
-        if ((int)SmemLayout::make(stages, stage_bytes).total > cta_max)
+        while (stages > 2 && (int)SmemLayout::make(stages, stage_bytes, gamma_bytes).total > cta_max)
+            --stages;
+        if ((int)SmemLayout::make(stages, stage_bytes, gamma_bytes).total > cta_max)
             return fail(BN_ERR_UNSUPPORTED, "stage of %d bytes does not fit shared memory", stage_bytes);
-        L.smem = SmemLayout::make(stages, stage_bytes).total;
+        L.smem = SmemLayout::make(stages, stage_bytes, gamma_bytes).total;
 
         int resident = 0;
         BN_TRY(resident_clusters(mode, L, &resident));
@@ -345,6 +354,8 @@ bn_status plan(int mode, Args *a, Launch *l)
         *l = L;
         a->stages = stages;
         a->stage_bytes = stage_bytes;
+        a->gamma_bytes = gamma_bytes;
+        a->spin_wait = g_tune_wait.load() == 2 ? 1 : 0;
         a->nchunks = nchunks;
         a->err = d->err;
         return BN_OK;
@@ -700,7 +711,7 @@ const char *bn_status_string(bn_status status)
 
 int bn_version(void) { return kVersion; }
 
-bn_status bn_set_tuning(int cluster_size, int stages, int threads, int ctas_per_sm)
+bn_status bn_set_tuning(int cluster_size, int stages, int threads, int ctas_per_sm, int wait_mode)
 {
     g_msg[0] = '\0';
     if (cluster_size != 0 && cluster_size != 1 && cluster_size != 2 && cluster_size != 4 &&
@@ -712,6 +723,9 @@ bn_status bn_set_tuning(int cluster_size, int stages, int threads, int ctas_per_
         return fail(BN_ERR_INVALID, "threads must be 0 or a multiple of 32 up to %d", kMaxConsumers);
     if (ctas_per_sm < 0 || ctas_per_sm > 8)
         return fail(BN_ERR_INVALID, "ctas_per_sm must be in [0, 8]");
+    if (wait_mode < 0 || wait_mode > 2)
+        return fail(BN_ERR_INVALID, "wait_mode must be 0, 1 or 2");
+    g_tune_wait.store(wait_mode);
     g_tune_cluster.store(cluster_size);
     g_tune_ctas.store(ctas_per_sm);
     g_tune_stages.store(stages);

@@ -126,6 +126,31 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
         : "memory");
     return done != 0;
 }
+// Non-suspending probes of the same phases (used when spin_wait is set).
+__device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ bool mbar_probe_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
 __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank)
 {
     uint32_t r;
@@ -173,7 +198,15 @@ __device__ __forceinline__ void consumer_sync(int nthreads)
 struct Ctl {
     volatile int *abort;  // shared flag: set once any wait of this CTA expired
     unsigned *err;        // device error word
+    bool spin;            // poll with test_wait instead of the suspending try_wait
 };
+
+template <bool CLUSTER_ACQUIRE>
+__device__ __forceinline__ bool phase_done(uint32_t bar, uint32_t parity, bool spin)
+{
+    if (spin) return CLUSTER_ACQUIRE ? mbar_probe_cluster(bar, parity) : mbar_probe(bar, parity);
+    return CLUSTER_ACQUIRE ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity);
+}
 
 // Wait for the phase of `bar` with parity `parity` to complete.  Returns false
 // (without waiting) once the CTA is aborting, or after the time limit, in
@@ -182,10 +215,10 @@ template <bool CLUSTER_ACQUIRE, bool HONOR_ABORT>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl &c)
 {
     if (HONOR_ABORT && *c.abort) return false;
-    if (CLUSTER_ACQUIRE ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
+    if (phase_done<CLUSTER_ACQUIRE>(bar, parity, c.spin)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1; i < kMaxSpins; ++i) {
-        if (CLUSTER_ACQUIRE ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
+        if (phase_done<CLUSTER_ACQUIRE>(bar, parity, c.spin)) return true;
         if ((i & 15u) == 0u) {
             if (HONOR_ABORT && *c.abort) return false;
             if (globaltimer() - t0 > kWaitLimitNs) break;
@@ -291,16 +324,6 @@ __device__ __forceinline__ uint32_t round2(f2 v)
 __device__ __forceinline__ uint4 round8(const f2 *v)
 {
     return make_uint4(round2(v[0]), round2(v[1]), round2(v[2]), round2(v[3]));
-}
-
-__device__ __forceinline__ void load_gamma8(const float *g, f2 *out)
-{
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(g));
-    const float4 b = __ldg(reinterpret_cast<const float4 *>(g) + 1);
-    out[0] = f2_make(a.x, a.y);
-    out[1] = f2_make(a.z, a.w);
-    out[2] = f2_make(b.x, b.y);
-    out[3] = f2_make(b.z, b.w);
 }
 
 // s + e == a + b exactly (Knuth's two-sum; no ordering assumption).
@@ -428,7 +451,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
 
-    const SmemLayout L = SmemLayout::make(a.stages, a.stage_bytes);
+    const SmemLayout L = SmemLayout::make(a.stages, a.stage_bytes, a.gamma_bytes);
     Smem sm;
     sm.stages = smem + L.stages_off;
     sm.stages_u32 = smem_addr(sm.stages);
@@ -473,7 +496,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
     fence_mbarrier_init();
     __syncthreads();
     if (cs > 1) cluster_sync_all();
-    const Ctl ctl{&s_abort, a.err};
+    const Ctl ctl{&s_abort, a.err, a.spin_wait != 0};
 
     if (warp == NW) {
         // ================= producer warp =================
@@ -600,6 +623,37 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
         };
         auto chunk = [&](const uint8_t *p, int lc) -> uint4 {
             return *reinterpret_cast<const uint4 *>(p + (size_t)lc * 16);
+        };
+        // Gamma slots: each consumer thread copies the gammas of its own chunks
+        // into shared memory once, laid out so that a warp's 16-byte reads are
+        // contiguous; it alone reads them back (no barrier needed).
+        //   slot (g, i, half) = gsm[((g * CPT + i) * 2 + half) * NT + tid]
+        float4 *gsm = reinterpret_cast<float4 *>(smem + L.gamma_off);
+        constexpr int kGPost = 0;
+        constexpr int kGPre = POSTNORM ? 1 : 0;
+        if constexpr (RESNORM) {
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) {
+                const int lc = tid + i * NT;
+                if (lc < nch) {
+                    const float4 *gq = reinterpret_cast<const float4 *>(a.gamma_pre + (size_t)(c0 + lc) * 8);
+                    gsm[((kGPre * CPT + i) * 2 + 0) * NT + tid] = __ldg(gq);
+                    gsm[((kGPre * CPT + i) * 2 + 1) * NT + tid] = __ldg(gq + 1);
+                    if constexpr (POSTNORM) {
+                        const float4 *gp = reinterpret_cast<const float4 *>(a.gamma_post + (size_t)(c0 + lc) * 8);
+                        gsm[((kGPost * CPT + i) * 2 + 0) * NT + tid] = __ldg(gp);
+                        gsm[((kGPost * CPT + i) * 2 + 1) * NT + tid] = __ldg(gp + 1);
+                    }
+                }
+            }
+        }
+        auto gamma8 = [&](int g, int i, f2 *out) {
+            const float4 x = gsm[((g * CPT + i) * 2 + 0) * NT + tid];
+            const float4 y = gsm[((g * CPT + i) * 2 + 1) * NT + tid];
+            out[0] = f2_make(x.x, x.y);
+            out[1] = f2_make(x.z, x.w);
+            out[2] = f2_make(y.x, y.y);
+            out[3] = f2_make(y.z, y.w);
         };
 
         for (int t = cl, it = 0; t < a.T; t += ncl, ++it) {
@@ -769,7 +823,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                         const int lc = tid + i * NT;
                         if (lc < nch) {
                             f2 g[4];
-                            load_gamma8(a.gamma_post + (size_t)(c0 + lc) * 8, g);
+                            gamma8(kGPost, i, g);
 #pragma unroll
                             for (int m = 0; m < 4; ++m) s[i][m] = mul_sep2(mul2(s[i][m], r1x2), g[m]);
                         }
@@ -805,7 +859,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                     const int lc = tid + i * NT;
                     if (lc < nch) {
                         f2 g[4], o[4];
-                        load_gamma8(a.gamma_pre + (size_t)(c0 + lc) * 8, g);
+                        gamma8(kGPre, i, g);
 #pragma unroll
                         for (int m = 0; m < 4; ++m) o[m] = mul2(mul2(s[i][m], r2x2), g[m]);
                         if (live)

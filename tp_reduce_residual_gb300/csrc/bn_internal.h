@@ -55,6 +55,8 @@ struct Args {
     int nchunks;              // H / 8 sixteen-byte chunks per row
     int stages;               // pipeline depth
     int stage_bytes;          // bytes of one stage (multiple of 128)
+    int gamma_bytes;          // shared-memory bytes of the per-thread gamma slots
+    int spin_wait;            // 1: poll barriers with test_wait; 0: try_wait
     float eps;
 };
 
@@ -69,11 +71,12 @@ struct Launch {
 
 // Dynamic shared-memory layout, identical on host and device.
 struct SmemLayout {
-    uint32_t stages_off, bars_off, red_off, xslot_off, meta_off, total;
-    __host__ __device__ static SmemLayout make(int stages, int stage_bytes) {
+    uint32_t stages_off, gamma_off, bars_off, red_off, xslot_off, meta_off, total;
+    __host__ __device__ static SmemLayout make(int stages, int stage_bytes, int gamma_bytes) {
         SmemLayout L;
         L.stages_off = 0;
-        L.bars_off = (uint32_t)stages * (uint32_t)stage_bytes;            // 128-aligned
+        L.gamma_off = (uint32_t)stages * (uint32_t)stage_bytes;           // 128-aligned
+        L.bars_off = L.gamma_off + (((uint32_t)gamma_bytes + 127u) & ~127u);
         uint32_t nbars = 2u * (uint32_t)stages + 6u;                      // full, empty, meta x2 x2, exchange x2
         L.red_off = L.bars_off + ((nbars * 8u + 15u) & ~15u);
         L.xslot_off = L.red_off + 2u * 32u * 8u;                          // float2 [2][32]
@@ -82,6 +85,14 @@ struct SmemLayout {
         return L;
     }
 };
+
+// Shared-memory bytes of the gamma slots: 32 bytes per chunk per gamma.
+__host__ __device__ inline int gamma_slot_bytes(int mode, int cpt, int consumers)
+{
+    if (!(mode & F_RESNORM)) return 0;
+    const int ngamma = (mode & F_POSTNORM) ? 2 : 1;
+    return ngamma * 32 * cpt * consumers;
+}
 
 // Per-mode host entry points, defined in the kernel translation units:
 //   launch_<mode>     enqueue the kernel with the given launch shape;
