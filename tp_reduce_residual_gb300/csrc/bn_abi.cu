@@ -293,10 +293,11 @@ bn_status plan(int mode, Args *a, Launch *l)
     int cs = g_tune_cluster.load();
     if (cs <= 0) cs = auto_cluster(T, nchunks, d->sms, (long long)per_row * 2 * H);
     if (cs > nchunks) cs = 1;
-    const int cap = g_tune_threads.load() > 0 ? g_tune_threads.load() : kMaxConsumers;
+    // measured on GB300: the finalize modes run best with 512 consumer threads
+    // (one CTA per SM), the reduce modes with 256 and several CTAs per SM
+    const int cap = g_tune_threads.load() > 0 ? g_tune_threads.load() : (fin ? kMaxConsumers : 256);
     const int want_stages = g_tune_stages.load();
     const int want_ctas = g_tune_ctas.load();
-    (void)fin;
 
     for (;; cs /= 2) {
         const int nch_max = (nchunks + cs - 1) / cs;

@@ -30,7 +30,7 @@
 //     FP32 rounding of the exact sum, independent of the row's split.
 //   * Cluster partial sums travel through distributed shared memory (remote
 //     st.shared::cluster plus a remote mbarrier arrive) -- no global scratch.
-//   * Every wait is bounded in time; on expiry the kernel records an error bit,
+//   * Every wait is bounded (SM cycles and polls); on expiry the kernel records an error bit,
 //     stops issuing copies, drains the copies it has in flight, runs the rest of
 //     its control flow without waiting and without storing, and returns.
 #pragma once
@@ -43,7 +43,8 @@
 namespace bn {
 namespace dev {
 
-constexpr unsigned long long kWaitLimitNs = 250ull * 1000ull * 1000ull;  // 250 ms
+// A wait gives up after 2^29 SM cycles (about 0.26 s at 2 GHz) or 2^26 polls.
+constexpr long long kWaitLimitCycles = 1ll << 29;
 constexpr uint32_t kMaxSpins = 1u << 26;
 constexpr unsigned kErrPerm = 1u;
 constexpr unsigned kErrTimeout = 2u;
@@ -53,13 +54,6 @@ constexpr unsigned kErrTimeout = 2u;
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t globaltimer()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -211,17 +205,22 @@ __device__ __forceinline__ bool phase_done(uint32_t bar, uint32_t parity, bool s
 // Wait for the phase of `bar` with parity `parity` to complete.  Returns false
 // (without waiting) once the CTA is aborting, or after the time limit, in
 // which case it records the timeout and starts the abort.
+// The clock is read only after 1024 unsuccessful polls: a wait that ends
+// quickly costs nothing but the polls themselves.
 template <bool CLUSTER_ACQUIRE, bool HONOR_ABORT>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl &c)
 {
     if (HONOR_ABORT && *c.abort) return false;
     if (phase_done<CLUSTER_ACQUIRE>(bar, parity, c.spin)) return true;
-    const uint64_t t0 = globaltimer();
+    long long t0 = 0;
     for (uint32_t i = 1; i < kMaxSpins; ++i) {
         if (phase_done<CLUSTER_ACQUIRE>(bar, parity, c.spin)) return true;
-        if ((i & 15u) == 0u) {
+        if ((i & 1023u) == 0u) {
             if (HONOR_ABORT && *c.abort) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) break;
+            if (i == 1024u)
+                t0 = clock64();
+            else if (clock64() - t0 > kWaitLimitCycles)
+                break;
         }
     }
     atomicOr(c.err, kErrTimeout);
