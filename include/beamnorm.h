@@ -188,15 +188,20 @@ BN_API const char *bn_status_string(bn_status status);
 /* Library version, major * 10000 + minor * 100 + patch. */
 BN_API int bn_version(void);
 
-/* Launch-shape overrides for measurement sweeps (process-wide; 0 = automatic):
- * cluster_size in {1,2,4,8,16} CTAs per token row, stages = pipeline depth,
- * threads = consumer threads per CTA (a multiple of 32, at most 512),
- * ctas_per_sm = CTAs sharing one SM (at most 8; capped by what registers
- * allow), wait_mode = how threads wait for a pipeline stage (1: suspending
- * try_wait, 2: polling test_wait).  Results do not depend on these settings,
- * only speed does. */
-BN_API bn_status bn_set_tuning(int cluster_size, int stages, int threads, int ctas_per_sm,
-                               int wait_mode);
+/* Launch-shape overrides for measurement sweeps (process-wide).  Every field
+ * 0 means automatic.  Results do not depend on these settings, only speed. */
+typedef struct {
+    int cluster_size;  /* CTAs per token row: 1, 2, 4, 8 or 16 */
+    int stages;        /* pipeline depth in stages, at most 64 */
+    int threads;       /* consumer threads per CTA: a multiple of 32, at most 512 */
+    int ctas_per_sm;   /* CTAs sharing one SM, at most 8 (capped by registers) */
+    int wait_mode;     /* 1: suspending try_wait, 2: polling test_wait */
+    int group;         /* row copies per pipeline stage, at most 64 */
+} bn_tuning;
+
+/* Set the overrides; NULL restores automatic choices.  BN_ERR_INVALID on an
+ * out-of-range field (nothing changes then). */
+BN_API bn_status bn_set_tuning(const bn_tuning *tuning);
 
 #ifdef __cplusplus
 }

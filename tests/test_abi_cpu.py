@@ -133,14 +133,17 @@ def test_split_and_finalize_only_reject_bad_arguments(L):
 
 
 def test_set_tuning_validates(L):
-    assert L.bn_set_tuning(3, 0, 0, 0, 0) == bn.ERR_INVALID
-    assert L.bn_set_tuning(0, 1, 0, 0, 0) == bn.ERR_INVALID
-    assert L.bn_set_tuning(0, 65, 0, 0, 0) == bn.ERR_INVALID
-    assert L.bn_set_tuning(0, 0, 48, 0, 0) == bn.ERR_INVALID
-    assert L.bn_set_tuning(0, 0, 0, 9, 0) == bn.ERR_INVALID
-    assert L.bn_set_tuning(0, 0, 0, 0, 3) == bn.ERR_INVALID
-    assert L.bn_set_tuning(16, 8, 256, 2, 2) == bn.OK
-    assert L.bn_set_tuning(0, 0, 0, 0, 0) == bn.OK
+    def st(*fields):
+        return L.bn_set_tuning(ctypes.byref(bn._Tuning(*fields)))
+    assert st(3, 0, 0, 0, 0, 0) == bn.ERR_INVALID
+    assert st(0, 1, 0, 0, 0, 0) == bn.ERR_INVALID
+    assert st(0, 65, 0, 0, 0, 0) == bn.ERR_INVALID
+    assert st(0, 0, 48, 0, 0, 0) == bn.ERR_INVALID
+    assert st(0, 0, 0, 9, 0, 0) == bn.ERR_INVALID
+    assert st(0, 0, 0, 0, 3, 0) == bn.ERR_INVALID
+    assert st(0, 0, 0, 0, 0, 65) == bn.ERR_INVALID
+    assert st(16, 8, 256, 2, 2, 4) == bn.OK
+    assert L.bn_set_tuning(None) == bn.OK
 
 
 def test_python_binding_checks_before_calling(L):

@@ -167,32 +167,33 @@ def test_decline_then_fallback_gives_the_same_bits():
 
 # ---- launch shapes, streams, graphs ------------------------------------------------------
 
-@pytest.mark.parametrize("cluster,stages,threads,ctas,wait", [
-    (1, 0, 0, 0, 0), (2, 0, 0, 0, 0), (4, 3, 0, 0, 2), (8, 0, 0, 0, 0), (16, 2, 0, 0, 2),
-    (1, 2, 0, 0, 1), (1, 7, 0, 0, 2), (1, 0, 256, 0, 0), (1, 0, 128, 0, 2), (2, 5, 64, 0, 0),
-    (1, 0, 128, 3, 0), (1, 4, 64, 4, 2),
+@pytest.mark.parametrize("cluster,stages,threads,ctas,wait,group", [
+    (1, 0, 0, 0, 0, 0), (2, 0, 0, 0, 0, 1), (4, 3, 0, 0, 2, 0), (8, 0, 0, 0, 0, 7),
+    (16, 2, 0, 0, 2, 0), (1, 2, 0, 0, 1, 1), (1, 7, 0, 0, 2, 3), (1, 0, 256, 0, 0, 11),
+    (1, 0, 128, 0, 2, 0), (2, 5, 64, 0, 0, 64), (1, 0, 128, 3, 0, 2), (1, 4, 64, 4, 2, 5),
 ])
-def test_launch_shapes_give_identical_bits(cluster, stages, threads, ctas, wait):
+def test_launch_shapes_give_identical_bits(cluster, stages, threads, ctas, wait, group):
     wl = inputs.custom("finalize_reduce_norm", 8, 8192, 10, partial_std=0.3)
     d = parity.gpu_inputs(wl, 21, seed=77)
     try:
-        bn.set_tuning(cluster, stages, threads, ctas, wait)
+        bn.set_tuning(cluster, stages, threads, ctas, wait, group)
         g = parity.run_fused(d)
     finally:
         bn.set_tuning()
     base = parity.run_fused(d)
     for key in ("sum", "ss", "z", "out", "residual_out"):
         assert_bits_equal(g[key], base[key], key)
-    parity.compare(g, parity.run_oracle(d), what=f"cluster={cluster} stages={stages} ctas={ctas}")
+    parity.compare(g, parity.run_oracle(d), what=f"cluster={cluster} stages={stages} ctas={ctas} group={group}")
 
 
 def test_reduce_launch_shapes_give_identical_bits():
     wl = inputs.custom("reduce_norm", 8, 5120, row_scale=True)
     d = parity.gpu_inputs(wl, 45, seed=78)
     base = parity.run_fused(d)
-    for cluster, threads, ctas in ((2, 0, 0), (4, 0, 0), (16, 0, 0), (1, 512, 1), (1, 64, 4)):
+    for cluster, threads, ctas, group in ((2, 0, 0, 0), (4, 0, 0, 3), (16, 0, 0, 9), (1, 512, 1, 1),
+                                          (1, 64, 4, 2)):
         try:
-            bn.set_tuning(cluster, 0, threads, ctas)
+            bn.set_tuning(cluster, 0, threads, ctas, 0, group)
             g = parity.run_fused(d)
         finally:
             bn.set_tuning()

@@ -45,6 +45,11 @@ _STATUS_NAMES = {OK: "BN_OK", ERR_INVALID: "BN_ERR_INVALID", ERR_UNSUPPORTED: "B
                  ERR_CUDA: "BN_ERR_CUDA", ERR_DEVICE: "BN_ERR_DEVICE"}
 
 
+class _Tuning(ctypes.Structure):
+    _fields_ = [("cluster_size", ctypes.c_int), ("stages", ctypes.c_int), ("threads", ctypes.c_int),
+                ("ctas_per_sm", ctypes.c_int), ("wait_mode", ctypes.c_int), ("group", ctypes.c_int)]
+
+
 class _Debug(ctypes.Structure):
     _fields_ = [("sum", ctypes.c_void_p), ("ss", ctypes.c_void_p), ("z", ctypes.c_void_p)]
 
@@ -91,7 +96,7 @@ def load() -> ctypes.CDLL:
             "bn_last_error": [],
             "bn_status_string": [_I],
             "bn_version": [],
-            "bn_set_tuning": [_I, _I, _I, _I, _I],
+            "bn_set_tuning": [ctypes.POINTER(_Tuning)],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -324,10 +329,11 @@ def check_device_error(stream=None, raise_on_error: bool = True) -> int:
 
 
 def set_tuning(cluster_size: int = 0, stages: int = 0, threads: int = 0, ctas_per_sm: int = 0,
-               wait_mode: int = 0) -> None:
+               wait_mode: int = 0, group: int = 0) -> None:
     """Override the launch shape for measurement sweeps (0 = automatic)."""
-    _check(load().bn_set_tuning(int(cluster_size), int(stages), int(threads), int(ctas_per_sm),
-                                int(wait_mode)))
+    t = _Tuning(int(cluster_size), int(stages), int(threads), int(ctas_per_sm), int(wait_mode),
+                int(group))
+    _check(load().bn_set_tuning(ctypes.byref(t)))
 
 
 def version() -> int:

@@ -49,7 +49,7 @@ bn_status cuda_fail(cudaError_t e, const char *what)
 // ---- tuning overrides (process-wide) -------------------------------------------
 
 std::atomic<int> g_tune_cluster{0}, g_tune_stages{0}, g_tune_threads{0}, g_tune_ctas{0},
-    g_tune_wait{0};
+    g_tune_wait{0}, g_tune_group{0};
 
 // ---- per-device state ------------------------------------------------------------
 
@@ -306,7 +306,15 @@ bn_status plan(int mode, Args *a, Launch *l)
         const int consumers = round_up((nch_max + cpt - 1) / cpt, 32);
         if (consumers > kMaxConsumers)
             return fail(BN_ERR_UNSUPPORTED, "row of %d chunks needs %d consumer threads", nch_max, consumers);
-        const int stage_bytes = round_up(nch_max * 16 * (sum_in ? 2 : 1), 128);
+        // one stage holds `group` row copies of item_bytes each; ~32 KB stages
+        // amortise the stage handshake while keeping several stages in flight
+        const int item_bytes = round_up(nch_max * 16 * (sum_in ? 2 : 1), 128);
+        int group = g_tune_group.load() > 0 ? g_tune_group.load() : (32 * 1024) / item_bytes;
+        if (sum_in) group = 1;  // the FP32 sum and the BF16 residual differ in size
+        if (group > per_row) group = per_row;
+        if (group < 1) group = 1;
+        const int stage_bytes = group * item_bytes;
+        const int stages_per_row = (per_row + group - 1) / group;
         const int gamma_bytes = gamma_slot_bytes(mode, cpt, consumers);
         const int overhead = (int)SmemLayout::make(0, stage_bytes, gamma_bytes).total + 2 * 16;
         const int cta_max = d->smem_optin - 1024;  // room for the kernel's static shared memory
@@ -333,7 +341,7 @@ bn_status plan(int mode, Args *a, Launch *l)
             stages = want_stages;
         } else {
             stages = (per_cta - overhead) / stage_bytes;
-            const int ahead = 2 * per_row + 2;
+            const int ahead = 2 * stages_per_row + 2;
             if (stages > ahead) stages = ahead;
         }
         if (stages > kMaxStages) stages = kMaxStages;
@@ -355,6 +363,8 @@ bn_status plan(int mode, Args *a, Launch *l)
         *l = L;
         a->stages = stages;
         a->stage_bytes = stage_bytes;
+        a->group = group;
+        a->item_bytes = item_bytes;
         a->gamma_bytes = gamma_bytes;
         a->spin_wait = g_tune_wait.load() == 2 ? 1 : 0;
         a->nchunks = nchunks;
@@ -712,25 +722,31 @@ const char *bn_status_string(bn_status status)
 
 int bn_version(void) { return kVersion; }
 
-bn_status bn_set_tuning(int cluster_size, int stages, int threads, int ctas_per_sm, int wait_mode)
+bn_status bn_set_tuning(const bn_tuning *t)
 {
     g_msg[0] = '\0';
-    if (cluster_size != 0 && cluster_size != 1 && cluster_size != 2 && cluster_size != 4 &&
-        cluster_size != 8 && cluster_size != 16)
+    bn_tuning z;
+    std::memset(&z, 0, sizeof z);
+    if (!t) t = &z;
+    const int cs = t->cluster_size;
+    if (cs != 0 && cs != 1 && cs != 2 && cs != 4 && cs != 8 && cs != 16)
         return fail(BN_ERR_INVALID, "cluster_size must be 0, 1, 2, 4, 8 or 16");
-    if (stages < 0 || stages > kMaxStages || stages == 1)
+    if (t->stages < 0 || t->stages > kMaxStages || t->stages == 1)
         return fail(BN_ERR_INVALID, "stages must be 0 or in [2, %d]", kMaxStages);
-    if (threads < 0 || threads > kMaxConsumers || threads % 32 != 0)
+    if (t->threads < 0 || t->threads > kMaxConsumers || t->threads % 32 != 0)
         return fail(BN_ERR_INVALID, "threads must be 0 or a multiple of 32 up to %d", kMaxConsumers);
-    if (ctas_per_sm < 0 || ctas_per_sm > 8)
+    if (t->ctas_per_sm < 0 || t->ctas_per_sm > 8)
         return fail(BN_ERR_INVALID, "ctas_per_sm must be in [0, 8]");
-    if (wait_mode < 0 || wait_mode > 2)
+    if (t->wait_mode < 0 || t->wait_mode > 2)
         return fail(BN_ERR_INVALID, "wait_mode must be 0, 1 or 2");
-    g_tune_wait.store(wait_mode);
-    g_tune_cluster.store(cluster_size);
-    g_tune_ctas.store(ctas_per_sm);
-    g_tune_stages.store(stages);
-    g_tune_threads.store(threads);
+    if (t->group < 0 || t->group > 64)
+        return fail(BN_ERR_INVALID, "group must be in [0, 64]");
+    g_tune_cluster.store(cs);
+    g_tune_stages.store(t->stages);
+    g_tune_threads.store(t->threads);
+    g_tune_ctas.store(t->ctas_per_sm);
+    g_tune_wait.store(t->wait_mode);
+    g_tune_group.store(t->group);
     return BN_OK;
 }
 

@@ -497,9 +497,21 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
     if (cs > 1) cluster_sync_all();
     const Ctl ctl{&s_abort, a.err, a.spin_wait != 0};
 
+    // Copies per token row ("items"), in the order both sides walk them:
+    //   FIN:    for each shard r: its k gathered rows, then its shared row;
+    //   reduce: the R shard rows;  norm only: the FP32 sum row;
+    //   then the residual row when the epilogue runs.
+    // A stage holds up to G = a.group consecutive items of one row (one
+    // barrier for all of them); a row always ends on a stage boundary.
+    const int per_shard = FIN ? a.k + (has_shared ? 1 : 0) : 1;
+    const int row_items = (SUM_IN ? 1 : a.R * per_shard) + (RESNORM ? 1 : 0);
+    const int G = a.group;
+    const uint32_t item_bytes = (uint32_t)a.item_bytes;
+
     if (warp == NW) {
         // ================= producer warp =================
-        uint32_t stage = 0, phase = 0, issued = 0;
+        uint32_t stage = 0, phase = 0, issued = 0;  // issued = stages armed
+        int pos = 0, n_in = 0;                      // item slot in the armed stage
         bool ok = true;
         // Gather indices and weights of a row are loaded into registers one row
         // ahead (all lanes, up to 8 slots per lane), so their latency overlaps
@@ -554,46 +566,66 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                 prefetch_meta(t + ncl);
             }
             if (lane == 0) {
-                auto issue = [&](const void *src, uint32_t bytes) -> bool {
-                    if (!wait_phase<false, true>(sm.empty0 + 8u * stage, phase ^ 1u, ctl)) return false;
+                int left = row_items;
+                // one copy into the next item slot; a stage is armed (its
+                // expected byte count set) when its first item is issued.  All
+                // items of a stage have the same size (a group of more than one
+                // item never holds the FP32 sum).
+                auto put = [&](const void *src, uint32_t bytes) -> bool {
                     const uint32_t fb = sm.full0 + 8u * stage;
-                    mbar_arrive_expect_tx(fb, bytes);
-                    bulk_g2s(sm.stages_u32 + stage * (uint32_t)a.stage_bytes, src, bytes, fb);
-                    ++issued;
-                    if (++stage == (uint32_t)S) {
-                        stage = 0;
-                        phase ^= 1u;
+                    if (pos == 0) {
+                        n_in = left < G ? left : G;
+                        if (!wait_phase<false, true>(sm.empty0 + 8u * stage, phase ^ 1u, ctl)) return false;
+                        mbar_arrive_expect_tx(fb, bytes * (uint32_t)n_in);
+                        ++issued;
+                    }
+                    bulk_g2s(sm.stages_u32 + stage * (uint32_t)a.stage_bytes + (uint32_t)pos * item_bytes,
+                             src, bytes, fb);
+                    --left;
+                    if (++pos == n_in) {
+                        pos = 0;
+                        if (++stage == (uint32_t)S) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
                     return true;
                 };
                 const uint32_t bytes16 = (uint32_t)nch * 16u;
                 const size_t col = (size_t)c0 * 8u;
                 if constexpr (SUM_IN) {
-                    ok = issue(a.sum_in + (size_t)t * H + col, bytes16 * 2u);
+                    ok = put(a.sum_in + (size_t)t * H + col, bytes16 * 2u);
                 } else if constexpr (FIN) {
                     const int32_t *mp = sm.mperm + slot * kMaxMeta;
                     for (int r = 0; r < a.R && ok; ++r) {
                         const uint16_t *xr = a.src + (size_t)r * a.T * a.k * H;
                         for (int j = 0; j < a.k && ok; ++j)
-                            ok = issue(xr + (size_t)mp[r * a.k + j] * H + col, bytes16);
+                            ok = put(xr + (size_t)mp[r * a.k + j] * H + col, bytes16);
                         if (ok && has_shared)
-                            ok = issue(a.shared + ((size_t)r * a.T + t) * H + col, bytes16);
+                            ok = put(a.shared + ((size_t)r * a.T + t) * H + col, bytes16);
                     }
                 } else {
                     for (int r = 0; r < a.R && ok; ++r)
-                        ok = issue(a.src + ((size_t)r * a.T + t) * H + col, bytes16);
+                        ok = put(a.src + ((size_t)r * a.T + t) * H + col, bytes16);
                 }
                 if constexpr (RESNORM) {
-                    if (ok) ok = issue(a.residual + (size_t)t * H + col, bytes16);
+                    if (ok) ok = put(a.residual + (size_t)t * H + col, bytes16);
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         }
-        // drain: wait (bounded, even when aborting) for every copy still in flight
+        // drain: wait (bounded, even when aborting) for every stage still in
+        // flight, including one left partly issued by an abort
         if (lane == 0) {
             const uint32_t n = issued < (uint32_t)S ? issued : (uint32_t)S;
             uint32_t st = stage, ph = phase;
-            for (uint32_t i = 0; i < n; ++i) {
+            if (pos != 0) {
+                // the armed stage never completes its byte count: give its
+                // issued copies the bounded time to land
+                wait_phase<false, false>(sm.full0 + 8u * st, ph, ctl);
+            }
+            const uint32_t done_n = pos != 0 ? n - 1 : n;
+            for (uint32_t i = 0; i < done_n; ++i) {
                 if (st == 0) {
                     st = (uint32_t)S - 1u;
                     ph ^= 1u;
@@ -608,16 +640,28 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
         uint32_t stage = 0, phase = 0;
         int nred = 0;
         bool live = true;  // false once a wait failed: keep the control flow, store nothing
+        // item cursor: a stage is waited for when its first item is taken and
+        // released when its last item is done
+        int cpos = 0, cn = 0, cleft = 0;
+        const uint8_t *cbase = sm.stages;
         auto take = [&]() -> const uint8_t * {
-            if (!wait_phase<false, true>(sm.full0 + 8u * stage, phase, ctl)) live = false;
-            return sm.stages + (size_t)stage * (size_t)a.stage_bytes;
+            if (cpos == 0) {
+                cn = cleft < G ? cleft : G;
+                if (!wait_phase<false, true>(sm.full0 + 8u * stage, phase, ctl)) live = false;
+                cbase = sm.stages + (size_t)stage * (size_t)a.stage_bytes;
+            }
+            return cbase + (size_t)cpos * item_bytes;
         };
         auto release = [&]() {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sm.empty0 + 8u * stage);
-            if (++stage == (uint32_t)S) {
-                stage = 0;
-                phase ^= 1u;
+            --cleft;
+            if (++cpos == cn) {
+                cpos = 0;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sm.empty0 + 8u * stage);
+                if (++stage == (uint32_t)S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
         };
         auto chunk = [&](const uint8_t *p, int lc) -> uint4 {
@@ -657,6 +701,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
 
         for (int t = cl, it = 0; t < a.T; t += ncl, ++it) {
             const int slot = it & 1;
+            cleft = row_items;
             f2 s[CPT][4];
 #pragma unroll
             for (int i = 0; i < CPT; ++i)

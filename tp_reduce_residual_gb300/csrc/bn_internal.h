@@ -54,7 +54,9 @@ struct Args {
     int R, T, H, k;
     int nchunks;              // H / 8 sixteen-byte chunks per row
     int stages;               // pipeline depth
-    int stage_bytes;          // bytes of one stage (multiple of 128)
+    int stage_bytes;          // bytes of one stage = group * item_bytes
+    int group;                // row copies (items) per stage
+    int item_bytes;           // stride of one item in a stage (multiple of 128)
     int gamma_bytes;          // shared-memory bytes of the per-thread gamma slots
     int spin_wait;            // 1: poll barriers with test_wait; 0: try_wait
     float eps;
