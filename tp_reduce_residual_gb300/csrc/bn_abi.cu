@@ -313,11 +313,14 @@ bn_status plan(int mode, Args *a, Launch *l)
         if (sum_in) group = 1;  // the FP32 sum and the BF16 residual differ in size
         if (group > per_row) group = per_row;
         if (group < 1) group = 1;
+        const int gamma_bytes = gamma_slot_bytes(mode, cpt, consumers);
+        const int cta_max = d->smem_optin - 1024;  // room for the kernel's static shared memory
+        // a group is shrunk until two stages fit one CTA
+        while (group > 1 && (int)SmemLayout::make(2, group * item_bytes, gamma_bytes).total > cta_max)
+            --group;
         const int stage_bytes = group * item_bytes;
         const int stages_per_row = (per_row + group - 1) / group;
-        const int gamma_bytes = gamma_slot_bytes(mode, cpt, consumers);
         const int overhead = (int)SmemLayout::make(0, stage_bytes, gamma_bytes).total + 2 * 16;
-        const int cta_max = d->smem_optin - 1024;  // room for the kernel's static shared memory
 
         Launch L;
         L.cluster = cs;
