@@ -306,10 +306,12 @@ bn_status plan(int mode, Args *a, Launch *l)
         const int consumers = round_up((nch_max + cpt - 1) / cpt, 32);
         if (consumers > kMaxConsumers)
             return fail(BN_ERR_UNSUPPORTED, "row of %d chunks needs %d consumer threads", nch_max, consumers);
-        // one stage holds `group` row copies of item_bytes each; ~32 KB stages
-        // amortise the stage handshake while keeping several stages in flight
+        // one stage holds `group` row copies of item_bytes each.  Measured on
+        // GB300: the finalize modes gain from ~48 KB stages (fewer handshakes
+        // over their many gathered copies), the reduce modes run best with one
+        // copy per stage.
         const int item_bytes = round_up(nch_max * 16 * (sum_in ? 2 : 1), 128);
-        int group = g_tune_group.load() > 0 ? g_tune_group.load() : (32 * 1024) / item_bytes;
+        int group = g_tune_group.load() > 0 ? g_tune_group.load() : (fin ? (48 * 1024) / item_bytes : 1);
         if (sum_in) group = 1;  // the FP32 sum and the BF16 residual differ in size
         if (group > per_row) group = per_row;
         if (group < 1) group = 1;
