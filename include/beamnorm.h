@@ -197,6 +197,7 @@ typedef struct {
     int ctas_per_sm;   /* CTAs sharing one SM, at most 8 (capped by registers) */
     int wait_mode;     /* 1: suspending try_wait, 2: polling test_wait */
     int group;         /* row copies per pipeline stage, at most 64 */
+    int split;         /* finalize rows: 1 split by columns, 2 split by shard */
 } bn_tuning;
 
 /* Set the overrides; NULL restores automatic choices.  BN_ERR_INVALID on an

@@ -142,7 +142,8 @@ def test_set_tuning_validates(L):
     assert st(0, 0, 0, 9, 0, 0) == bn.ERR_INVALID
     assert st(0, 0, 0, 0, 3, 0) == bn.ERR_INVALID
     assert st(0, 0, 0, 0, 0, 65) == bn.ERR_INVALID
-    assert st(16, 8, 256, 2, 2, 4) == bn.OK
+    assert st(0, 0, 0, 0, 0, 0, 3) == bn.ERR_INVALID
+    assert st(16, 8, 256, 2, 2, 4, 2) == bn.OK
     assert L.bn_set_tuning(None) == bn.OK
 
 

@@ -186,6 +186,49 @@ def test_launch_shapes_give_identical_bits(cluster, stages, threads, ctas, wait,
     parity.compare(g, parity.run_oracle(d), what=f"cluster={cluster} stages={stages} ctas={ctas} group={group}")
 
 
+SPLIT_CASES = [
+    # (R, T, k, H, with_shared, single_norm)
+    (8, 1, 10, 8192, True, False),
+    (8, 3, 8, 6144, False, False),
+    (3, 5, 4, 1000, True, True),
+    (2, 7, 3, 256, True, False),
+    (16, 2, 16, 4096, True, False),
+    (4, 40, 6, 2048, True, False),   # more rows than one pass of clusters
+]
+
+
+@pytest.mark.parametrize("R,T,k,H,with_shared,single", SPLIT_CASES)
+def test_shard_split_matches_column_split_and_oracle(R, T, k, H, with_shared, single):
+    """A cluster that splits a row by shard (each CTA finalizes one shard over
+    the whole row, then the z rows are summed in rank order through
+    distributed shared memory) gives the bits of the column split."""
+    wl = inputs.custom("finalize_reduce_norm", R, H, k, partial_std=0.3, shared_std=0.3)
+    d = parity.gpu_inputs(wl, T, seed=500 + R * 13 + T, with_shared=with_shared)
+    try:
+        bn.set_tuning(split=2)
+        g = parity.run_fused(d, single=single)
+        bn.set_tuning(split=1)
+        base = parity.run_fused(d, single=single)
+    finally:
+        bn.set_tuning()
+    for key in ("sum", "ss", "z", "out", "residual_out"):
+        assert_bits_equal(g[key], base[key], key)
+    parity.compare(g, parity.run_oracle(d, single=single), what=f"split R={R} T={T} k={k} H={H}")
+
+
+def test_shard_split_finalize_only():
+    wl = inputs.WORKLOADS[4]
+    d = parity.gpu_inputs(wl, 4)
+    try:
+        bn.set_tuning(split=2)
+        z = bn.finalize_only(d["expert_out"], d["perm"], d["w"], d["shared"])
+        torch.cuda.synchronize()
+    finally:
+        bn.set_tuning()
+    assert bn.check_device_error() == 0
+    assert_bits_equal(inputs.u16(z), parity.run_oracle(d)["z"], "z")
+
+
 def test_reduce_launch_shapes_give_identical_bits():
     wl = inputs.custom("reduce_norm", 8, 5120, row_scale=True)
     d = parity.gpu_inputs(wl, 45, seed=78)

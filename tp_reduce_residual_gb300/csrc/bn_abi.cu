@@ -49,7 +49,7 @@ bn_status cuda_fail(cudaError_t e, const char *what)
 // ---- tuning overrides (process-wide) -------------------------------------------
 
 std::atomic<int> g_tune_cluster{0}, g_tune_stages{0}, g_tune_threads{0}, g_tune_ctas{0},
-    g_tune_wait{0}, g_tune_group{0};
+    g_tune_wait{0}, g_tune_group{0}, g_tune_split{0};
 
 // ---- per-device state ------------------------------------------------------------
 
@@ -210,7 +210,7 @@ const ModeOps &ops_for(int mode)
 
 // Occupancy answers are cached: (device, mode, shape) -> resident clusters.
 struct OccEntry {
-    int dev, mode, cluster, consumers, cpt;
+    int dev, mode, split, cluster, consumers, cpt;
     size_t smem;
     int clusters;
 };
@@ -228,7 +228,7 @@ bn_status resident_clusters(int mode, const Launch &l, int *out)
         std::lock_guard<std::mutex> g(g_occ_mu);
         for (int i = 0; i < g_occ_n; ++i) {
             const OccEntry &o = g_occ[i];
-            if (o.dev == dev && o.mode == mode && o.cluster == l.cluster &&
+            if (o.dev == dev && o.mode == mode && o.split == l.split && o.cluster == l.cluster &&
                 o.consumers == l.consumers && o.cpt == l.cpt && o.smem == l.smem) {
                 *out = o.clusters;
                 return BN_OK;
@@ -242,7 +242,8 @@ bn_status resident_clusters(int mode, const Launch &l, int *out)
     }
     {
         std::lock_guard<std::mutex> g(g_occ_mu);
-        if (g_occ_n < kOccCache) g_occ[g_occ_n++] = OccEntry{dev, mode, l.cluster, l.consumers, l.cpt, l.smem, n};
+        if (g_occ_n < kOccCache)
+            g_occ[g_occ_n++] = OccEntry{dev, mode, l.split, l.cluster, l.consumers, l.cpt, l.smem, n};
     }
     *out = n;
     return BN_OK;
@@ -265,10 +266,10 @@ int auto_cluster(int T, int nchunks, int sms, long long row_bytes)
 }
 
 // Copies the producer issues per token row.
-int loads_per_row(int mode, const Args &a)
+int loads_per_row(int mode, const Args &a, bool split)
 {
     if (mode & F_SUM_IN) return 2;
-    int n = (mode & F_FIN) ? a.R * (a.k + (a.shared ? 1 : 0)) : a.R;
+    int n = (mode & F_FIN) ? (split ? 1 : a.R) * (a.k + (a.shared ? 1 : 0)) : a.R;
     if (mode & F_RESNORM) n += 1;
     return n;
 }
@@ -281,100 +282,132 @@ int loads_per_row(int mode, const Args &a)
 //             per-row reductions of one CTA overlap another CTA's streaming;
 //   stages    the SM's shared memory split over those CTAs, capped at two rows
 //             of copies ahead.
-bn_status plan(int mode, Args *a, Launch *l)
+// One launch shape for a given row split.  Sets *resident to the clusters the
+// device holds at once (0: this shape cannot be resident).
+bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, Launch *l,
+                    int *resident)
 {
-    const DeviceInfo *d = nullptr;
-    BN_TRY(device_info(&d));
-    const int T = a->T, H = a->H;
+    const int H = a->H;
     const bool sum_in = (mode & F_SUM_IN) != 0;
     const bool fin = (mode & F_FIN) != 0;
     const int nchunks = H / 8;
-    const int per_row = loads_per_row(mode, *a);
-    int cs = g_tune_cluster.load();
-    if (cs <= 0) cs = auto_cluster(T, nchunks, d->sms, (long long)per_row * 2 * H);
-    if (cs > nchunks) cs = 1;
+    const int per_row = loads_per_row(mode, *a, split);
     // measured on GB300: the finalize modes run best with 512 consumer threads
     // (one CTA per SM), the reduce modes with 256 and several CTAs per SM
     const int cap = g_tune_threads.load() > 0 ? g_tune_threads.load() : (fin ? kMaxConsumers : 256);
     const int want_stages = g_tune_stages.load();
     const int want_ctas = g_tune_ctas.load();
+    *resident = 0;
 
+    // chunks one CTA's threads must cover: the column slice, or the whole row
+    // when a cluster splits rows by shard
+    const int nch_max = split ? nchunks : (nchunks + cs - 1) / cs;
+    int cpt = 1;
+    while (cpt < 8 && (nch_max + cpt - 1) / cpt > cap) cpt *= 2;
+    const int consumers = round_up((nch_max + cpt - 1) / cpt, 32);
+    if (consumers > kMaxConsumers)
+        return fail(BN_ERR_UNSUPPORTED, "row of %d chunks needs %d consumer threads", nch_max, consumers);
+    // one stage holds `group` row copies of item_bytes each.  Measured on
+    // GB300: the finalize modes gain from ~48 KB stages (fewer handshakes
+    // over their many gathered copies), the reduce modes run best with one
+    // copy per stage.
+    const int item_bytes = round_up(nch_max * 16 * (sum_in ? 2 : 1), 128);
+    int group = g_tune_group.load() > 0 ? g_tune_group.load() : (fin ? (48 * 1024) / item_bytes : 1);
+    if (sum_in || split) group = 1;  // items of different sizes in one row
+    if (group > per_row) group = per_row;
+    if (group < 1) group = 1;
+    const int gamma_bytes = gamma_slot_bytes(mode, cpt, consumers);
+    const int zbuf_bytes = (split && !(mode & F_Z_OUT)) ? round_up(nchunks * 16, 128) : 0;
+    const int cta_max = d->smem_optin - 1024;  // room for the kernel's static shared memory
+    // a group is shrunk until two stages fit one CTA
+    while (group > 1 &&
+           (int)SmemLayout::make(2, group * item_bytes, gamma_bytes, zbuf_bytes).total > cta_max)
+        --group;
+    const int stage_bytes = group * item_bytes;
+    const int stages_per_row = (per_row + group - 1) / group;
+    const int overhead = (int)SmemLayout::make(0, stage_bytes, gamma_bytes, zbuf_bytes).total + 2 * 16;
+
+    Launch L;
+    L.split = split ? 1 : 0;
+    L.cluster = cs;
+    L.consumers = consumers;
+    L.cpt = cpt;
+    // CTAs per SM that registers and threads allow (probe with a 2-stage ring)
+    Launch probe = L;
+    probe.cluster = 1;
+    probe.smem = SmemLayout::make(2, stage_bytes, gamma_bytes, zbuf_bytes).total;
+    int resident_probe = 0;
+    BN_TRY(resident_clusters(mode, probe, &resident_probe));
+    int by_regs = resident_probe / (d->sms > 0 ? d->sms : 1);
+    if (by_regs < 1) by_regs = 1;
+    int ctas = want_ctas > 0 ? want_ctas : (by_regs < 4 ? by_regs : 4);
+    if (ctas > by_regs) ctas = by_regs;
+    int per_cta = d->smem_per_sm / ctas - d->smem_reserved - 1024;
+    if (per_cta > cta_max) per_cta = cta_max;
+
+    int stages;
+    if (want_stages > 0) {
+        stages = want_stages;
+    } else {
+        stages = (per_cta - overhead) / stage_bytes;
+        const int ahead = 2 * stages_per_row + 2;
+        if (stages > ahead) stages = ahead;
+    }
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) stages = 2;
+    while (stages > 2 &&
+           (int)SmemLayout::make(stages, stage_bytes, gamma_bytes, zbuf_bytes).total > cta_max)
+        --stages;
+    if ((int)SmemLayout::make(stages, stage_bytes, gamma_bytes, zbuf_bytes).total > cta_max)
+        return fail(BN_ERR_UNSUPPORTED, "stage of %d bytes does not fit shared memory", stage_bytes);
+    L.smem = SmemLayout::make(stages, stage_bytes, gamma_bytes, zbuf_bytes).total;
+
+    BN_TRY(resident_clusters(mode, L, resident));
+    if (*resident <= 0) return BN_OK;
+    const int ncl = a->T < *resident ? a->T : *resident;
+    L.grid = ncl * cs;
+    *l = L;
+    a->stages = stages;
+    a->stage_bytes = stage_bytes;
+    a->group = group;
+    a->item_bytes = item_bytes;
+    a->gamma_bytes = gamma_bytes;
+    a->zbuf_bytes = zbuf_bytes;
+    a->spin_wait = g_tune_wait.load() == 2 ? 1 : 0;
+    a->nchunks = nchunks;
+    a->err = d->err;
+    return BN_OK;
+}
+
+// Launch shape: the row split (by shard for finalize rows when rows are few,
+// else by column slices over a cluster of `cs` CTAs), consumer threads, CTAs
+// per SM and pipeline depth; see shape_for.
+bn_status plan(int mode, Args *a, Launch *l)
+{
+    const DeviceInfo *d = nullptr;
+    BN_TRY(device_info(&d));
+    const int T = a->T, H = a->H;
+    const int nchunks = H / 8;
+    int resident = 0;
+
+    // shard split: finalize modes with an epilogue (or the finalize alone),
+    // R >= 2, and few rows (measured on GB300: one row then takes k + 1 copies
+    // per CTA instead of R * (k + 1))
+    const bool can_split = (mode & F_FIN) && (mode & (F_RESNORM | F_Z_OUT)) && a->R >= 2;
+    const int pref = g_tune_split.load();
+    const bool split = can_split && (pref == 2 || (pref == 0 && (long long)T * a->R <= 2LL * d->sms));
+    if (split) {
+        BN_TRY(shape_for(mode, a, d, true, a->R, l, &resident));
+        if (resident > 0) return BN_OK;
+    }
+
+    int cs = g_tune_cluster.load();
+    if (cs <= 0) cs = auto_cluster(T, nchunks, d->sms, (long long)loads_per_row(mode, *a, false) * 2 * H);
+    if (cs > nchunks) cs = 1;
     for (;; cs /= 2) {
-        const int nch_max = (nchunks + cs - 1) / cs;
-        int cpt = 1;
-        while (cpt < 8 && (nch_max + cpt - 1) / cpt > cap) cpt *= 2;
-        const int consumers = round_up((nch_max + cpt - 1) / cpt, 32);
-        if (consumers > kMaxConsumers)
-            return fail(BN_ERR_UNSUPPORTED, "row of %d chunks needs %d consumer threads", nch_max, consumers);
-        // one stage holds `group` row copies of item_bytes each.  Measured on
-        // GB300: the finalize modes gain from ~48 KB stages (fewer handshakes
-        // over their many gathered copies), the reduce modes run best with one
-        // copy per stage.
-        const int item_bytes = round_up(nch_max * 16 * (sum_in ? 2 : 1), 128);
-        int group = g_tune_group.load() > 0 ? g_tune_group.load() : (fin ? (48 * 1024) / item_bytes : 1);
-        if (sum_in) group = 1;  // the FP32 sum and the BF16 residual differ in size
-        if (group > per_row) group = per_row;
-        if (group < 1) group = 1;
-        const int gamma_bytes = gamma_slot_bytes(mode, cpt, consumers);
-        const int cta_max = d->smem_optin - 1024;  // room for the kernel's static shared memory
-        // a group is shrunk until two stages fit one CTA
-        while (group > 1 && (int)SmemLayout::make(2, group * item_bytes, gamma_bytes).total > cta_max)
-            --group;
-        const int stage_bytes = group * item_bytes;
-        const int stages_per_row = (per_row + group - 1) / group;
-        const int overhead = (int)SmemLayout::make(0, stage_bytes, gamma_bytes).total + 2 * 16;
-
-        Launch L;
-        L.cluster = cs;
-        L.consumers = consumers;
-        L.cpt = cpt;
-        // CTAs per SM that registers and threads allow (probe with a 2-stage ring)
-        Launch probe = L;
-        probe.cluster = 1;
-        probe.smem = SmemLayout::make(2, stage_bytes, gamma_bytes).total;
-        int resident_probe = 0;
-        BN_TRY(resident_clusters(mode, probe, &resident_probe));
-        int by_regs = resident_probe / (d->sms > 0 ? d->sms : 1);
-        if (by_regs < 1) by_regs = 1;
-        int ctas = want_ctas > 0 ? want_ctas : (by_regs < 4 ? by_regs : 4);
-        if (ctas > by_regs) ctas = by_regs;
-        int per_cta = d->smem_per_sm / ctas - d->smem_reserved - 1024;
-        if (per_cta > cta_max) per_cta = cta_max;
-
-        int stages;
-        if (want_stages > 0) {
-            stages = want_stages;
-        } else {
-            stages = (per_cta - overhead) / stage_bytes;
-            const int ahead = 2 * stages_per_row + 2;
-            if (stages > ahead) stages = ahead;
-        }
-        if (stages > kMaxStages) stages = kMaxStages;
-        if (stages < 2) stages = 2;
-        while (stages > 2 && (int)SmemLayout::make(stages, stage_bytes, gamma_bytes).total > cta_max)
-            --stages;
-        if ((int)SmemLayout::make(stages, stage_bytes, gamma_bytes).total > cta_max)
-            return fail(BN_ERR_UNSUPPORTED, "stage of %d bytes does not fit shared memory", stage_bytes);
-        L.smem = SmemLayout::make(stages, stage_bytes, gamma_bytes).total;
-
-        int resident = 0;
-        BN_TRY(resident_clusters(mode, L, &resident));
-        if (resident <= 0) {
-            if (cs > 1) continue;  // this cluster size cannot be resident: halve it
-            return fail(BN_ERR_UNSUPPORTED, "no resident CTA for this shape");
-        }
-        const int ncl = T < resident ? T : resident;
-        L.grid = ncl * cs;
-        *l = L;
-        a->stages = stages;
-        a->stage_bytes = stage_bytes;
-        a->group = group;
-        a->item_bytes = item_bytes;
-        a->gamma_bytes = gamma_bytes;
-        a->spin_wait = g_tune_wait.load() == 2 ? 1 : 0;
-        a->nchunks = nchunks;
-        a->err = d->err;
-        return BN_OK;
+        BN_TRY(shape_for(mode, a, d, false, cs, l, &resident));
+        if (resident > 0) return BN_OK;
+        if (cs <= 1) return fail(BN_ERR_UNSUPPORTED, "no resident CTA for this shape");
     }
 }
 
@@ -746,12 +779,15 @@ bn_status bn_set_tuning(const bn_tuning *t)
         return fail(BN_ERR_INVALID, "wait_mode must be 0, 1 or 2");
     if (t->group < 0 || t->group > 64)
         return fail(BN_ERR_INVALID, "group must be in [0, 64]");
+    if (t->split < 0 || t->split > 2)
+        return fail(BN_ERR_INVALID, "split must be 0, 1 or 2");
     g_tune_cluster.store(cs);
     g_tune_stages.store(t->stages);
     g_tune_threads.store(t->threads);
     g_tune_ctas.store(t->ctas_per_sm);
     g_tune_wait.store(t->wait_mode);
     g_tune_group.store(t->group);
+    g_tune_split.store(t->split);
     return BN_OK;
 }
 

@@ -151,6 +151,19 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank)
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
 }
+__device__ __forceinline__ uint4 ld_cluster_u4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void fence_acq_rel_cluster()
+{
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
 __device__ __forceinline__ void st_cluster_f2(uint32_t addr, float x, float y)
 {
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(x), "f"(y)
@@ -436,7 +449,13 @@ __device__ __forceinline__ float row_sum_squares(f2 S2, f2 E2, int &nred, const 
     return S + E;
 }
 
-template <int MODE, int CPT>
+// SPLITR (finalize modes only): the CTAs of a cluster split a token row by
+// shard instead of by columns.  CTA q finalizes shard q over the whole row
+// (k + 1 copies instead of R * (k + 1)), keeps its BF16 result z_q in shared
+// memory, and after a cluster-wide signal every CTA sums the R z rows of its
+// own column slice in rank order through distributed shared memory; the
+// epilogue then runs on the slice exactly as in the column split.
+template <int MODE, int CPT, bool SPLITR>
 __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
 {
     constexpr bool FIN = (MODE & F_FIN) != 0;
@@ -450,7 +469,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
 
-    const SmemLayout L = SmemLayout::make(a.stages, a.stage_bytes, a.gamma_bytes);
+    const SmemLayout L = SmemLayout::make(a.stages, a.stage_bytes, a.gamma_bytes, a.zbuf_bytes);
     Smem sm;
     sm.stages = smem + L.stages_off;
     sm.stages_u32 = smem_addr(sm.stages);
@@ -473,6 +492,12 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
     const uint32_t q = cluster_ctarank();
     const int cl = (int)cluster_id_x();
     const int ncl = (int)ncluster_x();
+    // The shard split needs exactly one CTA per shard in a cluster (the host
+    // launches it so); any other shape returns at once, before any barrier.
+    if (SPLITR && cs != (uint32_t)a.R) {
+        if (threadIdx.x == 0) atomicOr(a.err, kErrTimeout);
+        return;
+    }
     // this CTA's slice of the row: chunks [c0, c0 + nch)
     const int c0 = (int)(((long long)q * a.nchunks) / (long long)cs);
     const int nch = (int)(((long long)(q + 1) * a.nchunks) / (long long)cs) - c0;
@@ -480,15 +505,15 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
     const size_t H = (size_t)a.H;
     const bool has_shared = FIN && a.shared != nullptr;
 
-    // barriers: full[S], empty[S], meta_full[2], meta_empty[2], exchange[2]
-    const int nbars = 2 * S + 6;
+    // barriers: full[S], empty[S], meta_full[2], meta_empty[2], exchange[2], z ready
+    const int nbars = 2 * S + 7;
     for (int i = tid; i < nbars; i += (int)blockDim.x) {
         uint32_t count;
         if (i < S) count = 1u;                      // full: the producer's expect-tx arrive
         else if (i < 2 * S) count = (uint32_t)NW;   // empty: one arrive per consumer warp
         else if (i < 2 * S + 2) count = 32u;        // meta_full: every producer lane
         else if (i < 2 * S + 4) count = (uint32_t)NW;  // meta_empty
-        else count = cs;                            // exchange: one arrive per CTA
+        else count = cs;                            // exchange, z ready: one arrive per CTA
         mbar_init(sm.full0 + 8u * (uint32_t)i, count);
     }
     if (tid == 0) s_abort = 0;
@@ -504,7 +529,9 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
     // A stage holds up to G = a.group consecutive items of one row (one
     // barrier for all of them); a row always ends on a stage boundary.
     const int per_shard = FIN ? a.k + (has_shared ? 1 : 0) : 1;
-    const int row_items = (SUM_IN ? 1 : a.R * per_shard) + (RESNORM ? 1 : 0);
+    const int row_items = (SUM_IN ? 1 : (SPLITR ? 1 : a.R) * per_shard) + (RESNORM ? 1 : 0);
+    const uint32_t zready = sm.ex0 + 16u;       // shard split: the z rows of all CTAs are ready
+    uint4 *zbuf = reinterpret_cast<uint4 *>(smem + L.zbuf_off);
     const int G = a.group;
     const uint32_t item_bytes = (uint32_t)a.item_bytes;
 
@@ -595,6 +622,15 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                 const size_t col = (size_t)c0 * 8u;
                 if constexpr (SUM_IN) {
                     ok = put(a.sum_in + (size_t)t * H + col, bytes16 * 2u);
+                } else if constexpr (FIN && SPLITR) {
+                    // this CTA's shard over the whole row
+                    const int32_t *mp = sm.mperm + slot * kMaxMeta;
+                    const int r = (int)q;
+                    const uint32_t row_bytes = (uint32_t)a.nchunks * 16u;
+                    const uint16_t *xr = a.src + (size_t)r * a.T * a.k * H;
+                    for (int j = 0; j < a.k && ok; ++j)
+                        ok = put(xr + (size_t)mp[r * a.k + j] * H, row_bytes);
+                    if (ok && has_shared) ok = put(a.shared + ((size_t)r * a.T + t) * H, row_bytes);
                 } else if constexpr (FIN) {
                     const int32_t *mp = sm.mperm + slot * kMaxMeta;
                     for (int r = 0; r < a.R && ok; ++r) {
@@ -724,6 +760,94 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                     }
                 }
                 release();
+            } else if constexpr (FIN && SPLITR) {
+                if (!wait_phase<false, true>(sm.mfull0 + 8u * slot, ((uint32_t)it >> 1) & 1u, ctl))
+                    live = false;
+                const float *wrow = sm.mw + slot * kMaxMeta;
+                const int r = (int)q;
+                // shard q over the whole row: chunks tid + i * NT < nchunks
+                f2 acc[CPT][4];
+#pragma unroll
+                for (int i = 0; i < CPT; ++i)
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) acc[i][m] = 0ull;
+                for (int j = 0; j < a.k; ++j) {
+                    const float wj = wrow[r * a.k + j];
+                    const f2 w2 = f2_make(wj, wj);
+                    const uint8_t *p = take();
+#pragma unroll
+                    for (int i = 0; i < CPT; ++i) {
+                        const int lc = tid + i * NT;
+                        if (lc < a.nchunks) {
+                            f2 x[4];
+                            widen8(chunk(p, lc), x);
+                            if (j == 0) {
+#pragma unroll
+                                for (int m = 0; m < 4; ++m) acc[i][m] = mul_sep2(w2, x[m]);
+                            } else {
+#pragma unroll
+                                for (int m = 0; m < 4; ++m)
+                                    acc[i][m] = add2(acc[i][m], mul_sep2(w2, x[m]));
+                            }
+                        }
+                    }
+                    release();
+                }
+                if (has_shared) {
+                    const uint8_t *p = take();
+#pragma unroll
+                    for (int i = 0; i < CPT; ++i) {
+                        const int lc = tid + i * NT;
+                        if (lc < a.nchunks) {
+                            f2 x[4];
+                            widen8(chunk(p, lc), x);
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) acc[i][m] = add2(acc[i][m], x[m]);
+                        }
+                    }
+                    release();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sm.mempty0 + 8u * slot);
+                // local BF16 rounding; z_q stays in this CTA's shared memory
+#pragma unroll
+                for (int i = 0; i < CPT; ++i) {
+                    const int lc = tid + i * NT;
+                    if (lc < a.nchunks) {
+                        const uint4 z = round8(acc[i]);
+                        if constexpr (REDUCE) zbuf[lc] = z;
+                        if ((Z_OUT || a.z_out != nullptr) && live)
+                            *reinterpret_cast<uint4 *>(a.z_out + ((size_t)r * a.T + t) * H +
+                                                       (size_t)lc * 8) = z;
+                    }
+                }
+                if constexpr (REDUCE) {
+                    // all z rows of the cluster ready: one remote arrive per CTA
+                    fence_acq_rel_cluster();
+                    consumer_sync(NT);
+                    if (tid == 0)
+                        for (uint32_t d = 0; d < cs; ++d) mbar_remote_arrive(mapa(zready, d));
+                    if (!wait_phase<true, true>(zready, (uint32_t)it & 1u, ctl)) live = false;
+                    // rank-ordered sum of the R z rows over this CTA's column slice
+                    const uint32_t zb = smem_addr(zbuf);
+                    for (int rr = 0; rr < a.R; ++rr) {
+#pragma unroll
+                        for (int i = 0; i < CPT; ++i) {
+                            const int lc = tid + i * NT;
+                            if (lc < nch) {
+                                f2 zf[4];
+                                widen8(ld_cluster_u4(mapa(zb + (uint32_t)(c0 + lc) * 16u, (uint32_t)rr)), zf);
+                                if (rr == 0) {
+#pragma unroll
+                                    for (int m = 0; m < 4; ++m) s[i][m] = zf[m];
+                                } else {
+#pragma unroll
+                                    for (int m = 0; m < 4; ++m) s[i][m] = add2(s[i][m], zf[m]);
+                                }
+                            }
+                        }
+                    }
+                }
             } else if constexpr (FIN) {
                 if (!wait_phase<false, true>(sm.mfull0 + 8u * slot, ((uint32_t)it >> 1) & 1u, ctl))
                     live = false;

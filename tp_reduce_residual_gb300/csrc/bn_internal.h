@@ -58,12 +58,14 @@ struct Args {
     int group;                // row copies (items) per stage
     int item_bytes;           // stride of one item in a stage (multiple of 128)
     int gamma_bytes;          // shared-memory bytes of the per-thread gamma slots
+    int zbuf_bytes;           // shard split: shared-memory bytes of one full z row
     int spin_wait;            // 1: poll barriers with test_wait; 0: try_wait
     float eps;
 };
 
 // Launch shape chosen on the host.
 struct Launch {
+    int split;       // 1: the CTAs of a cluster split a row by shard (finalize modes)
     int cluster;     // CTAs per token row (thread-block cluster size)
     int consumers;   // consumer threads per CTA (multiple of 32)
     int cpt;         // 16-byte chunks per consumer thread: 1, 2, 4 or 8
@@ -73,13 +75,16 @@ struct Launch {
 
 // Dynamic shared-memory layout, identical on host and device.
 struct SmemLayout {
-    uint32_t stages_off, gamma_off, bars_off, red_off, xslot_off, meta_off, total;
-    __host__ __device__ static SmemLayout make(int stages, int stage_bytes, int gamma_bytes) {
+    uint32_t stages_off, gamma_off, zbuf_off, bars_off, red_off, xslot_off, meta_off, total;
+    __host__ __device__ static SmemLayout make(int stages, int stage_bytes, int gamma_bytes,
+                                               int zbuf_bytes = 0) {
         SmemLayout L;
         L.stages_off = 0;
         L.gamma_off = (uint32_t)stages * (uint32_t)stage_bytes;           // 128-aligned
-        L.bars_off = L.gamma_off + (((uint32_t)gamma_bytes + 127u) & ~127u);
-        uint32_t nbars = 2u * (uint32_t)stages + 6u;                      // full, empty, meta x2 x2, exchange x2
+        L.zbuf_off = L.gamma_off + (((uint32_t)gamma_bytes + 127u) & ~127u);
+        L.bars_off = L.zbuf_off + (((uint32_t)zbuf_bytes + 127u) & ~127u);
+        // full, empty, meta x2 x2, exchange x2, z ready
+        uint32_t nbars = 2u * (uint32_t)stages + 7u;
         L.red_off = L.bars_off + ((nbars * 8u + 15u) & ~15u);
         L.xslot_off = L.red_off + 2u * 32u * 8u;                          // float2 [2][32]
         L.meta_off = L.xslot_off + 2u * (uint32_t)kMaxCluster * 8u;       // float2 [2][16]

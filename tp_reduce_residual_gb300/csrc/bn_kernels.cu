@@ -23,29 +23,46 @@ namespace {
 constexpr int kMode = BN_MODE_VALUE;
 constexpr int kMaxDevices = 64;
 
-const void *kernel_for(int cpt)
+template <bool SPLIT>
+const void *kernel_by_cpt(int cpt)
 {
     switch (cpt) {
-    case 1: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 1>);
-    case 2: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 2>);
-    case 4: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 4>);
-    case 8: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 8>);
+    case 1: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 1, SPLIT>);
+    case 2: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 2, SPLIT>);
+    case 4: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 4, SPLIT>);
+    case 8: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 8, SPLIT>);
     default: return nullptr;
     }
 }
 
-int cpt_index(int cpt) { return cpt == 1 ? 0 : cpt == 2 ? 1 : cpt == 4 ? 2 : 3; }
+// The shard split exists for the finalize modes with an epilogue or the
+// finalize alone; other modes have no such kernel.
+constexpr bool kHasSplit = (kMode & F_FIN) && (kMode & (F_RESNORM | F_Z_OUT));
+
+const void *kernel_for(int cpt, int split)
+{
+    if (split) {
+        if constexpr (kHasSplit) return kernel_by_cpt<true>(cpt);
+        return nullptr;
+    }
+    return kernel_by_cpt<false>(cpt);
+}
+
+int cpt_index(int cpt, int split)
+{
+    return (cpt == 1 ? 0 : cpt == 2 ? 1 : cpt == 4 ? 2 : 3) + (split ? 4 : 0);
+}
 
 // Function attributes are per device: set them once per (device, cpt).
 std::atomic<unsigned> g_prepared[kMaxDevices];
 
-cudaError_t prepare(const void *fn, int cpt)
+cudaError_t prepare(const void *fn, int cpt, int split)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    const unsigned bit = 1u << cpt_index(cpt);
+    const unsigned bit = 1u << cpt_index(cpt, split);
     if (g_prepared[dev].load(std::memory_order_acquire) & bit) return cudaSuccess;
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
@@ -86,9 +103,9 @@ void fill_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, const Launc
 
 cudaError_t BN_CAT(launch_, BN_MODE_NAME)(const Args &a, const Launch &l, cudaStream_t st)
 {
-    const void *fn = kernel_for(l.cpt);
+    const void *fn = kernel_for(l.cpt, l.split);
     if (!fn) return cudaErrorInvalidValue;
-    cudaError_t e = prepare(fn, l.cpt);
+    cudaError_t e = prepare(fn, l.cpt, l.split);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
@@ -99,12 +116,12 @@ cudaError_t BN_CAT(launch_, BN_MODE_NAME)(const Args &a, const Launch &l, cudaSt
 
 int BN_CAT(occupancy_, BN_MODE_NAME)(const Launch &l, cudaError_t *err)
 {
-    const void *fn = kernel_for(l.cpt);
+    const void *fn = kernel_for(l.cpt, l.split);
     if (!fn) {
         *err = cudaErrorInvalidValue;
         return 0;
     }
-    cudaError_t e = prepare(fn, l.cpt);
+    cudaError_t e = prepare(fn, l.cpt, l.split);
     if (e != cudaSuccess) {
         *err = e;
         return 0;
