@@ -391,11 +391,11 @@ bn_status plan(int mode, Args *a, Launch *l)
     int resident = 0;
 
     // shard split: finalize modes with an epilogue (or the finalize alone),
-    // R >= 2, and few rows (measured on GB300: one row then takes k + 1 copies
-    // per CTA instead of R * (k + 1))
+    // R >= 2, and few rows.  Measured on GB300 (R=8): 30 -> 18 us at T=1 and
+    // 4, but slower than the column split from T=16 on, so up to T*R = 64.
     const bool can_split = (mode & F_FIN) && (mode & (F_RESNORM | F_Z_OUT)) && a->R >= 2;
     const int pref = g_tune_split.load();
-    const bool split = can_split && (pref == 2 || (pref == 0 && (long long)T * a->R <= 2LL * d->sms));
+    const bool split = can_split && (pref == 2 || (pref == 0 && (long long)T * a->R <= 64));
     if (split) {
         BN_TRY(shape_for(mode, a, d, true, a->R, l, &resident));
         if (resident > 0) return BN_OK;

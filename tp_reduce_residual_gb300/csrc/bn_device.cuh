@@ -151,13 +151,13 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank)
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
 }
+// Remote shared-memory load; volatile keeps it after the preceding barrier wait.
 __device__ __forceinline__ uint4 ld_cluster_u4(uint32_t addr)
 {
     uint4 v;
     asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr)
-                 : "memory");
+                 : "r"(addr));
     return v;
 }
 __device__ __forceinline__ void fence_acq_rel_cluster()
@@ -828,21 +828,33 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                     if (tid == 0)
                         for (uint32_t d = 0; d < cs; ++d) mbar_remote_arrive(mapa(zready, d));
                     if (!wait_phase<true, true>(zready, (uint32_t)it & 1u, ctl)) live = false;
-                    // rank-ordered sum of the R z rows over this CTA's column slice
+                    // rank-ordered sum of the R z rows over this CTA's column
+                    // slice; the remote loads of four ranks are issued before
+                    // their (ordered) additions so that their latencies overlap
                     const uint32_t zb = smem_addr(zbuf);
-                    for (int rr = 0; rr < a.R; ++rr) {
 #pragma unroll
-                        for (int i = 0; i < CPT; ++i) {
-                            const int lc = tid + i * NT;
-                            if (lc < nch) {
-                                f2 zf[4];
-                                widen8(ld_cluster_u4(mapa(zb + (uint32_t)(c0 + lc) * 16u, (uint32_t)rr)), zf);
-                                if (rr == 0) {
+                    for (int i = 0; i < CPT; ++i) {
+                        const int lc = tid + i * NT;
+                        if (lc < nch) {
+                            const uint32_t za = zb + (uint32_t)(c0 + lc) * 16u;
+                            for (int r0 = 0; r0 < a.R; r0 += 4) {
+                                uint4 zv[4];
 #pragma unroll
-                                    for (int m = 0; m < 4; ++m) s[i][m] = zf[m];
-                                } else {
+                                for (int u = 0; u < 4; ++u)
+                                    if (r0 + u < a.R) zv[u] = ld_cluster_u4(mapa(za, (uint32_t)(r0 + u)));
 #pragma unroll
-                                    for (int m = 0; m < 4; ++m) s[i][m] = add2(s[i][m], zf[m]);
+                                for (int u = 0; u < 4; ++u) {
+                                    if (r0 + u < a.R) {
+                                        f2 zf[4];
+                                        widen8(zv[u], zf);
+                                        if (r0 + u == 0) {
+#pragma unroll
+                                            for (int m = 0; m < 4; ++m) s[i][m] = zf[m];
+                                        } else {
+#pragma unroll
+                                            for (int m = 0; m < 4; ++m) s[i][m] = add2(s[i][m], zf[m]);
+                                        }
+                                    }
                                 }
                             }
                         }
