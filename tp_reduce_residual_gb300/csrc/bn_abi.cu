@@ -321,11 +321,11 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     const int cta_max = d->smem_optin - 1024;  // room for the kernel's static shared memory
     // a group is shrunk until two stages fit one CTA
     while (group > 1 &&
-           (int)SmemLayout::make(2, group * item_bytes, gamma_bytes, zbuf_bytes).total > cta_max)
+           (int)SmemLayout::make(2, group * item_bytes, gamma_bytes, zbuf_bytes, fin).total > cta_max)
         --group;
     const int stage_bytes = group * item_bytes;
     const int stages_per_row = (per_row + group - 1) / group;
-    const int overhead = (int)SmemLayout::make(0, stage_bytes, gamma_bytes, zbuf_bytes).total + 2 * 16;
+    const int overhead = (int)SmemLayout::make(0, stage_bytes, gamma_bytes, zbuf_bytes, fin).total + 2 * 16;
 
     Launch L;
     L.split = split ? 1 : 0;
@@ -335,7 +335,7 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     // CTAs per SM that registers and threads allow (probe with a 2-stage ring)
     Launch probe = L;
     probe.cluster = 1;
-    probe.smem = SmemLayout::make(2, stage_bytes, gamma_bytes, zbuf_bytes).total;
+    probe.smem = SmemLayout::make(2, stage_bytes, gamma_bytes, zbuf_bytes, fin).total;
     int resident_probe = 0;
     BN_TRY(resident_clusters(mode, probe, &resident_probe));
     int by_regs = resident_probe / (d->sms > 0 ? d->sms : 1);
@@ -356,11 +356,11 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) stages = 2;
     while (stages > 2 &&
-           (int)SmemLayout::make(stages, stage_bytes, gamma_bytes, zbuf_bytes).total > cta_max)
+           (int)SmemLayout::make(stages, stage_bytes, gamma_bytes, zbuf_bytes, fin).total > cta_max)
         --stages;
-    if ((int)SmemLayout::make(stages, stage_bytes, gamma_bytes, zbuf_bytes).total > cta_max)
+    if ((int)SmemLayout::make(stages, stage_bytes, gamma_bytes, zbuf_bytes, fin).total > cta_max)
         return fail(BN_ERR_UNSUPPORTED, "stage of %d bytes does not fit shared memory", stage_bytes);
-    L.smem = SmemLayout::make(stages, stage_bytes, gamma_bytes, zbuf_bytes).total;
+    L.smem = SmemLayout::make(stages, stage_bytes, gamma_bytes, zbuf_bytes, fin).total;
 
     BN_TRY(resident_clusters(mode, L, resident));
     if (*resident <= 0) return BN_OK;

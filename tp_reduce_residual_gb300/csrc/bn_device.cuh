@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
 
-    const SmemLayout L = SmemLayout::make(a.stages, a.stage_bytes, a.gamma_bytes, a.zbuf_bytes);
+    const SmemLayout L = SmemLayout::make(a.stages, a.stage_bytes, a.gamma_bytes, a.zbuf_bytes, FIN);
     Smem sm;
     sm.stages = smem + L.stages_off;
     sm.stages_u32 = smem_addr(sm.stages);

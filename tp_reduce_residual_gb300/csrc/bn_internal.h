@@ -77,7 +77,7 @@ struct Launch {
 struct SmemLayout {
     uint32_t stages_off, gamma_off, zbuf_off, bars_off, red_off, xslot_off, meta_off, total;
     __host__ __device__ static SmemLayout make(int stages, int stage_bytes, int gamma_bytes,
-                                               int zbuf_bytes = 0) {
+                                               int zbuf_bytes, bool fin) {
         SmemLayout L;
         L.stages_off = 0;
         L.gamma_off = (uint32_t)stages * (uint32_t)stage_bytes;           // 128-aligned
@@ -88,7 +88,8 @@ struct SmemLayout {
         L.red_off = L.bars_off + ((nbars * 8u + 15u) & ~15u);
         L.xslot_off = L.red_off + 2u * 32u * 8u;                          // float2 [2][32]
         L.meta_off = L.xslot_off + 2u * (uint32_t)kMaxCluster * 8u;       // float2 [2][16]
-        L.total = L.meta_off + 2u * (uint32_t)kMaxMeta * 8u;              // int32 + float [2][256]
+        // gather indices and weights (finalize modes only): int32 + float [2][256]
+        L.total = L.meta_off + (fin ? 2u * (uint32_t)kMaxMeta * 8u : 0u);
         return L;
     }
 };
