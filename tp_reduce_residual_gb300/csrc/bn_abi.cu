@@ -342,7 +342,8 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     if (by_regs < 1) by_regs = 1;
     int ctas = want_ctas > 0 ? want_ctas : (by_regs < 4 ? by_regs : 4);
     if (ctas > by_regs) ctas = by_regs;
-    int per_cta = d->smem_per_sm / ctas - d->smem_reserved - 1024;
+    // the kernel's own static shared memory is 128 bytes: keep a 256-byte margin
+    int per_cta = d->smem_per_sm / ctas - d->smem_reserved - 256;
     if (per_cta > cta_max) per_cta = cta_max;
 
     int stages;
