@@ -325,7 +325,7 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
         --group;
     const int stage_bytes = group * item_bytes;
     const int stages_per_row = (per_row + group - 1) / group;
-    const int overhead = (int)SmemLayout::make(0, stage_bytes, gamma_bytes, zbuf_bytes, fin).total + 2 * 16;
+    const int overhead = (int)SmemLayout::make(0, stage_bytes, gamma_bytes, zbuf_bytes, fin).total;
 
     Launch L;
     L.split = split ? 1 : 0;
@@ -342,8 +342,9 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     if (by_regs < 1) by_regs = 1;
     int ctas = want_ctas > 0 ? want_ctas : (by_regs < 4 ? by_regs : 4);
     if (ctas > by_regs) ctas = by_regs;
-    // the kernel's own static shared memory is 128 bytes: keep a 256-byte margin
-    int per_cta = d->smem_per_sm / ctas - d->smem_reserved - 256;
+    // the kernel's own static shared memory is 128 bytes; the occupancy check
+    // below drops a stage if the estimate was one too many
+    int per_cta = d->smem_per_sm / ctas - d->smem_reserved - 128;
     if (per_cta > cta_max) per_cta = cta_max;
 
     int stages;
@@ -364,6 +365,12 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     L.smem = SmemLayout::make(stages, stage_bytes, gamma_bytes, zbuf_bytes, fin).total;
 
     BN_TRY(resident_clusters(mode, L, resident));
+    // keep the intended CTAs per SM: one stage less if the ring estimate overshot
+    if (want_stages == 0 && cs == 1 && stages > 2 && *resident < ctas * d->sms) {
+        --stages;
+        L.smem = SmemLayout::make(stages, stage_bytes, gamma_bytes, zbuf_bytes, fin).total;
+        BN_TRY(resident_clusters(mode, L, resident));
+    }
     if (*resident <= 0) return BN_OK;
     const int ncl = a->T < *resident ? a->T : *resident;
     L.grid = ncl * cs;
