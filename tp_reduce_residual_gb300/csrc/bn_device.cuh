@@ -771,27 +771,63 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                 for (int i = 0; i < CPT; ++i)
 #pragma unroll
                     for (int m = 0; m < 4; ++m) acc[i][m] = 0ull;
-                for (int j = 0; j < a.k; ++j) {
-                    const float wj = wrow[r * a.k + j];
-                    const f2 w2 = f2_make(wj, wj);
-                    const uint8_t *p = take();
+                // Up to four gathered rows (one stage each here) are waited for
+                // together; their loads and products are independent and only
+                // the additions run in slot order, so the dependent chain per
+                // row is one add instead of a full load-multiply-add.
+                const int U = S < 4 ? S : 4;
+                auto ahead = [&](int u) -> const uint8_t * {
+                    uint32_t st = stage + (uint32_t)u, ph = phase;
+                    if (st >= (uint32_t)S) {
+                        st -= (uint32_t)S;
+                        ph ^= 1u;
+                    }
+                    if (!wait_phase<false, true>(sm.full0 + 8u * st, ph, ctl)) live = false;
+                    return sm.stages + (size_t)st * (size_t)a.stage_bytes;
+                };
+                for (int j0 = 0; j0 < a.k; j0 += U) {
+                    const int n = (a.k - j0) < U ? (a.k - j0) : U;
+                    const uint8_t *pp[4] = {nullptr, nullptr, nullptr, nullptr};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (u < n) pp[u] = ahead(u);
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
                         if (lc < a.nchunks) {
-                            f2 x[4];
-                            widen8(chunk(p, lc), x);
-                            if (j == 0) {
+                            uint4 v[4];
 #pragma unroll
-                                for (int m = 0; m < 4; ++m) acc[i][m] = mul_sep2(w2, x[m]);
-                            } else {
+                            for (int u = 0; u < 4; ++u)
+                                if (u < n) v[u] = chunk(pp[u], lc);
 #pragma unroll
-                                for (int m = 0; m < 4; ++m)
-                                    acc[i][m] = add2(acc[i][m], mul_sep2(w2, x[m]));
+                            for (int u = 0; u < 4; ++u) {
+                                if (u < n) {
+                                    const float wj = wrow[r * a.k + j0 + u];
+                                    const f2 w2 = f2_make(wj, wj);
+                                    f2 x[4];
+                                    widen8(v[u], x);
+                                    if (j0 + u == 0) {
+#pragma unroll
+                                        for (int m = 0; m < 4; ++m) acc[i][m] = mul_sep2(w2, x[m]);
+                                    } else {
+#pragma unroll
+                                        for (int m = 0; m < 4; ++m)
+                                            acc[i][m] = add2(acc[i][m], mul_sep2(w2, x[m]));
+                                    }
+                                }
                             }
                         }
                     }
-                    release();
+                    // release the n stages in order (one item each)
+                    for (int u = 0; u < n; ++u) {
+                        --cleft;
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(sm.empty0 + 8u * stage);
+                        if (++stage == (uint32_t)S) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
                 }
                 if (has_shared) {
                     const uint8_t *p = take();
