@@ -198,11 +198,49 @@ typedef struct {
     int wait_mode;     /* 1: suspending try_wait, 2: polling test_wait */
     int group;         /* row copies per pipeline stage, at most 64 */
     int split;         /* finalize rows: 1 split by columns, 2 split by shard */
+    int dependent_launch; /* 1: plain stream order, 2: programmatic dependent
+                             launch (the launch and the kernel's setup overlap
+                             the previous kernel in the stream) */
 } bn_tuning;
 
 /* Set the overrides; NULL restores automatic choices.  BN_ERR_INVALID on an
  * out-of-range field (nothing changes then). */
 BN_API bn_status bn_set_tuning(const bn_tuning *tuning);
+
+/* The operations of the entry points above, for bn_query_launch. */
+typedef enum {
+    BN_OP_REDUCE_NORM = 0,
+    BN_OP_FINALIZE_REDUCE_NORM = 1,
+    BN_OP_REDUCE_RESIDUAL_NORM = 2,
+    BN_OP_FINALIZE_REDUCE_RESIDUAL_NORM = 3,
+    BN_OP_REDUCE_ONLY = 4,
+    BN_OP_FINALIZE_REDUCE_ONLY = 5,
+    BN_OP_NORM_ONLY = 6,
+    BN_OP_FINALIZE_ONLY = 7
+} bn_op;
+
+/* The launch shape one call would use on the current device. */
+typedef struct {
+    int split;                /* 1: a cluster of R CTAs splits each row by shard */
+    int cluster_size;         /* CTAs per token row */
+    int threads;              /* threads per CTA: consumer threads + one producer warp */
+    int chunks_per_thread;    /* 16-byte chunks of the CTA's slice per consumer thread */
+    int grid;                 /* CTAs launched (persistent; rows are grid-strided) */
+    int resident_ctas;        /* CTAs of this shape the device holds at once */
+    int stages;               /* pipeline stages in the shared-memory ring */
+    int stage_bytes;
+    int group;                /* row copies per stage */
+    int smem_bytes;           /* dynamic shared memory per CTA */
+} bn_launch_info;
+
+/* Fill *info with the launch shape that `op` would use for this shape on the
+ * current device, under the current tuning overrides; nothing is enqueued.
+ * k is ignored by the operations without a finalize; has_shared says whether
+ * the finalize call would pass a shared-expert row.  Shape errors and
+ * declines are reported as by the entry point itself; T == 0 gives BN_OK and
+ * an all-zero *info (no launch).  Needs a CUDA device (occupancy queries). */
+BN_API bn_status bn_query_launch(bn_op op, int R, int T, int k, int H, int has_shared,
+                                 bn_launch_info *info);
 
 #ifdef __cplusplus
 }

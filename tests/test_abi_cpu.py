@@ -143,7 +143,8 @@ def test_set_tuning_validates(L):
     assert st(0, 0, 0, 0, 3, 0) == bn.ERR_INVALID
     assert st(0, 0, 0, 0, 0, 65) == bn.ERR_INVALID
     assert st(0, 0, 0, 0, 0, 0, 3) == bn.ERR_INVALID
-    assert st(16, 8, 256, 2, 2, 4, 2) == bn.OK
+    assert st(0, 0, 0, 0, 0, 0, 0, 3) == bn.ERR_INVALID
+    assert st(16, 8, 256, 2, 2, 4, 2, 1) == bn.OK
     assert L.bn_set_tuning(None) == bn.OK
 
 
@@ -159,3 +160,19 @@ def test_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(bn, "LIB_PATH", "/nonexistent/libbeamnorm.so")
     with pytest.raises(RuntimeError, match="not built"):
         bn.load()
+
+
+def test_query_launch_validates_on_the_host(L):
+    info = bn._LaunchInfo()
+    q = lambda *a: L.bn_query_launch(*a, ctypes.byref(info))
+    assert L.bn_query_launch(0, 2, 8, 0, 256, 0, None) == bn.ERR_INVALID
+    assert q(8, 2, 8, 0, 256, 0) == bn.ERR_INVALID          # no such operation
+    assert q(-1, 2, 8, 0, 256, 0) == bn.ERR_INVALID
+    assert q(0, 0, 8, 0, 256, 0) == bn.ERR_INVALID          # R outside [1, 16]
+    assert q(1, 8, 8, 0, 256, 1) == bn.ERR_INVALID          # finalize needs k >= 1
+    assert q(0, 2, 8, 0, 260, 0) == bn.ERR_INVALID          # H % 8 != 0
+    assert q(0, 2, 8, 0, 40000, 0) == bn.ERR_UNSUPPORTED    # declined: H above the maximum
+    info.grid = 7
+    assert q(3, 8, 0, 10, 8192, 1) == bn.OK                 # T == 0: no launch, all zero
+    assert info.grid == 0 and info.stages == 0
+    assert bn.OPS.index("finalize_only") == 7

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from tests import parity
-from tests.helpers import assert_bits_equal
+from tests.helpers import assert_bf16_close, assert_bits_equal
 from tp_reduce_residual_gb300 import beamnorm as bn
 from tp_reduce_residual_gb300 import build as nbuild
 from tp_reduce_residual_gb300 import inputs
@@ -186,6 +186,32 @@ def test_launch_shapes_give_identical_bits(cluster, stages, threads, ctas, wait,
     parity.compare(g, parity.run_oracle(d), what=f"cluster={cluster} stages={stages} ctas={ctas} group={group}")
 
 
+@pytest.mark.gpu
+@pytest.mark.parametrize("op,R,T,k,H", [
+    ("reduce_norm", 4, 1024, 0, 5120), ("reduce_norm", 8, 1, 0, 8192),
+    ("finalize_reduce_norm", 8, 1, 10, 8192), ("finalize_reduce_norm", 8, 1024, 10, 8192),
+    ("norm_only", 1, 64, 0, 8192), ("finalize_only", 8, 4, 8, 6144),
+    ("reduce_residual_norm", 2, 8, 0, 256),
+])
+def test_launch_query_is_coherent(op, R, T, k, H):
+    props = torch.cuda.get_device_properties(0)
+    i = bn.launch_info(op, R, T, H, k)
+    assert i["threads"] % 32 == 0 and 64 <= i["threads"] <= 512 + 32
+    assert i["grid"] > 0 and i["grid"] % i["cluster_size"] == 0
+    assert i["grid"] // i["cluster_size"] <= T
+    assert i["stages"] >= 2 and i["stage_bytes"] % 128 == 0 and i["group"] >= 1
+    assert i["resident_ctas"] >= i["grid"]
+    assert i["smem_bytes"] <= props.shared_memory_per_block_optin
+    if i["split"]:
+        assert op.startswith("finalize") and i["cluster_size"] == R
+    try:
+        bn.set_tuning(stages=2, split=1 if op.startswith("finalize") else 0)
+        j = bn.launch_info(op, R, T, H, k)
+    finally:
+        bn.set_tuning()
+    assert j["stages"] == 2 and j["split"] == 0
+
+
 SPLIT_CASES = [
     # (R, T, k, H, with_shared, single_norm)
     (8, 1, 10, 8192, True, False),
@@ -268,6 +294,59 @@ def test_side_stream_and_graph_replay():
     torch.cuda.synchronize()
     assert_bits_equal(inputs.u16(out), eager["out"], "graph out")
     assert_bits_equal(inputs.u16(res), eager["residual_out"], "graph residual")
+
+
+def _dependent_chain(d, use_graph: bool):
+    """Five back-to-back calls where each reads what the previous one wrote:
+    the unfused pair (finalize_reduce_only writes the FP32 sum that norm_only
+    reads), then fused calls whose residual is the previous call's output."""
+    T, H = d["T"], d["H"]
+    s = torch.empty(T, H, dtype=torch.float32, device="cuda")
+    res = d["residual"].clone()
+    outs = [torch.empty_like(res) for _ in range(3)]
+
+    def body():
+        bn.finalize_reduce_only(d["expert_out"], d["perm"], d["w"], d["shared"], sum_out=s)
+        bn.norm_only(s, res, d["gamma_post"], d["gamma_pre"], d["eps"], out=outs[0])
+        for i in (1, 2):
+            bn.finalize_reduce_norm(d["expert_out"], d["perm"], d["w"], d["shared"], outs[i - 1],
+                                    d["gamma_post"], d["gamma_pre"], d["eps"], out=outs[i])
+
+    if use_graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            body()
+        s.fill_(float("nan"))
+        res.copy_(d["residual"])
+        for o in outs:
+            o.fill_(float("nan"))
+        g.replay()
+    else:
+        body()
+    torch.cuda.synchronize()
+    return [inputs.u16(t) for t in (res, *outs)] + [s.cpu().numpy()]
+
+
+@pytest.mark.parametrize("wl_index,T", [(4, 4), (3, 16), (4, 64)])
+def test_dependent_launch_keeps_stream_order(wl_index, T):
+    d = parity.gpu_inputs(inputs.WORKLOADS[wl_index], T)
+    runs = {}
+    try:
+        bn.set_tuning(dependent_launch=1)
+        plain = _dependent_chain(d, use_graph=False)
+        bn.set_tuning(dependent_launch=2)
+        runs["eager"] = _dependent_chain(d, use_graph=False)
+        runs["in a graph"] = _dependent_chain(d, use_graph=True)
+    finally:
+        bn.set_tuning()
+    names = ("residual", "out0", "out1", "out2", "sum")
+    for what, got in runs.items():
+        for a, b, n in zip(plain, got, names):
+            assert_bits_equal(b, a, f"programmatic launch, {what}: {n}")
+    # the unfused pair's results (out0 is overwritten in place by the next call)
+    ref = parity.run_oracle(d)
+    assert_bits_equal(plain[4], ref["sum"], "unfused pair sum")
+    assert_bf16_close(plain[0], ref["residual_out"], parity.MAX_ULP, "unfused pair residual")
 
 
 def test_two_calls_update_the_residual_twice():

@@ -31,8 +31,13 @@ EXPORTS = (
     "bn_reduce_norm", "bn_finalize_reduce_norm", "bn_reduce_residual_norm",
     "bn_finalize_reduce_residual_norm", "bn_reduce_only", "bn_finalize_reduce_only",
     "bn_norm_only", "bn_finalize_only", "bn_supports", "bn_check_device_error",
-    "bn_last_error", "bn_status_string", "bn_version", "bn_set_tuning",
+    "bn_last_error", "bn_status_string", "bn_version", "bn_set_tuning", "bn_query_launch",
 )
+
+# bn_op values of the entry points, for launch_info()
+OPS = ("reduce_norm", "finalize_reduce_norm", "reduce_residual_norm",
+       "finalize_reduce_residual_norm", "reduce_only", "finalize_reduce_only", "norm_only",
+       "finalize_only")
 
 
 class BeamNormError(RuntimeError):
@@ -48,7 +53,13 @@ _STATUS_NAMES = {OK: "BN_OK", ERR_INVALID: "BN_ERR_INVALID", ERR_UNSUPPORTED: "B
 class _Tuning(ctypes.Structure):
     _fields_ = [("cluster_size", ctypes.c_int), ("stages", ctypes.c_int), ("threads", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int), ("wait_mode", ctypes.c_int), ("group", ctypes.c_int),
-                ("split", ctypes.c_int)]
+                ("split", ctypes.c_int), ("dependent_launch", ctypes.c_int)]
+
+
+class _LaunchInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "split", "cluster_size", "threads", "chunks_per_thread", "grid", "resident_ctas",
+        "stages", "stage_bytes", "group", "smem_bytes")]
 
 
 class _Debug(ctypes.Structure):
@@ -98,6 +109,7 @@ def load() -> ctypes.CDLL:
             "bn_status_string": [_I],
             "bn_version": [],
             "bn_set_tuning": [ctypes.POINTER(_Tuning)],
+            "bn_query_launch": [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_LaunchInfo)],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -330,11 +342,19 @@ def check_device_error(stream=None, raise_on_error: bool = True) -> int:
 
 
 def set_tuning(cluster_size: int = 0, stages: int = 0, threads: int = 0, ctas_per_sm: int = 0,
-               wait_mode: int = 0, group: int = 0, split: int = 0) -> None:
+               wait_mode: int = 0, group: int = 0, split: int = 0, dependent_launch: int = 0) -> None:
     """Override the launch shape for measurement sweeps (0 = automatic)."""
     t = _Tuning(int(cluster_size), int(stages), int(threads), int(ctas_per_sm), int(wait_mode),
-                int(group), int(split))
+                int(group), int(split), int(dependent_launch))
     _check(load().bn_set_tuning(ctypes.byref(t)))
+
+
+def launch_info(op: str, R: int, T: int, H: int, k: int = 0, has_shared: bool = True) -> dict:
+    """The launch shape ``op`` would use for this shape on the current device."""
+    info = _LaunchInfo()
+    _check(load().bn_query_launch(OPS.index(op), int(R), int(T), int(k), int(H),
+                                  1 if has_shared else 0, ctypes.byref(info)))
+    return {name: int(getattr(info, name)) for name, _ in _LaunchInfo._fields_}
 
 
 def version() -> int:

@@ -49,7 +49,7 @@ bn_status cuda_fail(cudaError_t e, const char *what)
 // ---- tuning overrides (process-wide) -------------------------------------------
 
 std::atomic<int> g_tune_cluster{0}, g_tune_stages{0}, g_tune_threads{0}, g_tune_ctas{0},
-    g_tune_wait{0}, g_tune_group{0}, g_tune_split{0};
+    g_tune_wait{0}, g_tune_group{0}, g_tune_split{0}, g_tune_pdl{0};
 
 // ---- per-device state ------------------------------------------------------------
 
@@ -332,6 +332,7 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     L.cluster = cs;
     L.consumers = consumers;
     L.cpt = cpt;
+    L.pdl = 0;
     // CTAs per SM that registers and threads allow (probe with a 2-stage ring)
     Launch probe = L;
     probe.cluster = 1;
@@ -374,6 +375,9 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     if (*resident <= 0) return BN_OK;
     const int ncl = a->T < *resident ? a->T : *resident;
     L.grid = ncl * cs;
+    // programmatic dependent launch: the launch and this kernel's setup
+    // overlap the previous kernel in the stream (about 1 us per call measured)
+    L.pdl = g_tune_pdl.load() == 1 ? 0 : 1;
     *l = L;
     a->stages = stages;
     a->stage_bytes = stage_bytes;
@@ -789,6 +793,8 @@ bn_status bn_set_tuning(const bn_tuning *t)
         return fail(BN_ERR_INVALID, "group must be in [0, 64]");
     if (t->split < 0 || t->split > 2)
         return fail(BN_ERR_INVALID, "split must be 0, 1 or 2");
+    if (t->dependent_launch < 0 || t->dependent_launch > 2)
+        return fail(BN_ERR_INVALID, "dependent_launch must be 0, 1 or 2");
     g_tune_cluster.store(cs);
     g_tune_stages.store(t->stages);
     g_tune_threads.store(t->threads);
@@ -796,6 +802,46 @@ bn_status bn_set_tuning(const bn_tuning *t)
     g_tune_wait.store(t->wait_mode);
     g_tune_group.store(t->group);
     g_tune_split.store(t->split);
+    g_tune_pdl.store(t->dependent_launch);
+    return BN_OK;
+}
+
+bn_status bn_query_launch(bn_op op, int R, int T, int k, int H, int has_shared,
+                          bn_launch_info *info)
+{
+    g_msg[0] = '\0';
+    BN_REQUIRE(info != nullptr, "info is NULL");
+    std::memset(info, 0, sizeof *info);
+    static const int kModeOf[] = {kModeReduceNorm,    kModeFinReduceNorm, kModeReduceResNorm,
+                                  kModeFinReduceResNorm, kModeReduceOnly, kModeFinReduceOnly,
+                                  kModeNormOnly,      kModeFinOnly};
+    BN_REQUIRE((int)op >= 0 && (int)op < (int)(sizeof kModeOf / sizeof kModeOf[0]),
+               "op=%d is not an operation", (int)op);
+    const int mode = kModeOf[(int)op];
+    const bool fin = (mode & F_FIN) != 0;
+    if (mode & F_SUM_IN) R = 1;  // norm_only reads one FP32 row
+    BN_TRY(check_shape(R, T, fin ? k : 1, H, fin));
+    if (T == 0) return BN_OK;
+    BN_TRY(check_served(R, T, fin ? k : 1, H, fin));
+    Args a = base_args(R, T, fin ? k : 0, H, 0.f);
+    // only the presence of the shared rows matters to the shape; the address
+    // is a marker that is never dereferenced (nothing is launched)
+    static const uint16_t kSharedMarker[8] = {};
+    a.shared = (fin && has_shared) ? kSharedMarker : nullptr;
+    Launch l;
+    BN_TRY(plan(mode, &a, &l));
+    int resident = 0;
+    BN_TRY(resident_clusters(mode, l, &resident));
+    info->split = l.split;
+    info->cluster_size = l.cluster;
+    info->threads = l.consumers + 32;
+    info->chunks_per_thread = l.cpt;
+    info->grid = l.grid;
+    info->resident_ctas = resident * l.cluster;
+    info->stages = a.stages;
+    info->stage_bytes = a.stage_bytes;
+    info->group = a.group;
+    info->smem_bytes = (int)l.smem;
     return BN_OK;
 }
 

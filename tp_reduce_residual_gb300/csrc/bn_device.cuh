@@ -194,6 +194,19 @@ __device__ __forceinline__ void fence_mbarrier_init()
 {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
+// Programmatic dependent launch (sm_90 and later).  wait: block until every
+// grid this one depends on has completed and its memory is visible (a no-op
+// when the launch did not ask for programmatic serialization).  launch_dependents:
+// allow the next grid in the stream to be scheduled early; it still runs no
+// memory operation before its own wait.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 // Named barrier among the consumer warps only (the producer warp runs free).
 __device__ __forceinline__ void consumer_sync(int nthreads)
 {
@@ -495,6 +508,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
     // The shard split needs exactly one CTA per shard in a cluster (the host
     // launches it so); any other shape returns at once, before any barrier.
     if (SPLITR && cs != (uint32_t)a.R) {
+        griddep_wait();
         if (threadIdx.x == 0) atomicOr(a.err, kErrTimeout);
         return;
     }
@@ -520,6 +534,10 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
     fence_mbarrier_init();
     __syncthreads();
     if (cs > 1) cluster_sync_all();
+    // Only shared memory was touched so far: under a programmatic launch the
+    // setup above overlaps the previous kernel's tail.  No global load or store
+    // comes before this wait.
+    griddep_wait();
     const Ctl ctl{&s_abort, a.err, a.spin_wait != 0};
 
     // Copies per token row ("items"), in the order both sides walk them:
@@ -1090,6 +1108,10 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
             }
         }
     }
+    // Release the next kernel in the stream only now: released at setup, its
+    // CTAs would take SMs in the order this grid's SMs drain, which unbalances
+    // rows when CTAs sharing an SM carry unequal loads (measured on GB300).
+    griddep_launch_dependents();
     if (cs > 1) cluster_sync_all();
 }
 

@@ -71,6 +71,7 @@ struct Launch {
     int cpt;         // 16-byte chunks per consumer thread: 1, 2, 4 or 8
     int grid;        // CTAs (a multiple of cluster)
     size_t smem;     // dynamic shared memory bytes
+    int pdl;         // 1: programmatic dependent launch (setup overlaps the previous kernel)
 };
 
 // Dynamic shared-memory layout, identical on host and device.

@@ -87,16 +87,21 @@ void fill_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, const Launc
     cfg.blockDim = dim3((unsigned)(l.consumers + 32), 1, 1);
     cfg.dynamicSmemBytes = l.smem;
     cfg.stream = st;
-    cfg.attrs = nullptr;
+    cfg.attrs = attr;
     cfg.numAttrs = 0;
     if (l.cluster > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)l.cluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cudaLaunchAttribute &c = attr[cfg.numAttrs++];
+        c.id = cudaLaunchAttributeClusterDimension;
+        c.val.clusterDim.x = (unsigned)l.cluster;
+        c.val.clusterDim.y = 1;
+        c.val.clusterDim.z = 1;
     }
+    if (l.pdl && st != nullptr) {
+        cudaLaunchAttribute &p = attr[cfg.numAttrs++];
+        p.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        p.val.programmaticStreamSerializationAllowed = 1;
+    }
+    if (cfg.numAttrs == 0) cfg.attrs = nullptr;
 }
 
 }  // namespace
@@ -108,7 +113,7 @@ cudaError_t BN_CAT(launch_, BN_MODE_NAME)(const Args &a, const Launch &l, cudaSt
     cudaError_t e = prepare(fn, l.cpt, l.split);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     fill_config(cfg, attr, l, l.grid, st);
     void *args[] = {const_cast<Args *>(&a)};
     return cudaLaunchKernelExC(&cfg, fn, args);
@@ -135,8 +140,10 @@ int BN_CAT(occupancy_, BN_MODE_NAME)(const Launch &l, cudaError_t *err)
         return e == cudaSuccess ? per_sm * sms : 0;
     }
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
-    fill_config(cfg, attr, l, l.cluster, nullptr);
+    cudaLaunchAttribute attr[2];
+    Launch one = l;
+    one.pdl = 0;
+    fill_config(cfg, attr, one, l.cluster, nullptr);
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
     *err = e;
