@@ -317,7 +317,9 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     if (group > per_row) group = per_row;
     if (group < 1) group = 1;
     const int gamma_bytes = gamma_slot_bytes(mode, cpt, consumers);
-    const int zbuf_bytes = (split && !(mode & F_Z_OUT)) ? round_up(nchunks * 16, 128) : 0;
+    // shard split: each CTA's z buffer holds R rows of its column slice
+    const int zbuf_bytes =
+        (split && !(mode & F_Z_OUT)) ? round_up(a->R * ((nchunks + cs - 1) / cs) * 16, 128) : 0;
     const int cta_max = d->smem_optin - 1024;  // room for the kernel's static shared memory
     // a group is shrunk until two stages fit one CTA
     while (group > 1 &&
@@ -403,11 +405,12 @@ bn_status plan(int mode, Args *a, Launch *l)
     int resident = 0;
 
     // shard split: finalize modes with an epilogue (or the finalize alone),
-    // R >= 2, and few rows.  Measured on GB300 (R=8): 30 -> 18 us at T=1 and
-    // 4, but slower than the column split from T=16 on, so up to T*R = 64.
+    // R >= 2, and few rows.  Measured on GB300 (R=8, H=8192, k=10), shard
+    // split / column split: T=1 12.1 / 30 us, T=16 22.0 / 28.5 us, T=64
+    // 48.8 / 31.8 us; so up to T*R = 128.
     const bool can_split = (mode & F_FIN) && (mode & (F_RESNORM | F_Z_OUT)) && a->R >= 2;
     const int pref = g_tune_split.load();
-    const bool split = can_split && (pref == 2 || (pref == 0 && (long long)T * a->R <= 64));
+    const bool split = can_split && (pref == 2 || (pref == 0 && (long long)T * a->R <= 128));
     if (split) {
         BN_TRY(shape_for(mode, a, d, true, a->R, l, &resident));
         if (resident > 0) return BN_OK;

@@ -151,28 +151,22 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank)
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
 }
-// Remote shared-memory load; volatile keeps it after the preceding barrier wait.
-__device__ __forceinline__ uint4 ld_cluster_u4(uint32_t addr)
+// Asynchronous remote store of 16 bytes into another CTA's shared memory; its
+// completion counts 16 bytes on that CTA's mbarrier (addresses from mapa).
+__device__ __forceinline__ void st_async_u4(uint32_t addr, const uint4 &v, uint32_t bar)
 {
-    uint4 v;
-    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
-    return v;
-}
-__device__ __forceinline__ void fence_acq_rel_cluster()
-{
-    asm volatile("fence.acq_rel.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void st_cluster_f2(uint32_t addr, float x, float y)
-{
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(x), "f"(y)
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     addr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
                  : "memory");
 }
-__device__ __forceinline__ void mbar_remote_arrive(uint32_t bar_cluster_addr)
+// Asynchronous remote store of a float pair into another CTA's shared memory;
+// its completion counts 8 bytes on that CTA's mbarrier (addresses from mapa).
+__device__ __forceinline__ void st_async_f2(uint32_t addr, float x, float y, uint32_t bar)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
-                     bar_cluster_addr)
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+                     addr),
+                 "f"(x), "f"(y), "r"(bar)
                  : "memory");
 }
 // 1-D TMA bulk copy global -> this CTA's shared memory, completion counted in
@@ -446,12 +440,15 @@ __device__ __forceinline__ float row_sum_squares(f2 S2, f2 E2, int &nred, const 
     if (cs > 1) {
         float2 *slots = sm.xslot + b * kMaxCluster;
         const uint32_t bar = sm.ex0 + 8u * (uint32_t)b;
-        if (tid == 0) {
-            const uint32_t mine = smem_addr(slots + q);
-            for (uint32_t d = 0; d < cs; ++d) {
-                st_cluster_f2(mapa(mine, d), S, E);
-                mbar_remote_arrive(mapa(bar, d));
-            }
+        // Thread d stores this CTA's pair into slot q of CTA d with one
+        // asynchronous remote store that counts 8 bytes on CTA d's barrier;
+        // each CTA's own arrive expects cs * 8 bytes.  The cs sends overlap and
+        // need no fence (one thread storing and release-arriving for every
+        // CTA in turn cost ~2.3 us per exchange at cs = 8 on GB300).
+        if (tid == 0) mbar_arrive_expect_tx(bar, 8u * cs);
+        if (tid < (int)cs) {
+            const uint32_t d = (uint32_t)tid;
+            st_async_f2(mapa(smem_addr(slots + q), d), S, E, mapa(bar, d));
         }
         if (!wait_phase<true, true>(bar, (uint32_t)(nred >> 1) & 1u, ctl)) live = false;
         S = slots[0].x;
@@ -527,7 +524,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
         else if (i < 2 * S) count = (uint32_t)NW;   // empty: one arrive per consumer warp
         else if (i < 2 * S + 2) count = 32u;        // meta_full: every producer lane
         else if (i < 2 * S + 4) count = (uint32_t)NW;  // meta_empty
-        else count = cs;                            // exchange, z ready: one arrive per CTA
+        else count = 1u;                            // exchange, z ready: the owner's expect-tx arrive
         mbar_init(sm.full0 + 8u * (uint32_t)i, count);
     }
     if (tid == 0) s_abort = 0;
@@ -863,53 +860,47 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sm.mempty0 + 8u * slot);
-                // local BF16 rounding; z_q stays in this CTA's shared memory
+                // Local BF16 rounding.  Each 16-byte chunk of z_q goes straight
+                // to the CTA whose column slice holds it, into row q of that
+                // CTA's z buffer ([R][zstride] chunks), as an asynchronous
+                // remote store counted on that CTA's z-ready barrier; each CTA
+                // expects R * nch chunks of 16 bytes.
+                const int zstride = (a.nchunks + (int)cs - 1) / (int)cs;
+                const uint32_t zb = smem_addr(zbuf);
+                if constexpr (REDUCE) {
+                    if (tid == 0) mbar_arrive_expect_tx(zready, (uint32_t)(a.R * nch) * 16u);
+                }
 #pragma unroll
                 for (int i = 0; i < CPT; ++i) {
                     const int lc = tid + i * NT;
                     if (lc < a.nchunks) {
                         const uint4 z = round8(acc[i]);
-                        if constexpr (REDUCE) zbuf[lc] = z;
+                        if constexpr (REDUCE) {
+                            // owner: the last CTA o whose slice starts at or before lc
+                            const int o = ((lc + 1) * (int)cs + a.nchunks - 1) / a.nchunks - 1;
+                            const int oc0 = (int)(((long long)o * a.nchunks) / (long long)cs);
+                            const uint32_t dst = zb + (uint32_t)((int)q * zstride + (lc - oc0)) * 16u;
+                            st_async_u4(mapa(dst, (uint32_t)o), z, mapa(zready, (uint32_t)o));
+                        }
                         if ((Z_OUT || a.z_out != nullptr) && live)
                             *reinterpret_cast<uint4 *>(a.z_out + ((size_t)r * a.T + t) * H +
                                                        (size_t)lc * 8) = z;
                     }
                 }
                 if constexpr (REDUCE) {
-                    // all z rows of the cluster ready: one remote arrive per CTA
-                    fence_acq_rel_cluster();
-                    consumer_sync(NT);
-                    if (tid == 0)
-                        for (uint32_t d = 0; d < cs; ++d) mbar_remote_arrive(mapa(zready, d));
                     if (!wait_phase<true, true>(zready, (uint32_t)it & 1u, ctl)) live = false;
-                    // rank-ordered sum of the R z rows over this CTA's column
-                    // slice; the remote loads of four ranks are issued before
-                    // their (ordered) additions so that their latencies overlap
-                    const uint32_t zb = smem_addr(zbuf);
+                    // rank-ordered sum of the R z rows over this CTA's slice,
+                    // all from its own shared memory
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
                         if (lc < nch) {
-                            const uint32_t za = zb + (uint32_t)(c0 + lc) * 16u;
-                            for (int r0 = 0; r0 < a.R; r0 += 4) {
-                                uint4 zv[4];
+                            widen8(zbuf[lc], s[i]);
+                            for (int rr = 1; rr < a.R; ++rr) {
+                                f2 zf[4];
+                                widen8(zbuf[rr * zstride + lc], zf);
 #pragma unroll
-                                for (int u = 0; u < 4; ++u)
-                                    if (r0 + u < a.R) zv[u] = ld_cluster_u4(mapa(za, (uint32_t)(r0 + u)));
-#pragma unroll
-                                for (int u = 0; u < 4; ++u) {
-                                    if (r0 + u < a.R) {
-                                        f2 zf[4];
-                                        widen8(zv[u], zf);
-                                        if (r0 + u == 0) {
-#pragma unroll
-                                            for (int m = 0; m < 4; ++m) s[i][m] = zf[m];
-                                        } else {
-#pragma unroll
-                                            for (int m = 0; m < 4; ++m) s[i][m] = add2(s[i][m], zf[m]);
-                                        }
-                                    }
-                                }
+                                for (int m = 0; m < 4; ++m) s[i][m] = add2(s[i][m], zf[m]);
                             }
                         }
                     }
