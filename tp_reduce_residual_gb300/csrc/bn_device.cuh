@@ -331,6 +331,37 @@ __device__ __forceinline__ void widen8(const uint4 &v, f2 *x)
     x[3] = widen2(v.w);
 }
 
+// s[m] += the BF16 pair in word m of v, lane by lane, with PTX's mixed-precision
+// add (sm_100 and later): it converts the BF16 operand exactly and rounds the
+// sum once, the result of widening and then adding, in one instruction per
+// element instead of one and a half.
+__device__ __forceinline__ float add_bf16_lo(float c, uint32_t w)
+{
+    float r;
+    asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; add.rn.f32.bf16 %0, lo, %1; }"
+        : "=f"(r)
+        : "f"(c), "r"(w));
+    return r;
+}
+__device__ __forceinline__ float add_bf16_hi(float c, uint32_t w)
+{
+    float r;
+    asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; add.rn.f32.bf16 %0, hi, %1; }"
+        : "=f"(r)
+        : "f"(c), "r"(w));
+    return r;
+}
+__device__ __forceinline__ void add_bf16x8(f2 *s, const uint4 &v)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        float lo, hi;
+        f2_split(s[m], lo, hi);
+        s[m] = f2_make(add_bf16_lo(lo, w[m]), add_bf16_hi(hi, w[m]));
+    }
+}
+
 // Round a pair to BF16 (nearest even) and pack it, low lane in the low half.
 __device__ __forceinline__ uint32_t round2(f2 v)
 {
@@ -849,12 +880,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (lc < a.nchunks) {
-                            f2 x[4];
-                            widen8(chunk(p, lc), x);
-#pragma unroll
-                            for (int m = 0; m < 4; ++m) acc[i][m] = add2(acc[i][m], x[m]);
-                        }
+                        if (lc < a.nchunks) add_bf16x8(acc[i], chunk(p, lc));
                     }
                     release();
                 }
@@ -896,12 +922,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                         const int lc = tid + i * NT;
                         if (lc < nch) {
                             widen8(zbuf[lc], s[i]);
-                            for (int rr = 1; rr < a.R; ++rr) {
-                                f2 zf[4];
-                                widen8(zbuf[rr * zstride + lc], zf);
-#pragma unroll
-                                for (int m = 0; m < 4; ++m) s[i][m] = add2(s[i][m], zf[m]);
-                            }
+                            for (int rr = 1; rr < a.R; ++rr) add_bf16x8(s[i], zbuf[rr * zstride + lc]);
                         }
                     }
                 }
@@ -950,12 +971,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
 #pragma unroll
                         for (int i = 0; i < CPT; ++i) {
                             const int lc = tid + i * NT;
-                            if (lc < nch) {
-                                f2 x[4];
-                                widen8(chunk(p, lc), x);
-#pragma unroll
-                                for (int m = 0; m < 4; ++m) acc[i][m] = add2(acc[i][m], x[m]);
-                            }
+                            if (lc < nch) add_bf16x8(acc[i], chunk(p, lc));
                         }
                         release();
                     }
@@ -969,15 +985,10 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                                 *reinterpret_cast<uint4 *>(a.z_out + ((size_t)r * a.T + t) * H +
                                                            (size_t)(c0 + lc) * 8) = z;
                             if constexpr (REDUCE) {
-                                f2 zf[4];
-                                widen8(z, zf);
-                                if (r == 0) {
-#pragma unroll
-                                    for (int m = 0; m < 4; ++m) s[i][m] = zf[m];
-                                } else {
-#pragma unroll
-                                    for (int m = 0; m < 4; ++m) s[i][m] = add2(s[i][m], zf[m]);
-                                }
+                                if (r == 0)
+                                    widen8(z, s[i]);
+                                else
+                                    add_bf16x8(s[i], z);
                             }
                         }
                     }
@@ -1000,12 +1011,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (lc < nch) {
-                            f2 x[4];
-                            widen8(chunk(p, lc), x);
-#pragma unroll
-                            for (int m = 0; m < 4; ++m) s[i][m] = add2(s[i][m], x[m]);
-                        }
+                        if (lc < nch) add_bf16x8(s[i], chunk(p, lc));
                     }
                     release();
                 }
@@ -1062,13 +1068,9 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
                         if (lc < nch) {
-                            f2 rf[4];
-                            widen8(chunk(p, lc), rf);
+                            add_bf16x8(s[i], chunk(p, lc));  // h = residual + y
 #pragma unroll
-                            for (int m = 0; m < 4; ++m) {
-                                s[i][m] = add2(rf[m], s[i][m]);
-                                acc_square2(S2, E2, s[i][m]);
-                            }
+                            for (int m = 0; m < 4; ++m) acc_square2(S2, E2, s[i][m]);
                             if (live)
                                 *reinterpret_cast<uint4 *>(a.residual + (size_t)t * H +
                                                            (size_t)(c0 + lc) * 8) = round8(s[i]);
