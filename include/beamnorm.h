@@ -191,7 +191,8 @@ BN_API int bn_version(void);
 /* Launch-shape overrides for measurement sweeps (process-wide).  Every field
  * 0 means automatic.  Results do not depend on these settings, only speed. */
 typedef struct {
-    int cluster_size;  /* CTAs per token row: 1, 2, 4, 8 or 16 */
+    int cluster_size;  /* CTAs per token row, at most 16 (a shard split takes
+                          one that divides R) */
     int stages;        /* pipeline depth in stages, at most 64 */
     int threads;       /* consumer threads per CTA: a multiple of 32, at most 512 */
     int ctas_per_sm;   /* CTAs sharing one SM, at most 8 (capped by registers) */

@@ -135,7 +135,8 @@ def test_split_and_finalize_only_reject_bad_arguments(L):
 def test_set_tuning_validates(L):
     def st(*fields):
         return L.bn_set_tuning(ctypes.byref(bn._Tuning(*fields)))
-    assert st(3, 0, 0, 0, 0, 0) == bn.ERR_INVALID
+    assert st(17, 0, 0, 0, 0, 0) == bn.ERR_INVALID
+    assert st(-1, 0, 0, 0, 0, 0) == bn.ERR_INVALID
     assert st(0, 1, 0, 0, 0, 0) == bn.ERR_INVALID
     assert st(0, 65, 0, 0, 0, 0) == bn.ERR_INVALID
     assert st(0, 0, 48, 0, 0, 0) == bn.ERR_INVALID

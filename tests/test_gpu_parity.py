@@ -203,7 +203,7 @@ def test_launch_query_is_coherent(op, R, T, k, H):
     assert i["resident_ctas"] >= i["grid"]
     assert i["smem_bytes"] <= props.shared_memory_per_block_optin
     if i["split"]:
-        assert op.startswith("finalize") and i["cluster_size"] == R
+        assert op.startswith("finalize") and R % i["cluster_size"] == 0
     try:
         bn.set_tuning(stages=2, split=1 if op.startswith("finalize") else 0)
         j = bn.launch_info(op, R, T, H, k)
@@ -220,33 +220,45 @@ SPLIT_CASES = [
     (2, 7, 3, 256, True, False),
     (16, 2, 16, 4096, True, False),
     (4, 40, 6, 2048, True, False),   # more rows than one pass of clusters
+    (6, 9, 5, 1536, True, False),    # cluster sizes 2, 3 and 6
+    (12, 2, 3, 768, True, False),    # cluster sizes 2, 3, 4, 6 and 12
 ]
 
 
 @pytest.mark.parametrize("R,T,k,H,with_shared,single", SPLIT_CASES)
 def test_shard_split_matches_column_split_and_oracle(R, T, k, H, with_shared, single):
-    """A cluster that splits a row by shard (each CTA finalizes one shard over
-    the whole row, then the z rows are summed in rank order through
-    distributed shared memory) gives the bits of the column split."""
+    """A cluster that splits a row by shard (each of its cs CTAs finalizes R/cs
+    shards over the whole row and sends every chunk of each z row to the CTA
+    owning that column slice, where the R rows are summed in rank order)
+    gives the bits of the column split, for every cluster size dividing R."""
     wl = inputs.custom("finalize_reduce_norm", R, H, k, partial_std=0.3, shared_std=0.3)
     d = parity.gpu_inputs(wl, T, seed=500 + R * 13 + T, with_shared=with_shared)
+    sizes = [c for c in range(2, R + 1) if R % c == 0]
+    runs = {}
     try:
-        bn.set_tuning(split=2)
-        g = parity.run_fused(d, single=single)
         bn.set_tuning(split=1)
         base = parity.run_fused(d, single=single)
+        for c in sizes:
+            bn.set_tuning(cluster_size=c, split=2)
+            info = bn.launch_info("finalize_reduce_residual_norm" if single else "finalize_reduce_norm",
+                                  R, T, H, k, has_shared=with_shared)
+            assert info["split"] == 1 and info["cluster_size"] == c, info
+            runs[info["cluster_size"]] = parity.run_fused(d, single=single)
     finally:
         bn.set_tuning()
-    for key in ("sum", "ss", "z", "out", "residual_out"):
-        assert_bits_equal(g[key], base[key], key)
-    parity.compare(g, parity.run_oracle(d, single=single), what=f"split R={R} T={T} k={k} H={H}")
+    for c, g in runs.items():
+        for key in ("sum", "ss", "z", "out", "residual_out"):
+            assert_bits_equal(g[key], base[key], f"cs={c} {key}")
+    parity.compare(base, parity.run_oracle(d, single=single), what=f"split R={R} T={T} k={k} H={H}")
 
 
-def test_shard_split_finalize_only():
+@pytest.mark.parametrize("cs", [8, 4, 2])
+def test_shard_split_finalize_only(cs):
     wl = inputs.WORKLOADS[4]
     d = parity.gpu_inputs(wl, 4)
     try:
-        bn.set_tuning(split=2)
+        bn.set_tuning(cluster_size=cs, split=2)
+        assert bn.launch_info("finalize_only", wl.R, 4, wl.H, wl.k)["cluster_size"] == cs
         z = bn.finalize_only(d["expert_out"], d["perm"], d["w"], d["shared"])
         torch.cuda.synchronize()
     finally:

@@ -265,11 +265,12 @@ int auto_cluster(int T, int nchunks, int sms, long long row_bytes)
     return cs;
 }
 
-// Copies the producer issues per token row.
-int loads_per_row(int mode, const Args &a, bool split)
+// Copies the producer of one CTA issues per token row (cs: the cluster size of
+// a shard split, whose CTAs take R / cs shards each).
+int loads_per_row(int mode, const Args &a, bool split, int cs)
 {
     if (mode & F_SUM_IN) return 2;
-    int n = (mode & F_FIN) ? (split ? 1 : a.R) * (a.k + (a.shared ? 1 : 0)) : a.R;
+    int n = (mode & F_FIN) ? (split ? a.R / cs : a.R) * (a.k + (a.shared ? 1 : 0)) : a.R;
     if (mode & F_RESNORM) n += 1;
     return n;
 }
@@ -291,7 +292,7 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     const bool sum_in = (mode & F_SUM_IN) != 0;
     const bool fin = (mode & F_FIN) != 0;
     const int nchunks = H / 8;
-    const int per_row = loads_per_row(mode, *a, split);
+    const int per_row = loads_per_row(mode, *a, split, cs);
     // measured on GB300: the finalize modes run best with 512 consumer threads
     // (one CTA per SM), the reduce modes with 256 and several CTAs per SM
     const int cap = g_tune_threads.load() > 0 ? g_tune_threads.load() : (fin ? kMaxConsumers : 256);
@@ -316,7 +317,8 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     if (sum_in || split) group = 1;  // items of different sizes in one row
     if (group > per_row) group = per_row;
     if (group < 1) group = 1;
-    const int gamma_bytes = gamma_slot_bytes(mode, cpt, consumers);
+    const int slice = (nchunks + cs - 1) / cs;  // the largest column slice of the epilogue
+    const int gamma_bytes = gamma_slot_bytes(mode, slice);
     // shard split: each CTA's z buffer holds R rows of its column slice
     const int zbuf_bytes =
         (split && !(mode & F_Z_OUT)) ? round_up(a->R * ((nchunks + cs - 1) / cs) * 16, 128) : 0;
@@ -386,6 +388,7 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     a->group = group;
     a->item_bytes = item_bytes;
     a->gamma_bytes = gamma_bytes;
+    a->gamma_stride = slice;
     a->zbuf_bytes = zbuf_bytes;
     a->spin_wait = g_tune_wait.load() == 2 ? 1 : 0;
     a->nchunks = nchunks;
@@ -404,20 +407,25 @@ bn_status plan(int mode, Args *a, Launch *l)
     const int nchunks = H / 8;
     int resident = 0;
 
-    // shard split: finalize modes with an epilogue (or the finalize alone),
-    // R >= 2, and few rows.  Measured on GB300 (R=8, H=8192, k=10), shard
-    // split / column split: T=1 12.1 / 30 us, T=16 22.0 / 28.5 us, T=64
-    // 48.8 / 31.8 us; so up to T*R = 128.
+    // Shard split: finalize modes with an epilogue (or the finalize alone),
+    // R >= 2, few rows.  The cluster takes the largest size cs dividing R
+    // whose clusters all fit on the device at once for these T rows (one
+    // wave); each CTA finalizes R / cs shards.  Measured on GB300 (R=8,
+    // H=8192, k=10; shard / column split): T=1 12.1 / 30 us, T=16 22.0 / 28.5
+    // us with cs=8 (15 resident clusters: two waves).
     const bool can_split = (mode & F_FIN) && (mode & (F_RESNORM | F_Z_OUT)) && a->R >= 2;
     const int pref = g_tune_split.load();
-    const bool split = can_split && (pref == 2 || (pref == 0 && (long long)T * a->R <= 128));
-    if (split) {
-        BN_TRY(shape_for(mode, a, d, true, a->R, l, &resident));
-        if (resident > 0) return BN_OK;
+    if (can_split && (pref == 2 || (pref == 0 && (long long)T * a->R <= 512))) {
+        const int want_cs = g_tune_cluster.load();
+        for (int c = a->R < kMaxCluster ? a->R : kMaxCluster; c >= 2; --c) {
+            if (a->R % c != 0 || (want_cs > 0 && c != want_cs)) continue;
+            BN_TRY(shape_for(mode, a, d, true, c, l, &resident));
+            if (resident > 0 && (pref == 2 || T <= resident)) return BN_OK;
+        }
     }
 
     int cs = g_tune_cluster.load();
-    if (cs <= 0) cs = auto_cluster(T, nchunks, d->sms, (long long)loads_per_row(mode, *a, false) * 2 * H);
+    if (cs <= 0) cs = auto_cluster(T, nchunks, d->sms, (long long)loads_per_row(mode, *a, false, 1) * 2 * H);
     if (cs > nchunks) cs = 1;
     for (;; cs /= 2) {
         BN_TRY(shape_for(mode, a, d, false, cs, l, &resident));
@@ -782,8 +790,8 @@ bn_status bn_set_tuning(const bn_tuning *t)
     std::memset(&z, 0, sizeof z);
     if (!t) t = &z;
     const int cs = t->cluster_size;
-    if (cs != 0 && cs != 1 && cs != 2 && cs != 4 && cs != 8 && cs != 16)
-        return fail(BN_ERR_INVALID, "cluster_size must be 0, 1, 2, 4, 8 or 16");
+    if (cs < 0 || cs > kMaxCluster)
+        return fail(BN_ERR_INVALID, "cluster_size must be in [0, %d]", kMaxCluster);
     if (t->stages < 0 || t->stages > kMaxStages || t->stages == 1)
         return fail(BN_ERR_INVALID, "stages must be 0 or in [2, %d]", kMaxStages);
     if (t->threads < 0 || t->threads > kMaxConsumers || t->threads % 32 != 0)

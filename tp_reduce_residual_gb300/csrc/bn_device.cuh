@@ -490,12 +490,13 @@ __device__ __forceinline__ float row_sum_squares(f2 S2, f2 E2, int &nred, const 
     return S + E;
 }
 
-// SPLITR (finalize modes only): the CTAs of a cluster split a token row by
-// shard instead of by columns.  CTA q finalizes shard q over the whole row
-// (k + 1 copies instead of R * (k + 1)), keeps its BF16 result z_q in shared
-// memory, and after a cluster-wide signal every CTA sums the R z rows of its
-// own column slice in rank order through distributed shared memory; the
-// epilogue then runs on the slice exactly as in the column split.
+// SPLITR (finalize modes only): the cs CTAs of a cluster split a token row by
+// shard instead of by columns (cs divides R).  CTA q finalizes shards
+// q * R/cs .. (q + 1) * R/cs - 1 over the whole row ((k + 1) * R/cs copies
+// instead of R * (k + 1)) and sends every chunk of each BF16 result z_r to
+// the CTA whose column slice holds it; each CTA then sums the R z rows of its
+// slice in rank order and runs the epilogue on the slice exactly as in the
+// column split.
 template <int MODE, int CPT, bool SPLITR>
 __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
 {
@@ -533,9 +534,9 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
     const uint32_t q = cluster_ctarank();
     const int cl = (int)cluster_id_x();
     const int ncl = (int)ncluster_x();
-    // The shard split needs exactly one CTA per shard in a cluster (the host
-    // launches it so); any other shape returns at once, before any barrier.
-    if (SPLITR && cs != (uint32_t)a.R) {
+    // The shard split needs a cluster size that divides R (the host launches
+    // it so); any other shape returns at once, before any barrier.
+    if (SPLITR && (a.R % (int)cs) != 0) {
         griddep_wait();
         if (threadIdx.x == 0) atomicOr(a.err, kErrTimeout);
         return;
@@ -575,7 +576,8 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
     // A stage holds up to G = a.group consecutive items of one row (one
     // barrier for all of them); a row always ends on a stage boundary.
     const int per_shard = FIN ? a.k + (has_shared ? 1 : 0) : 1;
-    const int row_items = (SUM_IN ? 1 : (SPLITR ? 1 : a.R) * per_shard) + (RESNORM ? 1 : 0);
+    const int spc = SPLITR ? a.R / (int)cs : a.R;  // shards per CTA (shard split)
+    const int row_items = (SUM_IN ? 1 : spc * per_shard) + (RESNORM ? 1 : 0);
     const uint32_t zready = sm.ex0 + 16u;       // shard split: the z rows of all CTAs are ready
     uint4 *zbuf = reinterpret_cast<uint4 *>(smem + L.zbuf_off);
     const int G = a.group;
@@ -669,14 +671,16 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                 if constexpr (SUM_IN) {
                     ok = put(a.sum_in + (size_t)t * H + col, bytes16 * 2u);
                 } else if constexpr (FIN && SPLITR) {
-                    // this CTA's shard over the whole row
+                    // this CTA's shards over the whole row
                     const int32_t *mp = sm.mperm + slot * kMaxMeta;
-                    const int r = (int)q;
                     const uint32_t row_bytes = (uint32_t)a.nchunks * 16u;
-                    const uint16_t *xr = a.src + (size_t)r * a.T * a.k * H;
-                    for (int j = 0; j < a.k && ok; ++j)
-                        ok = put(xr + (size_t)mp[r * a.k + j] * H, row_bytes);
-                    if (ok && has_shared) ok = put(a.shared + ((size_t)r * a.T + t) * H, row_bytes);
+                    for (int rr = 0; rr < spc && ok; ++rr) {
+                        const int r = (int)q * spc + rr;
+                        const uint16_t *xr = a.src + (size_t)r * a.T * a.k * H;
+                        for (int j = 0; j < a.k && ok; ++j)
+                            ok = put(xr + (size_t)mp[r * a.k + j] * H, row_bytes);
+                        if (ok && has_shared) ok = put(a.shared + ((size_t)r * a.T + t) * H, row_bytes);
+                    }
                 } else if constexpr (FIN) {
                     const int32_t *mp = sm.mperm + slot * kMaxMeta;
                     for (int r = 0; r < a.R && ok; ++r) {
@@ -750,9 +754,10 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
             return *reinterpret_cast<const uint4 *>(p + (size_t)lc * 16);
         };
         // Gamma slots: each consumer thread copies the gammas of its own chunks
-        // into shared memory once, laid out so that a warp's 16-byte reads are
-        // contiguous; it alone reads them back (no barrier needed).
-        //   slot (g, i, half) = gsm[((g * CPT + i) * 2 + half) * NT + tid]
+        // into shared memory once, laid out by chunk so that a warp's 16-byte
+        // reads are contiguous; it alone reads them back (no barrier needed).
+        //   slot (g, half, lc) = gsm[(g * 2 + half) * gstride + lc], lc < nch
+        const int gstride = a.gamma_stride;
         float4 *gsm = reinterpret_cast<float4 *>(smem + L.gamma_off);
         constexpr int kGPost = 0;
         constexpr int kGPre = POSTNORM ? 1 : 0;
@@ -762,19 +767,20 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                 const int lc = tid + i * NT;
                 if (lc < nch) {
                     const float4 *gq = reinterpret_cast<const float4 *>(a.gamma_pre + (size_t)(c0 + lc) * 8);
-                    gsm[((kGPre * CPT + i) * 2 + 0) * NT + tid] = __ldg(gq);
-                    gsm[((kGPre * CPT + i) * 2 + 1) * NT + tid] = __ldg(gq + 1);
+                    gsm[(kGPre * 2 + 0) * gstride + lc] = __ldg(gq);
+                    gsm[(kGPre * 2 + 1) * gstride + lc] = __ldg(gq + 1);
                     if constexpr (POSTNORM) {
                         const float4 *gp = reinterpret_cast<const float4 *>(a.gamma_post + (size_t)(c0 + lc) * 8);
-                        gsm[((kGPost * CPT + i) * 2 + 0) * NT + tid] = __ldg(gp);
-                        gsm[((kGPost * CPT + i) * 2 + 1) * NT + tid] = __ldg(gp + 1);
+                        gsm[(kGPost * 2 + 0) * gstride + lc] = __ldg(gp);
+                        gsm[(kGPost * 2 + 1) * gstride + lc] = __ldg(gp + 1);
                     }
                 }
             }
         }
         auto gamma8 = [&](int g, int i, f2 *out) {
-            const float4 x = gsm[((g * CPT + i) * 2 + 0) * NT + tid];
-            const float4 y = gsm[((g * CPT + i) * 2 + 1) * NT + tid];
+            const int lc = tid + i * NT;
+            const float4 x = gsm[(g * 2 + 0) * gstride + lc];
+            const float4 y = gsm[(g * 2 + 1) * gstride + lc];
             out[0] = f2_make(x.x, x.y);
             out[1] = f2_make(x.z, x.w);
             out[2] = f2_make(y.x, y.y);
@@ -810,109 +816,112 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                 if (!wait_phase<false, true>(sm.mfull0 + 8u * slot, ((uint32_t)it >> 1) & 1u, ctl))
                     live = false;
                 const float *wrow = sm.mw + slot * kMaxMeta;
-                const int r = (int)q;
-                // shard q over the whole row: chunks tid + i * NT < nchunks
-                f2 acc[CPT][4];
-#pragma unroll
-                for (int i = 0; i < CPT; ++i)
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) acc[i][m] = 0ull;
-                // Up to four gathered rows (one stage each here) are waited for
-                // together; their loads and products are independent and only
-                // the additions run in slot order, so the dependent chain per
-                // row is one add instead of a full load-multiply-add.
-                const int U = S < 4 ? S : 4;
-                auto ahead = [&](int u) -> const uint8_t * {
-                    uint32_t st = stage + (uint32_t)u, ph = phase;
-                    if (st >= (uint32_t)S) {
-                        st -= (uint32_t)S;
-                        ph ^= 1u;
-                    }
-                    if (!wait_phase<false, true>(sm.full0 + 8u * st, ph, ctl)) live = false;
-                    return sm.stages + (size_t)st * (size_t)a.stage_bytes;
-                };
-                for (int j0 = 0; j0 < a.k; j0 += U) {
-                    const int n = (a.k - j0) < U ? (a.k - j0) : U;
-                    const uint8_t *pp[4] = {nullptr, nullptr, nullptr, nullptr};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        if (u < n) pp[u] = ahead(u);
-#pragma unroll
-                    for (int i = 0; i < CPT; ++i) {
-                        const int lc = tid + i * NT;
-                        if (lc < a.nchunks) {
-                            uint4 v[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                if (u < n) v[u] = chunk(pp[u], lc);
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                if (u < n) {
-                                    const float wj = wrow[r * a.k + j0 + u];
-                                    const f2 w2 = f2_make(wj, wj);
-                                    f2 x[4];
-                                    widen8(v[u], x);
-                                    if (j0 + u == 0) {
-#pragma unroll
-                                        for (int m = 0; m < 4; ++m) acc[i][m] = mul_sep2(w2, x[m]);
-                                    } else {
-#pragma unroll
-                                        for (int m = 0; m < 4; ++m)
-                                            acc[i][m] = add2(acc[i][m], mul_sep2(w2, x[m]));
-                                    }
-                                }
-                            }
-                        }
-                    }
-                    // release the n stages in order (one item each)
-                    for (int u = 0; u < n; ++u) {
-                        --cleft;
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(sm.empty0 + 8u * stage);
-                        if (++stage == (uint32_t)S) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
-                    }
-                }
-                if (has_shared) {
-                    const uint8_t *p = take();
-#pragma unroll
-                    for (int i = 0; i < CPT; ++i) {
-                        const int lc = tid + i * NT;
-                        if (lc < a.nchunks) add_bf16x8(acc[i], chunk(p, lc));
-                    }
-                    release();
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sm.mempty0 + 8u * slot);
-                // Local BF16 rounding.  Each 16-byte chunk of z_q goes straight
-                // to the CTA whose column slice holds it, into row q of that
-                // CTA's z buffer ([R][zstride] chunks), as an asynchronous
+                // Each 16-byte chunk of every z_r this CTA finalizes goes
+                // straight to the CTA whose column slice holds it, into row r of
+                // that CTA's z buffer ([R][zstride] chunks), as an asynchronous
                 // remote store counted on that CTA's z-ready barrier; each CTA
-                // expects R * nch chunks of 16 bytes.
+                // expects R * nch chunks of 16 bytes per token row.
                 const int zstride = (a.nchunks + (int)cs - 1) / (int)cs;
                 const uint32_t zb = smem_addr(zbuf);
                 if constexpr (REDUCE) {
                     if (tid == 0) mbar_arrive_expect_tx(zready, (uint32_t)(a.R * nch) * 16u);
                 }
+                // shards q * spc .. q * spc + spc - 1, each over the whole row
+                // (chunks tid + i * NT < nchunks)
+                for (int rr = 0; rr < spc; ++rr) {
+                    const int r = (int)q * spc + rr;
+                    f2 acc[CPT][4];
 #pragma unroll
-                for (int i = 0; i < CPT; ++i) {
-                    const int lc = tid + i * NT;
-                    if (lc < a.nchunks) {
-                        const uint4 z = round8(acc[i]);
-                        if constexpr (REDUCE) {
-                            // owner: the last CTA o whose slice starts at or before lc
-                            const int o = ((lc + 1) * (int)cs + a.nchunks - 1) / a.nchunks - 1;
-                            const int oc0 = (int)(((long long)o * a.nchunks) / (long long)cs);
-                            const uint32_t dst = zb + (uint32_t)((int)q * zstride + (lc - oc0)) * 16u;
-                            st_async_u4(mapa(dst, (uint32_t)o), z, mapa(zready, (uint32_t)o));
+                    for (int i = 0; i < CPT; ++i)
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) acc[i][m] = 0ull;
+                    // Up to four gathered rows (one stage each here) are waited
+                    // for together; their loads and products are independent and
+                    // only the additions run in slot order.
+                    const int U = S < 4 ? S : 4;
+                    auto ahead = [&](int u) -> const uint8_t * {
+                        uint32_t st = stage + (uint32_t)u, ph = phase;
+                        if (st >= (uint32_t)S) {
+                            st -= (uint32_t)S;
+                            ph ^= 1u;
                         }
-                        if ((Z_OUT || a.z_out != nullptr) && live)
-                            *reinterpret_cast<uint4 *>(a.z_out + ((size_t)r * a.T + t) * H +
-                                                       (size_t)lc * 8) = z;
+                        if (!wait_phase<false, true>(sm.full0 + 8u * st, ph, ctl)) live = false;
+                        return sm.stages + (size_t)st * (size_t)a.stage_bytes;
+                    };
+                    for (int j0 = 0; j0 < a.k; j0 += U) {
+                        const int n = (a.k - j0) < U ? (a.k - j0) : U;
+                        const uint8_t *pp[4] = {nullptr, nullptr, nullptr, nullptr};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            if (u < n) pp[u] = ahead(u);
+#pragma unroll
+                        for (int i = 0; i < CPT; ++i) {
+                            const int lc = tid + i * NT;
+                            if (lc < a.nchunks) {
+                                uint4 v[4];
+#pragma unroll
+                                for (int u = 0; u < 4; ++u)
+                                    if (u < n) v[u] = chunk(pp[u], lc);
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    if (u < n) {
+                                        const float wj = wrow[r * a.k + j0 + u];
+                                        const f2 w2 = f2_make(wj, wj);
+                                        f2 x[4];
+                                        widen8(v[u], x);
+                                        if (j0 + u == 0) {
+#pragma unroll
+                                            for (int m = 0; m < 4; ++m) acc[i][m] = mul_sep2(w2, x[m]);
+                                        } else {
+#pragma unroll
+                                            for (int m = 0; m < 4; ++m)
+                                                acc[i][m] = add2(acc[i][m], mul_sep2(w2, x[m]));
+                                        }
+                                    }
+                                }
+                            }
+                        }
+                        // release the n stages in order (one item each)
+                        for (int u = 0; u < n; ++u) {
+                            --cleft;
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(sm.empty0 + 8u * stage);
+                            if (++stage == (uint32_t)S) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
+                        }
+                    }
+                    if (has_shared) {
+                        const uint8_t *p = take();
+#pragma unroll
+                        for (int i = 0; i < CPT; ++i) {
+                            const int lc = tid + i * NT;
+                            if (lc < a.nchunks) add_bf16x8(acc[i], chunk(p, lc));
+                        }
+                        release();
+                    }
+                    // local BF16 rounding, then each chunk to its owner
+#pragma unroll
+                    for (int i = 0; i < CPT; ++i) {
+                        const int lc = tid + i * NT;
+                        if (lc < a.nchunks) {
+                            const uint4 z = round8(acc[i]);
+                            if constexpr (REDUCE) {
+                                // owner: the last CTA o whose slice starts at or before lc
+                                const int o = ((lc + 1) * (int)cs + a.nchunks - 1) / a.nchunks - 1;
+                                const int oc0 = (int)(((long long)o * a.nchunks) / (long long)cs);
+                                const uint32_t dst = zb + (uint32_t)(r * zstride + (lc - oc0)) * 16u;
+                                st_async_u4(mapa(dst, (uint32_t)o), z, mapa(zready, (uint32_t)o));
+                            }
+                            if ((Z_OUT || a.z_out != nullptr) && live)
+                                *reinterpret_cast<uint4 *>(a.z_out + ((size_t)r * a.T + t) * H +
+                                                           (size_t)lc * 8) = z;
+                        }
                     }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sm.mempty0 + 8u * slot);
                 if constexpr (REDUCE) {
                     if (!wait_phase<true, true>(zready, (uint32_t)it & 1u, ctl)) live = false;
                     // rank-ordered sum of the R z rows over this CTA's slice,
@@ -947,7 +956,9 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                         }
                         release();
                     }
-                    // slots 1..k-1: acc = acc + wj * xj
+                    // slots 1..k-1: acc = acc + wj * xj (two slots per iteration
+                    // let the next copy's loads issue ahead of this one's adds)
+#pragma unroll 2
                     for (int j = 1; j < a.k; ++j) {
                         const float wj = wrow[r * a.k + j];
                         const f2 w2 = f2_make(wj, wj);

@@ -58,6 +58,7 @@ struct Args {
     int group;                // row copies (items) per stage
     int item_bytes;           // stride of one item in a stage (multiple of 128)
     int gamma_bytes;          // shared-memory bytes of the per-thread gamma slots
+    int gamma_stride;         // 16-byte slots per gamma half: the largest column slice in chunks
     int zbuf_bytes;           // shard split: shared-memory bytes of one full z row
     int spin_wait;            // 1: poll barriers with test_wait; 0: try_wait
     float eps;
@@ -96,11 +97,11 @@ struct SmemLayout {
 };
 
 // Shared-memory bytes of the gamma slots: 32 bytes per chunk per gamma.
-__host__ __device__ inline int gamma_slot_bytes(int mode, int cpt, int consumers)
+__host__ __device__ inline int gamma_slot_bytes(int mode, int slice_chunks)
 {
     if (!(mode & F_RESNORM)) return 0;
     const int ngamma = (mode & F_POSTNORM) ? 2 : 1;
-    return ngamma * 32 * cpt * consumers;
+    return ngamma * 32 * slice_chunks;
 }
 
 // Per-mode host entry points, defined in the kernel translation units:
