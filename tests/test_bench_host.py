@@ -85,3 +85,12 @@ def test_reference_arm_runs_on_cpu_and_prints_one_line():
 def test_measured_peak_is_read_or_falls_back():
     peak, kind = bench.measured_peak()
     assert peak > 1000 and kind in ("measured", "fallback")
+
+
+def test_kernel_hash_ignores_comments_only():
+    a = 'int f(int x) { return x + 1; }  // add one\n'
+    b = '/* the successor */\nint f(int x)\n{\n    return x + 1;  // comment changed\n}\n'
+    c = 'int f(int x) { return x + 2; }\n'
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    assert bench._code_only('const char *s = "a // b";') == 'const char *s = "a // b";'

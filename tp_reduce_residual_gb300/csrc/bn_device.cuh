@@ -28,8 +28,9 @@
 //     one explicit fma for the error term, two-sum for the additions), combined
 //     in a fixed warp/block/cluster tree, and rounded once: the result is the
 //     FP32 rounding of the exact sum, independent of the row's split.
-//   * Cluster partial sums travel through distributed shared memory (remote
-//     st.shared::cluster plus a remote mbarrier arrive) -- no global scratch.
+//   * Cluster partial sums (and the shard split's z rows) travel through
+//     distributed shared memory as st.async remote stores whose completion
+//     the receiving CTA's mbarrier counts in bytes -- no global scratch.
 //   * Every wait is bounded (SM cycles and polls); on expiry the kernel records an error bit,
 //     stops issuing copies, drains the copies it has in flight, runs the rest of
 //     its control flow without waiting and without storing, and returns.
