@@ -499,7 +499,7 @@ __device__ __forceinline__ float row_sum_squares(f2 S2, f2 E2, int &nred, const 
 // slice in rank order and runs the epilogue on the slice exactly as in the
 // column split.
 template <int MODE, int CPT, bool SPLITR>
-__global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
+__global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 {
     constexpr bool FIN = (MODE & F_FIN) != 0;
     constexpr bool SUM_IN = (MODE & F_SUM_IN) != 0;
@@ -583,6 +583,17 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
     uint4 *zbuf = reinterpret_cast<uint4 *>(smem + L.zbuf_off);
     const int G = a.group;
     const uint32_t item_bytes = (uint32_t)a.item_bytes;
+    // Items per stage, from the items left in the row: up to G.  In the shard
+    // split the residual copy (a column slice) is smaller than the whole-row
+    // copies before it, so it takes a stage of its own.
+    constexpr bool kLoneLast = SPLITR && RESNORM;
+    auto items_in_stage = [&](int left) -> int {
+        if (kLoneLast) {
+            if (left == 1) return 1;
+            --left;
+        }
+        return left < G ? left : G;
+    };
 
     if (warp == NW) {
         // ================= producer warp =================
@@ -650,7 +661,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                 auto put = [&](const void *src, uint32_t bytes) -> bool {
                     const uint32_t fb = sm.full0 + 8u * stage;
                     if (pos == 0) {
-                        n_in = left < G ? left : G;
+                        n_in = items_in_stage(left);
                         if (!wait_phase<false, true>(sm.empty0 + 8u * stage, phase ^ 1u, ctl)) return false;
                         mbar_arrive_expect_tx(fb, bytes * (uint32_t)n_in);
                         ++issued;
@@ -733,7 +744,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
         const uint8_t *cbase = sm.stages;
         auto take = [&]() -> const uint8_t * {
             if (cpos == 0) {
-                cn = cleft < G ? cleft : G;
+                cn = items_in_stage(cleft);
                 if (!wait_phase<false, true>(sm.full0 + 8u * stage, phase, ctl)) live = false;
                 cbase = sm.stages + (size_t)stage * (size_t)a.stage_bytes;
             }
@@ -836,62 +847,39 @@ __global__ void __launch_bounds__(kMaxConsumers + 32) bn_kernel(const Args a)
                     for (int i = 0; i < CPT; ++i)
 #pragma unroll
                         for (int m = 0; m < 4; ++m) acc[i][m] = 0ull;
-                    // Up to four gathered rows (one stage each here) are waited
-                    // for together; their loads and products are independent and
-                    // only the additions run in slot order.
-                    const int U = S < 4 ? S : 4;
-                    auto ahead = [&](int u) -> const uint8_t * {
-                        uint32_t st = stage + (uint32_t)u, ph = phase;
-                        if (st >= (uint32_t)S) {
-                            st -= (uint32_t)S;
-                            ph ^= 1u;
-                        }
-                        if (!wait_phase<false, true>(sm.full0 + 8u * st, ph, ctl)) live = false;
-                        return sm.stages + (size_t)st * (size_t)a.stage_bytes;
-                    };
-                    for (int j0 = 0; j0 < a.k; j0 += U) {
-                        const int n = (a.k - j0) < U ? (a.k - j0) : U;
-                        const uint8_t *pp[4] = {nullptr, nullptr, nullptr, nullptr};
+                    // slot 0: acc = w0 * x0
+                    {
+                        const float w0 = wrow[r * a.k];
+                        const f2 w2 = f2_make(w0, w0);
+                        const uint8_t *p = take();
 #pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            if (u < n) pp[u] = ahead(u);
+                        for (int i = 0; i < CPT; ++i) {
+                            const int lc = tid + i * NT;
+                            f2 x[4] = {0ull, 0ull, 0ull, 0ull};
+                            if (lc < a.nchunks) widen8(chunk(p, lc), x);
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) acc[i][m] = mul_sep2(w2, x[m]);
+                        }
+                        release();
+                    }
+                    // slots 1..k-1: acc = acc + wj * xj
+#pragma unroll 2
+                    for (int j = 1; j < a.k; ++j) {
+                        const float wj = wrow[r * a.k + j];
+                        const f2 w2 = f2_make(wj, wj);
+                        const uint8_t *p = take();
 #pragma unroll
                         for (int i = 0; i < CPT; ++i) {
                             const int lc = tid + i * NT;
                             if (lc < a.nchunks) {
-                                uint4 v[4];
+                                f2 x[4];
+                                widen8(chunk(p, lc), x);
 #pragma unroll
-                                for (int u = 0; u < 4; ++u)
-                                    if (u < n) v[u] = chunk(pp[u], lc);
-#pragma unroll
-                                for (int u = 0; u < 4; ++u) {
-                                    if (u < n) {
-                                        const float wj = wrow[r * a.k + j0 + u];
-                                        const f2 w2 = f2_make(wj, wj);
-                                        f2 x[4];
-                                        widen8(v[u], x);
-                                        if (j0 + u == 0) {
-#pragma unroll
-                                            for (int m = 0; m < 4; ++m) acc[i][m] = mul_sep2(w2, x[m]);
-                                        } else {
-#pragma unroll
-                                            for (int m = 0; m < 4; ++m)
-                                                acc[i][m] = add2(acc[i][m], mul_sep2(w2, x[m]));
-                                        }
-                                    }
-                                }
+                                for (int m = 0; m < 4; ++m)
+                                    acc[i][m] = add2(acc[i][m], mul_sep2(w2, x[m]));
                             }
                         }
-                        // release the n stages in order (one item each)
-                        for (int u = 0; u < n; ++u) {
-                            --cleft;
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(sm.empty0 + 8u * stage);
-                            if (++stage == (uint32_t)S) {
-                                stage = 0;
-                                phase ^= 1u;
-                            }
-                        }
+                        release();
                     }
                     if (has_shared) {
                         const uint8_t *p = take();
