@@ -323,9 +323,12 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     const int zbuf_bytes =
         (split && !(mode & F_Z_OUT)) ? round_up(a->R * ((nchunks + cs - 1) / cs) * 16, 128) : 0;
     const int cta_max = d->smem_optin - 1024;  // room for the kernel's static shared memory
-    // a group is shrunk until two stages fit one CTA
-    while (group > 1 &&
-           (int)SmemLayout::make(2, group * item_bytes, gamma_bytes, zbuf_bytes, fin).total > cta_max)
+    // A group is shrunk until two stages fit one CTA, or three when the group
+    // is automatic (measured, shard split of C4 at T=64: 2 stages of 3 copies
+    // 27.9 us, 3 stages of 2 copies 26.1 us).
+    const int min_stages = g_tune_group.load() > 0 ? 2 : 3;
+    while (group > 1 && (int)SmemLayout::make(min_stages, group * item_bytes, gamma_bytes, zbuf_bytes,
+                                              fin).total > cta_max)
         --group;
     const int stage_bytes = group * item_bytes;
     const int stages_per_row = (per_row + group - 1) / group;
