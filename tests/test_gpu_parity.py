@@ -45,6 +45,7 @@ REDUCE_SMALL = [
     (1, 3, 8, False, 0.5),         # one chunk per row
     (16, 2, 32768, False, 0.5),    # largest served R and H
     (5, 153, 6144, True, 0.5),     # more rows than SMs
+    (4, 300, 32768, False, 0.5),   # largest H with many rows: the row needs a cluster
 ]
 
 
@@ -63,6 +64,7 @@ FIN_SMALL = [
     (2, 7, 3, 1000),
     (1, 5, 1, 64),
     (16, 3, 16, 4096),             # R*k = 256, the served maximum
+    (2, 200, 2, 32768),            # largest H with many rows
 ]
 
 
@@ -210,6 +212,23 @@ def test_launch_query_is_coherent(op, R, T, k, H):
     finally:
         bn.set_tuning()
     assert j["stages"] == 2 and j["split"] == 0
+
+
+@pytest.mark.gpu
+def test_every_supported_shape_has_a_launch():
+    """bn_supports promises a launch for every valid shape it accepts: the
+    planner finds one (widening the row split where one CTA's shared memory
+    cannot hold a slice) for the extremes of R, k, T and H."""
+    for H in (8, 256, 5120, 8192, 16384, 24576, 32768):
+        for R, k in ((1, 1), (2, 2), (8, 10), (16, 16)):
+            for T in (1, 17, 300, 5000):
+                assert bn.load().bn_supports(R, T, k, H) == 1
+                for op in ("reduce_norm", "reduce_residual_norm", "reduce_only", "norm_only"):
+                    bn.launch_info(op, R, T, H)
+                for op in ("finalize_reduce_norm", "finalize_reduce_residual_norm",
+                           "finalize_reduce_only", "finalize_only"):
+                    bn.launch_info(op, R, T, H, k)
+                    bn.launch_info(op, R, T, H, k, has_shared=False)
 
 
 SPLIT_CASES = [

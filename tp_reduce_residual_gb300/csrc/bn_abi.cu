@@ -422,19 +422,33 @@ bn_status plan(int mode, Args *a, Launch *l)
         const int want_cs = g_tune_cluster.load();
         for (int c = a->R < kMaxCluster ? a->R : kMaxCluster; c >= 2; --c) {
             if (a->R % c != 0 || (want_cs > 0 && c != want_cs)) continue;
-            BN_TRY(shape_for(mode, a, d, true, c, l, &resident));
+            const bn_status st = shape_for(mode, a, d, true, c, l, &resident);
+            if (st == BN_ERR_UNSUPPORTED) continue;  // this cluster's CTAs do not fit
+            if (st != BN_OK) return st;
             if (resident > 0 && (pref == 2 || T <= resident)) return BN_OK;
         }
     }
 
-    int cs = g_tune_cluster.load();
+    const int want_cs = g_tune_cluster.load();
+    int cs = want_cs;
     if (cs <= 0) cs = auto_cluster(T, nchunks, d->sms, (long long)loads_per_row(mode, *a, false, 1) * 2 * H);
     if (cs > nchunks) cs = 1;
-    for (;; cs /= 2) {
-        BN_TRY(shape_for(mode, a, d, false, cs, l, &resident));
-        if (resident > 0) return BN_OK;
-        if (cs <= 1) return fail(BN_ERR_UNSUPPORTED, "no resident CTA for this shape");
+    // A slice too wide for one CTA's shared memory (gamma slots and two
+    // stages: reduce rows above about 19 K elements at one CTA per row) takes
+    // a larger cluster; a shape with no resident cluster takes a smaller one.
+    for (int tried = 0; tried < 2 * kMaxCluster; ++tried) {
+        const bn_status st = shape_for(mode, a, d, false, cs, l, &resident);
+        if (st == BN_OK && resident > 0) return BN_OK;
+        if (st != BN_OK && st != BN_ERR_UNSUPPORTED) return st;
+        if (st == BN_ERR_UNSUPPORTED) {
+            if (want_cs > 0 || cs * 2 > kMaxCluster || cs * 2 > nchunks) return st;
+            cs *= 2;
+        } else {
+            if (cs <= 1) break;
+            cs /= 2;
+        }
     }
+    return fail(BN_ERR_UNSUPPORTED, "no resident CTA for this shape");
 }
 
 bn_status run(int mode, Args &a, void *stream)
