@@ -251,7 +251,8 @@ bn_status resident_clusters(int mode, const Launch &l, int *out)
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
-// CTAs per token row.  A cluster splits a row only when the rows alone would
+// CTAs per token row for the finalize modes' column split (few finalize rows
+// take the shard split instead).  A cluster splits a row only when the rows alone would
 // leave SMs idle and a row is heavy enough (about 192 KB of copies per CTA)
 // to repay the two cluster-wide exchanges; each CTA keeps at least 32 chunks.
 int auto_cluster(int T, int nchunks, int sms, long long row_bytes)
@@ -262,6 +263,20 @@ int auto_cluster(int T, int nchunks, int sms, long long row_bytes)
     while (by_bytes < kMaxCluster && (long long)by_bytes * 2 * 192 * 1024 <= row_bytes) by_bytes *= 2;
     int cs = by_rows < by_bytes ? by_rows : by_bytes;
     while (cs > 1 && nchunks / cs < 32) cs /= 2;
+    return cs;
+}
+
+// CTAs per token row for the reduce modes: while rows are few, a cluster
+// splits each row so that more SMs work on it, as long as the CTAs of all
+// rows fit about two per SM and each keeps at least 64 chunks.  Measured on
+// GB300 (us per call, clusters of 1 / 2 / 4 / 8): C2 (R=8, H=8192) at T=1
+// 7.76 / 6.57 / 5.69 / 5.46, T=8 7.82 / 6.71 / 5.85 / 5.60, T=64 8.50 / 7.71
+// / 7.92 / 8.07; C1 (R=4, H=5120) at T=1 5.68 / 5.01 / 4.46 / 4.34, T=64
+// 5.90 / 5.35 / 5.17 / 6.19; from T=256 on one CTA per row is fastest.
+int auto_cluster_reduce(int T, int nchunks, int sms)
+{
+    int cs = 1;
+    while (cs < 8 && (long long)T * cs * 2 <= 2LL * sms && nchunks / (cs * 2) >= 64) cs *= 2;
     return cs;
 }
 
@@ -431,7 +446,9 @@ bn_status plan(int mode, Args *a, Launch *l)
 
     const int want_cs = g_tune_cluster.load();
     int cs = want_cs;
-    if (cs <= 0) cs = auto_cluster(T, nchunks, d->sms, (long long)loads_per_row(mode, *a, false, 1) * 2 * H);
+    if (cs <= 0)
+        cs = (mode & F_FIN) ? auto_cluster(T, nchunks, d->sms, (long long)loads_per_row(mode, *a, false, 1) * 2 * H)
+                            : auto_cluster_reduce(T, nchunks, d->sms);
     if (cs > nchunks) cs = 1;
     // A slice too wide for one CTA's shared memory (gamma slots and two
     // stages: reduce rows above about 19 K elements at one CTA per row) takes
