@@ -22,6 +22,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -413,6 +414,21 @@ def sweep(bn, peak, l2_bytes, max_sets=64):
 # ---------------------------------------------------------------------------------------
 # CPU oracle baseline (bounded sample of the same workload)
 
+def host_cpu() -> dict:
+    """The host the oracle runs on: logical CPUs and the CPU's name."""
+    name = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                if key.strip() in ("model name", "Model", "Hardware") and val.strip():
+                    name = val.strip()
+                    break
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "cpu": name, "arch": platform.machine()}
+
+
 def oracle_sample_time(wl, T, target_s, seed_rows=0):
     """Time the oracle on enough sampled token rows of the workload to take
     about target_s seconds; return (GB/s, rows, seconds)."""
@@ -508,7 +524,8 @@ def main(argv=None):
     if not args.no_cpu and rank == 0:
         gbs, n, secs = oracle_sample_time(wl, T, args.cpu_seconds)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n} of {T} token rows of {wl.describe(T)}, {secs:.1f} s single-threaded"}
+               "sample": f"{n} of {T} token rows of {wl.describe(T)}, {secs:.1f} s single-threaded",
+               "host": host_cpu()}
 
     if rank == 0:
         key = f"C{wl.index}:{T}"
@@ -585,7 +602,7 @@ def main_reference(args, rank, world, wl, T, B):
         "config": {"workload": wl.describe(T), "op": wl.op, "R": wl.R, "H": wl.H, "k": wl.k, "T": T,
                    "bytes_per_step": Bn},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{n} token rows of {wl.describe(T)} per step"},
+                         "sample": f"{n} token rows of {wl.describe(T)} per step", "host": host_cpu()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
