@@ -210,7 +210,7 @@ const ModeOps &ops_for(int mode)
 
 // Occupancy answers are cached: (device, mode, shape) -> resident clusters.
 struct OccEntry {
-    int dev, mode, split, cluster, consumers, cpt;
+    int dev, mode, split, full, cluster, consumers, cpt;
     size_t smem;
     int clusters;
 };
@@ -228,7 +228,8 @@ bn_status resident_clusters(int mode, const Launch &l, int *out)
         std::lock_guard<std::mutex> g(g_occ_mu);
         for (int i = 0; i < g_occ_n; ++i) {
             const OccEntry &o = g_occ[i];
-            if (o.dev == dev && o.mode == mode && o.split == l.split && o.cluster == l.cluster &&
+            if (o.dev == dev && o.mode == mode && o.split == l.split && o.full == l.full &&
+                o.cluster == l.cluster &&
                 o.consumers == l.consumers && o.cpt == l.cpt && o.smem == l.smem) {
                 *out = o.clusters;
                 return BN_OK;
@@ -243,7 +244,7 @@ bn_status resident_clusters(int mode, const Launch &l, int *out)
     {
         std::lock_guard<std::mutex> g(g_occ_mu);
         if (g_occ_n < kOccCache)
-            g_occ[g_occ_n++] = OccEntry{dev, mode, l.split, l.cluster, l.consumers, l.cpt, l.smem, n};
+            g_occ[g_occ_n++] = OccEntry{dev, mode, l.split, l.full, l.cluster, l.consumers, l.cpt, l.smem, n};
     }
     *out = n;
     return BN_OK;
@@ -355,6 +356,9 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     L.consumers = consumers;
     L.cpt = cpt;
     L.pdl = 0;
+    // every CTA's slice exactly cpt chunks per consumer thread: the kernel
+    // without per-chunk bounds checks
+    L.full = (!split && nchunks % cs == 0 && nchunks / cs == cpt * consumers) ? 1 : 0;
     // CTAs per SM that registers and threads allow (probe with a 2-stage ring)
     Launch probe = L;
     probe.cluster = 1;

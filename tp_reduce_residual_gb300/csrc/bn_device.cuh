@@ -498,7 +498,10 @@ __device__ __forceinline__ float row_sum_squares(f2 S2, f2 E2, int &nred, const 
 // the CTA whose column slice holds it; each CTA then sums the R z rows of its
 // slice in rank order and runs the epilogue on the slice exactly as in the
 // column split.
-template <int MODE, int CPT, bool SPLITR>
+// FULL: every consumer thread owns exactly CPT chunks of every slice it
+// works on (the host launches it only when slice == CPT * consumers for all
+// CTAs), so the per-chunk bounds checks drop out of the loops.
+template <int MODE, int CPT, bool SPLITR, bool FULL>
 __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 {
     constexpr bool FIN = (MODE & F_FIN) != 0;
@@ -777,7 +780,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
             for (int i = 0; i < CPT; ++i) {
                 const int lc = tid + i * NT;
-                if (lc < nch) {
+                if (FULL || lc < nch) {
                     const float4 *gq = reinterpret_cast<const float4 *>(a.gamma_pre + (size_t)(c0 + lc) * 8);
                     gsm[(kGPre * 2 + 0) * gstride + lc] = __ldg(gq);
                     gsm[(kGPre * 2 + 1) * gstride + lc] = __ldg(gq + 1);
@@ -814,7 +817,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                 for (int i = 0; i < CPT; ++i) {
                     const int lc = tid + i * NT;
-                    if (lc < nch) {
+                    if (FULL || lc < nch) {
                         const uint4 u = *reinterpret_cast<const uint4 *>(p + (size_t)lc * 32);
                         const uint4 v = *reinterpret_cast<const uint4 *>(p + (size_t)lc * 32 + 16);
                         s[i][0] = ((f2)u.y << 32) | u.x;
@@ -918,7 +921,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (lc < nch) {
+                        if (FULL || lc < nch) {
                             widen8(zbuf[lc], s[i]);
                             for (int rr = 1; rr < a.R; ++rr) add_bf16x8(s[i], zbuf[rr * zstride + lc]);
                         }
@@ -939,7 +942,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                         for (int i = 0; i < CPT; ++i) {
                             const int lc = tid + i * NT;
                             f2 x[4] = {0ull, 0ull, 0ull, 0ull};
-                            if (lc < nch) widen8(chunk(p, lc), x);
+                            if (FULL || lc < nch) widen8(chunk(p, lc), x);
 #pragma unroll
                             for (int m = 0; m < 4; ++m) acc[i][m] = mul_sep2(w2, x[m]);
                         }
@@ -955,7 +958,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                         for (int i = 0; i < CPT; ++i) {
                             const int lc = tid + i * NT;
-                            if (lc < nch) {
+                            if (FULL || lc < nch) {
                                 f2 x[4];
                                 widen8(chunk(p, lc), x);
 #pragma unroll
@@ -971,7 +974,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                         for (int i = 0; i < CPT; ++i) {
                             const int lc = tid + i * NT;
-                            if (lc < nch) add_bf16x8(acc[i], chunk(p, lc));
+                            if (FULL || lc < nch) add_bf16x8(acc[i], chunk(p, lc));
                         }
                         release();
                     }
@@ -979,7 +982,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (lc < nch) {
+                        if (FULL || lc < nch) {
                             const uint4 z = round8(acc[i]);
                             if ((Z_OUT || a.z_out != nullptr) && live)
                                 *reinterpret_cast<uint4 *>(a.z_out + ((size_t)r * a.T + t) * H +
@@ -1002,7 +1005,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (lc < nch) widen8(chunk(p, lc), s[i]);
+                        if (FULL || lc < nch) widen8(chunk(p, lc), s[i]);
                     }
                     release();
                 }
@@ -1011,7 +1014,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (lc < nch) add_bf16x8(s[i], chunk(p, lc));
+                        if (FULL || lc < nch) add_bf16x8(s[i], chunk(p, lc));
                     }
                     release();
                 }
@@ -1023,7 +1026,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (lc < nch) {
+                        if (FULL || lc < nch) {
                             f2 *dst = reinterpret_cast<f2 *>(a.sum_out + (size_t)t * H +
                                                              (size_t)(c0 + lc) * 8);
                             reinterpret_cast<ulonglong2 *>(dst)[0] = make_ulonglong2(s[i][0], s[i][1]);
@@ -1041,7 +1044,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (lc < nch) {
+                        if (FULL || lc < nch) {
 #pragma unroll
                             for (int m = 0; m < 4; ++m) acc_square2(S1, E1, s[i][m]);
                         }
@@ -1052,7 +1055,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (lc < nch) {
+                        if (FULL || lc < nch) {
                             f2 g[4];
                             gamma8(kGPost, i, g);
 #pragma unroll
@@ -1067,7 +1070,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (lc < nch) {
+                        if (FULL || lc < nch) {
                             add_bf16x8(s[i], chunk(p, lc));  // h = residual + y
 #pragma unroll
                             for (int m = 0; m < 4; ++m) acc_square2(S2, E2, s[i][m]);
@@ -1084,7 +1087,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                 for (int i = 0; i < CPT; ++i) {
                     const int lc = tid + i * NT;
-                    if (lc < nch) {
+                    if (FULL || lc < nch) {
                         f2 g[4], o[4];
                         gamma8(kGPre, i, g);
 #pragma unroll

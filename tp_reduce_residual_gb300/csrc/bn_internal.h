@@ -73,6 +73,7 @@ struct Launch {
     int grid;        // CTAs (a multiple of cluster)
     size_t smem;     // dynamic shared memory bytes
     int pdl;         // 1: programmatic dependent launch (setup overlaps the previous kernel)
+    int full;        // 1: every slice is exactly cpt * consumers chunks (unchecked kernel)
 };
 
 // Dynamic shared-memory layout, identical on host and device.

@@ -23,14 +23,14 @@ namespace {
 constexpr int kMode = BN_MODE_VALUE;
 constexpr int kMaxDevices = 64;
 
-template <bool SPLIT>
+template <bool SPLIT, bool FULL>
 const void *kernel_by_cpt(int cpt)
 {
     switch (cpt) {
-    case 1: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 1, SPLIT>);
-    case 2: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 2, SPLIT>);
-    case 4: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 4, SPLIT>);
-    case 8: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 8, SPLIT>);
+    case 1: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 1, SPLIT, FULL>);
+    case 2: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 2, SPLIT, FULL>);
+    case 4: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 4, SPLIT, FULL>);
+    case 8: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 8, SPLIT, FULL>);
     default: return nullptr;
     }
 }
@@ -39,30 +39,32 @@ const void *kernel_by_cpt(int cpt)
 // finalize alone; other modes have no such kernel.
 constexpr bool kHasSplit = (kMode & F_FIN) && (kMode & (F_RESNORM | F_Z_OUT));
 
-const void *kernel_for(int cpt, int split)
+// The shard split's epilogue slice is narrower than its finalize row, so it
+// always takes the checked kernel.
+const void *kernel_for(int cpt, int split, int full)
 {
     if (split) {
-        if constexpr (kHasSplit) return kernel_by_cpt<true>(cpt);
+        if constexpr (kHasSplit) return kernel_by_cpt<true, false>(cpt);
         return nullptr;
     }
-    return kernel_by_cpt<false>(cpt);
+    return full ? kernel_by_cpt<false, true>(cpt) : kernel_by_cpt<false, false>(cpt);
 }
 
-int cpt_index(int cpt, int split)
+int cpt_index(int cpt, int split, int full)
 {
-    return (cpt == 1 ? 0 : cpt == 2 ? 1 : cpt == 4 ? 2 : 3) + (split ? 4 : 0);
+    return (cpt == 1 ? 0 : cpt == 2 ? 1 : cpt == 4 ? 2 : 3) + (split ? 4 : 0) + (full ? 8 : 0);
 }
 
 // Function attributes are per device: set them once per (device, cpt).
 std::atomic<unsigned> g_prepared[kMaxDevices];
 
-cudaError_t prepare(const void *fn, int cpt, int split)
+cudaError_t prepare(const void *fn, int cpt, int split, int full)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    const unsigned bit = 1u << cpt_index(cpt, split);
+    const unsigned bit = 1u << cpt_index(cpt, split, full);
     if (g_prepared[dev].load(std::memory_order_acquire) & bit) return cudaSuccess;
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
@@ -108,9 +110,9 @@ void fill_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, const Launc
 
 cudaError_t BN_CAT(launch_, BN_MODE_NAME)(const Args &a, const Launch &l, cudaStream_t st)
 {
-    const void *fn = kernel_for(l.cpt, l.split);
+    const void *fn = kernel_for(l.cpt, l.split, l.full);
     if (!fn) return cudaErrorInvalidValue;
-    cudaError_t e = prepare(fn, l.cpt, l.split);
+    cudaError_t e = prepare(fn, l.cpt, l.split, l.full);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
@@ -121,12 +123,12 @@ cudaError_t BN_CAT(launch_, BN_MODE_NAME)(const Args &a, const Launch &l, cudaSt
 
 int BN_CAT(occupancy_, BN_MODE_NAME)(const Launch &l, cudaError_t *err)
 {
-    const void *fn = kernel_for(l.cpt, l.split);
+    const void *fn = kernel_for(l.cpt, l.split, l.full);
     if (!fn) {
         *err = cudaErrorInvalidValue;
         return 0;
     }
-    cudaError_t e = prepare(fn, l.cpt, l.split);
+    cudaError_t e = prepare(fn, l.cpt, l.split, l.full);
     if (e != cudaSuccess) {
         *err = e;
         return 0;
