@@ -356,9 +356,10 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     L.consumers = consumers;
     L.cpt = cpt;
     L.pdl = 0;
-    // every CTA's slice exactly cpt chunks per consumer thread: the kernel
-    // without per-chunk bounds checks
-    L.full = (!split && nchunks % cs == 0 && nchunks / cs == cpt * consumers) ? 1 : 0;
+    // every CTA's slice (the whole row for a shard split's finalize) exactly
+    // cpt chunks per consumer thread: the kernel without those bounds checks
+    L.full = split ? (nchunks == cpt * consumers ? 1 : 0)
+                   : (nchunks % cs == 0 && nchunks / cs == cpt * consumers ? 1 : 0);
     // CTAs per SM that registers and threads allow (probe with a 2-stage ring)
     Launch probe = L;
     probe.cluster = 1;

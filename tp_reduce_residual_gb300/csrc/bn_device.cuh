@@ -500,7 +500,9 @@ __device__ __forceinline__ float row_sum_squares(f2 S2, f2 E2, int &nred, const 
 // column split.
 // FULL: every consumer thread owns exactly CPT chunks of every slice it
 // works on (the host launches it only when slice == CPT * consumers for all
-// CTAs), so the per-chunk bounds checks drop out of the loops.
+// CTAs), so the per-chunk bounds checks drop out of the loops.  In the shard
+// split it covers the finalize over the whole row (nchunks == CPT *
+// consumers); the epilogue slice there stays checked.
 template <int MODE, int CPT, bool SPLITR, bool FULL>
 __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 {
@@ -780,7 +782,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
             for (int i = 0; i < CPT; ++i) {
                 const int lc = tid + i * NT;
-                if (FULL || lc < nch) {
+                if ((FULL && !SPLITR) || lc < nch) {
                     const float4 *gq = reinterpret_cast<const float4 *>(a.gamma_pre + (size_t)(c0 + lc) * 8);
                     gsm[(kGPre * 2 + 0) * gstride + lc] = __ldg(gq);
                     gsm[(kGPre * 2 + 1) * gstride + lc] = __ldg(gq + 1);
@@ -817,7 +819,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                 for (int i = 0; i < CPT; ++i) {
                     const int lc = tid + i * NT;
-                    if (FULL || lc < nch) {
+                    if ((FULL && !SPLITR) || lc < nch) {
                         const uint4 u = *reinterpret_cast<const uint4 *>(p + (size_t)lc * 32);
                         const uint4 v = *reinterpret_cast<const uint4 *>(p + (size_t)lc * 32 + 16);
                         s[i][0] = ((f2)u.y << 32) | u.x;
@@ -859,7 +861,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                         for (int i = 0; i < CPT; ++i) {
                             const int lc = tid + i * NT;
                             f2 x[4] = {0ull, 0ull, 0ull, 0ull};
-                            if (lc < a.nchunks) widen8(chunk(p, lc), x);
+                            if (FULL || lc < a.nchunks) widen8(chunk(p, lc), x);
 #pragma unroll
                             for (int m = 0; m < 4; ++m) acc[i][m] = mul_sep2(w2, x[m]);
                         }
@@ -874,7 +876,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                         for (int i = 0; i < CPT; ++i) {
                             const int lc = tid + i * NT;
-                            if (lc < a.nchunks) {
+                            if (FULL || lc < a.nchunks) {
                                 f2 x[4];
                                 widen8(chunk(p, lc), x);
 #pragma unroll
@@ -889,7 +891,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                         for (int i = 0; i < CPT; ++i) {
                             const int lc = tid + i * NT;
-                            if (lc < a.nchunks) add_bf16x8(acc[i], chunk(p, lc));
+                            if (FULL || lc < a.nchunks) add_bf16x8(acc[i], chunk(p, lc));
                         }
                         release();
                     }
@@ -897,7 +899,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (lc < a.nchunks) {
+                        if (FULL || lc < a.nchunks) {
                             const uint4 z = round8(acc[i]);
                             if constexpr (REDUCE) {
                                 // owner: the last CTA o whose slice starts at or before lc
@@ -921,7 +923,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (FULL || lc < nch) {
+                        if ((FULL && !SPLITR) || lc < nch) {
                             widen8(zbuf[lc], s[i]);
                             for (int rr = 1; rr < a.R; ++rr) add_bf16x8(s[i], zbuf[rr * zstride + lc]);
                         }
@@ -942,7 +944,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                         for (int i = 0; i < CPT; ++i) {
                             const int lc = tid + i * NT;
                             f2 x[4] = {0ull, 0ull, 0ull, 0ull};
-                            if (FULL || lc < nch) widen8(chunk(p, lc), x);
+                            if ((FULL && !SPLITR) || lc < nch) widen8(chunk(p, lc), x);
 #pragma unroll
                             for (int m = 0; m < 4; ++m) acc[i][m] = mul_sep2(w2, x[m]);
                         }
@@ -958,7 +960,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                         for (int i = 0; i < CPT; ++i) {
                             const int lc = tid + i * NT;
-                            if (FULL || lc < nch) {
+                            if ((FULL && !SPLITR) || lc < nch) {
                                 f2 x[4];
                                 widen8(chunk(p, lc), x);
 #pragma unroll
@@ -974,7 +976,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                         for (int i = 0; i < CPT; ++i) {
                             const int lc = tid + i * NT;
-                            if (FULL || lc < nch) add_bf16x8(acc[i], chunk(p, lc));
+                            if ((FULL && !SPLITR) || lc < nch) add_bf16x8(acc[i], chunk(p, lc));
                         }
                         release();
                     }
@@ -982,7 +984,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (FULL || lc < nch) {
+                        if ((FULL && !SPLITR) || lc < nch) {
                             const uint4 z = round8(acc[i]);
                             if ((Z_OUT || a.z_out != nullptr) && live)
                                 *reinterpret_cast<uint4 *>(a.z_out + ((size_t)r * a.T + t) * H +
@@ -1005,7 +1007,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (FULL || lc < nch) widen8(chunk(p, lc), s[i]);
+                        if ((FULL && !SPLITR) || lc < nch) widen8(chunk(p, lc), s[i]);
                     }
                     release();
                 }
@@ -1014,7 +1016,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (FULL || lc < nch) add_bf16x8(s[i], chunk(p, lc));
+                        if ((FULL && !SPLITR) || lc < nch) add_bf16x8(s[i], chunk(p, lc));
                     }
                     release();
                 }
@@ -1026,7 +1028,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (FULL || lc < nch) {
+                        if ((FULL && !SPLITR) || lc < nch) {
                             f2 *dst = reinterpret_cast<f2 *>(a.sum_out + (size_t)t * H +
                                                              (size_t)(c0 + lc) * 8);
                             reinterpret_cast<ulonglong2 *>(dst)[0] = make_ulonglong2(s[i][0], s[i][1]);
@@ -1044,7 +1046,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (FULL || lc < nch) {
+                        if ((FULL && !SPLITR) || lc < nch) {
 #pragma unroll
                             for (int m = 0; m < 4; ++m) acc_square2(S1, E1, s[i][m]);
                         }
@@ -1055,7 +1057,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (FULL || lc < nch) {
+                        if ((FULL && !SPLITR) || lc < nch) {
                             f2 g[4];
                             gamma8(kGPost, i, g);
 #pragma unroll
@@ -1070,7 +1072,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                     for (int i = 0; i < CPT; ++i) {
                         const int lc = tid + i * NT;
-                        if (FULL || lc < nch) {
+                        if ((FULL && !SPLITR) || lc < nch) {
                             add_bf16x8(s[i], chunk(p, lc));  // h = residual + y
 #pragma unroll
                             for (int m = 0; m < 4; ++m) acc_square2(S2, E2, s[i][m]);
@@ -1087,7 +1089,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 #pragma unroll
                 for (int i = 0; i < CPT; ++i) {
                     const int lc = tid + i * NT;
-                    if (FULL || lc < nch) {
+                    if ((FULL && !SPLITR) || lc < nch) {
                         f2 g[4], o[4];
                         gamma8(kGPre, i, g);
 #pragma unroll

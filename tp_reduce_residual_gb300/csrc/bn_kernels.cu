@@ -39,12 +39,10 @@ const void *kernel_by_cpt(int cpt)
 // finalize alone; other modes have no such kernel.
 constexpr bool kHasSplit = (kMode & F_FIN) && (kMode & (F_RESNORM | F_Z_OUT));
 
-// The shard split's epilogue slice is narrower than its finalize row, so it
-// always takes the checked kernel.
 const void *kernel_for(int cpt, int split, int full)
 {
     if (split) {
-        if constexpr (kHasSplit) return kernel_by_cpt<true, false>(cpt);
+        if constexpr (kHasSplit) return full ? kernel_by_cpt<true, true>(cpt) : kernel_by_cpt<true, false>(cpt);
         return nullptr;
     }
     return full ? kernel_by_cpt<false, true>(cpt) : kernel_by_cpt<false, false>(cpt);
