@@ -231,8 +231,10 @@ __device__ __forceinline__ bool phase_done(uint32_t bar, uint32_t parity, bool s
 template <bool CLUSTER_ACQUIRE, bool HONOR_ABORT>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl &c)
 {
-    if (HONOR_ABORT && *c.abort) return false;
+    // a completed phase returns at once (its data is valid even in a CTA that
+    // is aborting); the abort flag is read only when the wait must poll
     if (phase_done<CLUSTER_ACQUIRE>(bar, parity, c.spin)) return true;
+    if (HONOR_ABORT && *c.abort) return false;
     long long t0 = 0;
     for (uint32_t i = 1; i < kMaxSpins; ++i) {
         if (phase_done<CLUSTER_ACQUIRE>(bar, parity, c.spin)) return true;
