@@ -197,7 +197,8 @@ typedef struct {
     int threads;       /* consumer threads per CTA: a multiple of 32, at most 512 */
     int ctas_per_sm;   /* CTAs sharing one SM, at most 8 (capped by registers) */
     int wait_mode;     /* 1: suspending try_wait, 2: polling test_wait */
-    int group;         /* row copies per pipeline stage, at most 64 */
+    int group;         /* row copies per pipeline stage, at most 64; the finalize
+                          modes only (the other modes carry one copy a stage) */
     int split;         /* finalize rows: 1 split by columns, 2 split by shard */
     int dependent_launch; /* 1: plain stream order, 2: programmatic dependent
                              launch (the launch and the kernel's setup overlap

@@ -327,10 +327,10 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     // one stage holds `group` row copies of item_bytes each.  Measured on
     // GB300: the finalize modes gain from ~48 KB stages (fewer handshakes
     // over their many gathered copies), the reduce modes run best with one
-    // copy per stage.
+    // copy per stage, and their kernels assume it (no item cursor).
     const int item_bytes = round_up(nch_max * 16 * (sum_in ? 2 : 1), 128);
     int group = g_tune_group.load() > 0 ? g_tune_group.load() : (fin ? (48 * 1024) / item_bytes : 1);
-    if (sum_in) group = 1;  // one FP32 row and the residual: nothing to group
+    if (!fin) group = 1;
     if (group > per_row) group = per_row;
     if (group < 1) group = 1;
     const int slice = (nchunks + cs - 1) / cs;  // the largest column slice of the epilogue

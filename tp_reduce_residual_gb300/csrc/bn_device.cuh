@@ -746,11 +746,12 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
         int nred = 0;
         bool live = true;  // false once a wait failed: keep the control flow, store nothing
         // item cursor: a stage is waited for when its first item is taken and
-        // released when its last item is done
+        // released when its last item is done.  The reduce modes carry one
+        // item per stage, so there every take waits and every release frees.
         int cpos = 0, cn = 0, cleft = 0;
         const uint8_t *cbase = sm.stages;
         auto take = [&]() -> const uint8_t * {
-            if (cpos == 0) {
+            if (!FIN || cpos == 0) {
                 cn = items_in_stage(cleft);
                 if (!wait_phase<false, true>(sm.full0 + 8u * stage, phase, ctl)) live = false;
                 cbase = sm.stages + (size_t)stage * (size_t)a.stage_bytes;
@@ -759,7 +760,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
         };
         auto release = [&]() {
             --cleft;
-            if (++cpos == cn) {
+            if (!FIN || ++cpos == cn) {
                 cpos = 0;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sm.empty0 + 8u * stage);
