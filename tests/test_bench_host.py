@@ -61,7 +61,7 @@ def test_row_ranges_partition_the_batch(T, world):
 def test_workload_parsing_and_bytes():
     wl, T = bench.parse_workload("C4:1024")
     assert (wl.R, wl.H, wl.k, T) == (8, 8192, 10, 1024)
-    # the survey's per-call figure for this workload: 1.527 GB
+    # T*H*(2Rk + 2R + 6) + 8RkT + 8H bytes for R=8, H=8192, k=10, T=1024: 1.527 GB
     assert abs(bench.workload_bytes(wl, T) / 1e9 - 1.527) < 0.001
     wl2, T2 = bench.parse_workload("C2:4096")
     assert abs(bench.workload_bytes(wl2, T2) / 1e6 - 738.3) < 0.1

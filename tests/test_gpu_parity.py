@@ -215,6 +215,33 @@ def test_launch_query_is_coherent(op, R, T, k, H):
 
 
 @pytest.mark.gpu
+def test_reduce_planner_balances_rows_per_sm():
+    """One CTA per reduce row: the planner takes 512-thread CTAs when an SM then
+    runs at least as many consumer threads and takes no more rows, with a gain
+    in one (R=8, H=8192 at T=1024 and 4096; R=8, H=16384), keeps the default
+    where both tie (T=256), where the wide CTA runs fewer threads (R=4,
+    H=5120) or would hold one chunk per thread (H=4096), and sizes the ring
+    for the CTAs that actually share an SM when rows are fewer than CTA slots."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms != 152:
+        pytest.skip("expected shapes are those of a 152-SM GB300")
+    for T in (1024, 4096):
+        i = bn.launch_info("reduce_norm", 8, T, 8192)
+        assert (i["threads"], i["chunks_per_thread"], i["cluster_size"]) == (544, 2, 1)
+    i = bn.launch_info("reduce_norm", 8, 256, 8192)
+    assert (i["threads"], i["chunks_per_thread"]) == (288, 4)
+    i = bn.launch_info("reduce_norm", 8, 1024, 16384)
+    assert (i["threads"], i["chunks_per_thread"]) == (544, 4)
+    i = bn.launch_info("reduce_norm", 8, 1024, 4096)
+    assert (i["threads"], i["chunks_per_thread"]) == (288, 2)
+    for T in (1024, 4096):
+        i = bn.launch_info("reduce_norm", 4, T, 5120)
+        assert (i["threads"], i["chunks_per_thread"], i["resident_ctas"]) == (192, 4, 3 * sms)
+    i = bn.launch_info("reduce_norm", 4, 256, 5120)
+    assert i["threads"] == 192 and i["resident_ctas"] == 2 * sms and i["grid"] == 256
+
+
+@pytest.mark.gpu
 def test_every_supported_shape_has_a_launch():
     """bn_supports promises a launch for every valid shape it accepts: the
     planner finds one (widening the row split where one CTA's shared memory

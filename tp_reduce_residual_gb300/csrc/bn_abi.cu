@@ -293,16 +293,18 @@ int loads_per_row(int mode, const Args &a, bool split, int cs)
 
 // Launch shape:
 //   cluster   CTAs per row (automatic: split rows while rows alone leave SMs idle);
-//   consumers up to 256 threads (reduce modes) or 512 (finalize modes) per CTA,
-//             each owning CPT 16-byte chunks of the CTA's slice;
+//   consumers up to `cap` threads per CTA (0: 256 for the reduce modes, 512
+//             for the finalize modes), each owning CPT 16-byte chunks of the
+//             CTA's slice;
 //   CTAs/SM   as many as registers and threads allow (at most 4), so that the
-//             per-row reductions of one CTA overlap another CTA's streaming;
+//             per-row reductions of one CTA overlap another CTA's streaming,
+//             but no more than the rows put on one SM when one CTA takes a row;
 //   stages    the SM's shared memory split over those CTAs, capped at two rows
 //             of copies ahead.
 // One launch shape for a given row split.  Sets *resident to the clusters the
 // device holds at once (0: this shape cannot be resident).
-bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, Launch *l,
-                    int *resident)
+bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, int cap_in,
+                    Launch *l, int *resident)
 {
     const int H = a->H;
     const bool sum_in = (mode & F_SUM_IN) != 0;
@@ -311,7 +313,9 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     const int per_row = loads_per_row(mode, *a, split, cs);
     // measured on GB300: the finalize modes run best with 512 consumer threads
     // (one CTA per SM), the reduce modes with 256 and several CTAs per SM
-    const int cap = g_tune_threads.load() > 0 ? g_tune_threads.load() : (fin ? kMaxConsumers : 256);
+    const int cap = g_tune_threads.load() > 0 ? g_tune_threads.load()
+                    : cap_in > 0               ? cap_in
+                                               : (fin ? kMaxConsumers : 256);
     const int want_stages = g_tune_stages.load();
     const int want_ctas = g_tune_ctas.load();
     *resident = 0;
@@ -370,6 +374,13 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     if (by_regs < 1) by_regs = 1;
     int ctas = want_ctas > 0 ? want_ctas : (by_regs < 4 ? by_regs : 4);
     if (ctas > by_regs) ctas = by_regs;
+    // One CTA per row and fewer rows than CTA slots: the ring is sized for the
+    // CTAs that will share an SM.  Measured on GB300, C1 (R=4, H=5120) at
+    // T=256: 256 CTAs with rings sized for 3 per SM 8.69 us, for 2 per SM 6.94.
+    if (!split && cs == 1 && want_ctas == 0 && want_stages == 0 && d->sms > 0) {
+        const int fill = (a->T + d->sms - 1) / d->sms;
+        if (fill >= 1 && fill < ctas) ctas = fill;
+    }
     // the kernel's own static shared memory is 128 bytes; the occupancy check
     // below drops a stage if the estimate was one too many
     int per_cta = d->smem_per_sm / ctas - d->smem_reserved - 128;
@@ -419,6 +430,51 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     return BN_OK;
 }
 
+// Consumer threads one SM runs for a shape, and the most token rows one SM
+// takes (rows per CTA on the busiest CTA times the CTAs that share an SM).
+void sm_load(const Launch &l, int resident, int T, int sms, long long *threads, long long *rows)
+{
+    const int per_sm = resident / (sms > 0 ? sms : 1);
+    const int grid = l.grid > 0 ? l.grid : 1;
+    int sharing = (grid + sms - 1) / (sms > 0 ? sms : 1);
+    if (sharing > per_sm) sharing = per_sm;
+    if (sharing < 1) sharing = 1;
+    *threads = (long long)l.consumers * sharing;
+    *rows = (long long)((T + grid - 1) / grid) * sharing;
+}
+
+// Reduce rows with one CTA per row: the default shape (up to 256 consumer
+// threads, several CTAs per SM) against one with up to 512 threads per CTA
+// (at least 2 chunks per thread).  The wider shape is taken when an SM runs
+// at least as many consumer threads with it and takes no more rows, and it
+// is better on one of the two.  Measured on GB300 (us per call):
+//   R=8, H=8192 (2 CTAs x 256 threads / 1 CTA x 512 per SM): T=256 12.24 /
+//     12.51 (same threads and rows per SM: kept), T=1024 34.7 / 31.85,
+//     T=4096 113.3 / 108.2;
+//   R=8, H=16384, T=1024 (1 CTA x 256 threads of 8 chunks / 1 x 512 of 4):
+//     93.5 / 67.3;
+//   R=4, H=5120 keeps 3 CTAs x 160 threads against 1 x 320 (T=1024 18.0 /
+//     20.4); R=8, H=4096 keeps 256 threads (512 would take 1 chunk each:
+//     T=1024 19.1 / 24.2).
+bn_status wider_ctas(int mode, Args *a, const DeviceInfo *d, Launch *l, int resident)
+{
+    Args wa = *a;
+    Launch wl{};
+    int wres = 0;
+    const bn_status st = shape_for(mode, &wa, d, false, 1, kMaxConsumers, &wl, &wres);
+    if (st == BN_ERR_UNSUPPORTED || wres <= 0) return BN_OK;
+    if (st != BN_OK) return st;
+    if (wl.cpt < 2 || wl.consumers <= l->consumers) return BN_OK;
+    long long th0, rows0, th1, rows1;
+    sm_load(*l, resident, a->T, d->sms, &th0, &rows0);
+    sm_load(wl, wres, a->T, d->sms, &th1, &rows1);
+    if (th1 >= th0 && rows1 <= rows0 && (th1 > th0 || rows1 < rows0)) {
+        *a = wa;
+        *l = wl;
+    }
+    return BN_OK;
+}
+
 // Launch shape: the row split (by shard for finalize rows when rows are few,
 // else by column slices over a cluster of `cs` CTAs), consumer threads, CTAs
 // per SM and pipeline depth; see shape_for.
@@ -442,7 +498,7 @@ bn_status plan(int mode, Args *a, Launch *l)
         const int want_cs = g_tune_cluster.load();
         for (int c = a->R < kMaxCluster ? a->R : kMaxCluster; c >= 2; --c) {
             if (a->R % c != 0 || (want_cs > 0 && c != want_cs)) continue;
-            const bn_status st = shape_for(mode, a, d, true, c, l, &resident);
+            const bn_status st = shape_for(mode, a, d, true, c, 0, l, &resident);
             if (st == BN_ERR_UNSUPPORTED) continue;  // this cluster's CTAs do not fit
             if (st != BN_OK) return st;
             if (resident > 0 && (pref == 2 || T <= resident)) return BN_OK;
@@ -459,8 +515,12 @@ bn_status plan(int mode, Args *a, Launch *l)
     // stages: reduce rows above about 19 K elements at one CTA per row) takes
     // a larger cluster; a shape with no resident cluster takes a smaller one.
     for (int tried = 0; tried < 2 * kMaxCluster; ++tried) {
-        const bn_status st = shape_for(mode, a, d, false, cs, l, &resident);
-        if (st == BN_OK && resident > 0) return BN_OK;
+        const bn_status st = shape_for(mode, a, d, false, cs, 0, l, &resident);
+        if (st == BN_OK && resident > 0) {
+            if (!(mode & F_FIN) && cs == 1 && g_tune_threads.load() == 0)
+                return wider_ctas(mode, a, d, l, resident);
+            return BN_OK;
+        }
         if (st != BN_OK && st != BN_ERR_UNSUPPORTED) return st;
         if (st == BN_ERR_UNSUPPORTED) {
             if (want_cs > 0 || cs * 2 > kMaxCluster || cs * 2 > nchunks) return st;
