@@ -215,13 +215,14 @@ def workload_bytes(wl, T, split=False, with_shared=True):
     return inputs.algorithmic_bytes(wl.op, wl.R, T, wl.H, wl.k, split=split, with_shared=with_shared)
 
 
-def call_fused(bn, d, res, out, stream=None):
+def call_fused(bn, d, res, out, stream=None, workspace=None):
     if d["op"] == "reduce_norm":
         bn.reduce_norm(d["partials"], res, d["gamma_post"], d["gamma_pre"], d["eps"], out=out,
                        stream=stream)
     else:
         bn.finalize_reduce_norm(d["expert_out"], d["perm"], d["w"], d["shared"], res,
-                                d["gamma_post"], d["gamma_pre"], d["eps"], out=out, stream=stream)
+                                d["gamma_post"], d["gamma_pre"], d["eps"], out=out, stream=stream,
+                                workspace=workspace)
 
 
 def call_split(bn, d, res, out, s):
@@ -392,6 +393,15 @@ def sweep(bn, peak, l2_bytes, max_sets=64):
                    "us_cold": round(cold, 3), "us_hot": round(hot, 3),
                    "gbs_cold": round(B / cold / 1e3, 1), "frac_cold": round(B / cold / 1e3 / peak, 4),
                    "l2_cold": bool(n_sets * B >= 4 * l2_bytes)}
+            if wl.op == "finalize_reduce_norm" and bn.finalize_workspace_bytes(wl.R, T, wl.k, wl.H):
+                # the same calls with a workspace: each token row over many CTAs
+                ws = bn.finalize_workspace(wl.R, T, wl.k, wl.H, device="cuda")
+                ws_fns = [(lambda i=i: call_fused(bn, sets[i % n_sets], sets[i % n_sets]["residual"],
+                                                  outs[i % n_sets], workspace=ws))
+                          for i in range(ncalls)]
+                wu = graph_time_us(ws_fns)
+                row.update(us_ws_cold=round(wu, 3), frac_ws_cold=round(B / wu / 1e3 / peak, 4))
+                del ws
             if wl.index == 4:
                 Bs = workload_bytes(wl, T, split=True)
                 sums = [torch.empty(T, wl.H, device="cuda") for _ in range(n_sets)]

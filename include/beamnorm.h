@@ -64,6 +64,7 @@
 #ifndef BEAMNORM_H
 #define BEAMNORM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -140,6 +141,48 @@ BN_API bn_status bn_finalize_reduce_residual_norm(const uint16_t *expert_out, co
                                            int R, int T, int k, int H,
                                            uint16_t *residual, const float *gamma, float eps,
                                            uint16_t *out, const bn_debug *dbg, void *stream);
+
+/* ---- finalize with a caller-provided workspace (few token rows) --------- */
+
+/* Bytes of workspace with which bn_finalize_reduce_norm_ws and
+ * bn_finalize_reduce_residual_norm_ws spread each token row over many CTAs,
+ * or 0 when that path does not serve the shape (it serves 1 <= T <= 8 and
+ * H <= 8192, where one CTA or one cluster per token row leaves most SMs idle).  Pure host logic: the counters (T words, padded to 256 bytes)
+ * then the per-shard BF16 finalize results [T, R, H]. */
+BN_API size_t bn_finalize_workspace_bytes(int R, int T, int k, int H);
+
+/* bn_finalize_reduce_norm with a workspace.
+ *   workspace        device memory, 16-byte aligned, owned by the caller; it
+ *                    must be zero-filled before its first use, and every
+ *                    call leaves its counters at zero again.  One workspace
+ *                    serves one call at a time: calls that may run
+ *                    concurrently (different streams) need their own.
+ *   workspace_bytes  its size.  With at least bn_finalize_workspace_bytes()
+ *                    bytes (and that size non-zero) the row's finalize is
+ *                    split over many CTAs and its epilogue run by the CTA
+ *                    that finishes the row last; otherwise the workspace is
+ *                    not touched and the call is bn_finalize_reduce_norm.
+ * The results are those of bn_finalize_reduce_norm: the same per-shard BF16
+ * rounding, rank-ordered FP32 sum and norms.  The workspace must not overlap
+ * any other buffer of the call (BN_ERR_INVALID).
+ * Sources: as bn_finalize_reduce_norm. */
+BN_API bn_status bn_finalize_reduce_norm_ws(const uint16_t *expert_out, const int32_t *perm,
+                                     const float *w, const uint16_t *shared,
+                                     int R, int T, int k, int H,
+                                     uint16_t *residual, const float *gamma_post,
+                                     const float *gamma_pre, float eps, uint16_t *out,
+                                     const bn_debug *dbg, void *workspace,
+                                     size_t workspace_bytes, void *stream);
+
+/* bn_finalize_reduce_residual_norm with a workspace, as above.
+ * Source: sglang pull request 34134, description (second fused pattern). */
+BN_API bn_status bn_finalize_reduce_residual_norm_ws(const uint16_t *expert_out,
+                                              const int32_t *perm, const float *w,
+                                              const uint16_t *shared, int R, int T, int k,
+                                              int H, uint16_t *residual, const float *gamma,
+                                              float eps, uint16_t *out, const bn_debug *dbg,
+                                              void *workspace, size_t workspace_bytes,
+                                              void *stream);
 
 /* ---- unfused pieces (the decline / fallback path and its measurement) --- */
 

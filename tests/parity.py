@@ -38,8 +38,9 @@ def _nan_like(shape, dtype):
     return torch.full(shape, float("nan"), dtype=dtype, device="cuda")
 
 
-def run_fused(d, single: bool = False, debug: bool = True, stream=None) -> dict:
-    """One fused call on a copy of the residual; outputs prefilled with NaN."""
+def run_fused(d, single: bool = False, debug: bool = True, stream=None, workspace=None) -> dict:
+    """One fused call on a copy of the residual; outputs prefilled with NaN.
+    ``workspace`` goes to the finalize entries (their many-CTA path)."""
     op, R, T, H, k = d["op"], d["R"], d["T"], d["H"], d["k"]
     fin = op == "finalize_reduce_norm"
     res = d["residual"].clone()
@@ -59,11 +60,11 @@ def run_fused(d, single: bool = False, debug: bool = True, stream=None) -> dict:
         if single:
             bn.finalize_reduce_residual_norm(d["expert_out"], d["perm"], d["w"], d["shared"], res,
                                              d["gamma_pre"], d["eps"], out=out, debug=dbg,
-                                             stream=stream)
+                                             stream=stream, workspace=workspace)
         else:
             bn.finalize_reduce_norm(d["expert_out"], d["perm"], d["w"], d["shared"], res,
                                     d["gamma_post"], d["gamma_pre"], d["eps"], out=out, debug=dbg,
-                                    stream=stream)
+                                    stream=stream, workspace=workspace)
     bits = bn.check_device_error(stream=stream)
     assert bits == 0, bits
     r = {"out": inputs.u16(out), "residual_out": inputs.u16(res)}

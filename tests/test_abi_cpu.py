@@ -123,6 +123,41 @@ def test_finalize_rejects_bad_arguments(L):
     assert call(T=0) == bn.OK
 
 
+def test_finalize_workspace_size(L):
+    # the counters (T words, padded to 256 bytes), then z [T, R, H] BF16
+    assert L.bn_finalize_workspace_bytes(8, 1, 10, 8192) == 256 + 8 * 8192 * 2
+    assert L.bn_finalize_workspace_bytes(8, 8, 10, 8192) == 256 + 8 * 8 * 8192 * 2
+    assert L.bn_finalize_workspace_bytes(2, 9, 3, 64) == 0        # above the served T
+    assert L.bn_finalize_workspace_bytes(3, 7, 5, 6144) == 256 + 7 * 3 * 6144 * 2
+    for R, T, k, H in ((8, 0, 10, 8192), (8, 4, 10, 8200), (0, 4, 1, 64), (17, 4, 1, 64),
+                       (2, 4, 0, 64), (2, 4, 17, 64), (2, 4, 3, 60)):
+        assert L.bn_finalize_workspace_bytes(R, T, k, H) == 0, (R, T, k, H)
+    assert bn.finalize_workspace_bytes(8, 4, 10, 8192) == 256 + 4 * 8 * 8192 * 2
+
+
+def test_finalize_with_workspace_rejects_bad_arguments(L):
+    f = L.bn_finalize_reduce_norm_ws
+    need = L.bn_finalize_workspace_bytes(2, 4, 3, 64)
+    args = dict(x=A16, perm=A16 * 10, w=A16 * 20, sh=A16 * 30, R=2, T=4, k=3, H=64,
+                res=A16 * 40, gp=A16 * 50, gq=A16 * 60, eps=1e-6, out=A16 * 70, ws=A16 * 80,
+                wsb=need)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(a["x"], a["perm"], a["w"], a["sh"], a["R"], a["T"], a["k"], a["H"], a["res"],
+                 a["gp"], a["gq"], a["eps"], a["out"], None, a["ws"], a["wsb"], None)
+
+    assert call(ws=A16 * 80 + 8) == bn.ERR_INVALID          # workspace misaligned
+    assert call(ws=A16 * 10) == bn.ERR_INVALID              # workspace overlaps perm
+    assert call(ws=A16 * 70) == bn.ERR_INVALID              # workspace overlaps out
+    assert call(k=0) == bn.ERR_INVALID
+    assert call(perm=None) == bn.ERR_INVALID
+    assert call(T=0) == bn.OK
+    g = L.bn_finalize_reduce_residual_norm_ws
+    assert g(A16, A16 * 10, A16 * 20, None, 2, 4, 3, 64, A16 * 40, A16 * 50, 1e-6, A16 * 70, None,
+             A16 * 40, need, None) == bn.ERR_INVALID         # workspace overlaps the residual
+
+
 def test_split_and_finalize_only_reject_bad_arguments(L):
     assert L.bn_reduce_only(A16, 2, 4, 64, None, None) == bn.ERR_INVALID
     assert L.bn_reduce_only(A16, 2, 4, 64, A16 + 32, None) == bn.ERR_INVALID   # sum overlaps

@@ -152,6 +152,116 @@ def test_finalize_only_matches_oracle():
     assert_bits_equal(inputs.u16(z), ref["z"], "z")
 
 
+# ---- the finalize with a workspace: token rows spread over many CTAs ----------------
+
+WIDE = [
+    # (R, T, k, H, with_shared)
+    (8, 1, 10, 8192, True),
+    (8, 4, 10, 8192, True),
+    (8, 8, 10, 8192, False),       # the largest T the path serves
+    (8, 5, 8, 6144, True),         # 768 chunks: ragged epilogue slices
+    (2, 7, 3, 1000, True),         # 125 chunks: one CTA per row, ragged warps
+    (16, 3, 16, 4096, True),       # R*k = 256; 16 z rows in two batches
+    (1, 5, 1, 64, False),          # one shard, one slot
+    (3, 8, 5, 8192, True),         # tasks of a CTA span two shards
+    (5, 2, 7, 2048, True),         # 1280 tasks: the third CTA of a row half busy
+]
+
+
+def _counters_zero(ws, T):
+    return int(ws[: ((T * 4 + 255) // 256) * 256].count_nonzero().item()) == 0
+
+
+@pytest.mark.parametrize("R,T,k,H,with_shared", WIDE)
+def test_wide_finalize_matches_oracle(R, T, k, H, with_shared):
+    wl = inputs.custom("finalize_reduce_norm", R, H, k, partial_std=0.3, shared_std=0.3)
+    d = parity.gpu_inputs(wl, T, seed=3000 + R * 13 + T, with_shared=with_shared)
+    ws = bn.finalize_workspace(R, T, k, H, device="cuda")
+    assert ws is not None and ws.numel() == bn.finalize_workspace_bytes(R, T, k, H)
+    g = parity.run_fused(d, workspace=ws)
+    parity.compare(g, parity.run_oracle(d), what=f"wide finalize R={R} T={T} k={k} H={H}")
+    # the per-shard rounding and the rank-ordered sum are those of the
+    # one-CTA-per-row path, bit for bit
+    base = parity.run_fused(d)
+    assert_bits_equal(g["z"], base["z"], "z")
+    assert_bits_equal(g["sum"], base["sum"], "sum")
+    torch.cuda.synchronize()
+    assert _counters_zero(ws, T)
+    # the same workspace serves the next call unchanged
+    g2 = parity.run_fused(d, workspace=ws)
+    for key in ("sum", "ss", "z", "out", "residual_out"):
+        assert_bits_equal(g2[key], g[key], key)
+
+
+def test_wide_single_norm_variant():
+    wl = inputs.custom("finalize_reduce_norm", 8, 6144, 8, partial_std=0.3)
+    d = parity.gpu_inputs(wl, 7, seed=33)
+    ws = bn.finalize_workspace(8, 7, 8, 6144, device="cuda")
+    g = parity.run_fused(d, single=True, workspace=ws)
+    parity.compare(g, parity.run_oracle(d, single=True), what="wide single norm")
+    assert np.all(g["ss"][:, 0] == 0.0)
+
+
+def test_wide_workspace_too_small_or_unserved_takes_the_plain_path():
+    wl = inputs.custom("finalize_reduce_norm", 8, 8192, 10, partial_std=0.3)
+    d = parity.gpu_inputs(wl, 4, seed=34)
+    need = bn.finalize_workspace_bytes(8, 4, 10, 8192)
+    small = torch.full((need - 16,), 7, dtype=torch.uint8, device="cuda")
+    g = parity.run_fused(d, workspace=small)
+    base = parity.run_fused(d)
+    for key in ("sum", "ss", "z", "out", "residual_out"):
+        assert_bits_equal(g[key], base[key], key)
+    assert int((small != 7).sum().item()) == 0          # not touched
+    assert bn.finalize_workspace_bytes(8, 9, 10, 8192) == 0    # above the served T
+    assert bn.finalize_workspace_bytes(8, 4, 10, 16384) == 0   # above the served H
+
+
+def test_wide_perm_out_of_range_sets_the_device_flag():
+    wl = inputs.custom("finalize_reduce_norm", 2, 256, 4, partial_std=0.3)
+    d = parity.gpu_inputs(wl, 6, seed=9)
+    bad = d["perm"].clone()
+    bad[1, 2, 3] = 6 * 4 + 5
+    bad[0, 0, 0] = -1
+    ws = bn.finalize_workspace(2, 6, 4, 256, device="cuda")
+    res = d["residual"].clone()
+    bn.finalize_reduce_norm(d["expert_out"], bad, d["w"], d["shared"], res, d["gamma_post"],
+                            d["gamma_pre"], d["eps"], workspace=ws)
+    assert bn.check_device_error(raise_on_error=False) == bn.DEVERR_PERM_RANGE
+    assert _counters_zero(ws, 6)
+    g = parity.run_fused(d, workspace=ws)
+    parity.compare(g, parity.run_oracle(d), what="wide, after the flagged call")
+
+
+def test_wide_path_in_a_graph_on_a_side_stream():
+    wl = inputs.WORKLOADS[4]
+    d = parity.gpu_inputs(wl, 4)
+    ws = bn.finalize_workspace(8, 4, 10, 8192, device="cuda")
+    res = d["residual"].clone()
+    out = torch.empty_like(res)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            for _ in range(3):  # three dependent calls on one workspace
+                bn.finalize_reduce_norm(d["expert_out"], d["perm"], d["w"], d["shared"], res,
+                                        d["gamma_post"], d["gamma_pre"], d["eps"], out=out,
+                                        workspace=ws)
+    res.copy_(d["residual"])
+    graph.replay()
+    torch.cuda.synchronize()
+    # three calls chained through the residual: the same as three plain calls
+    res2 = d["residual"].clone()
+    out2 = torch.empty_like(res2)
+    for _ in range(3):
+        bn.finalize_reduce_norm(d["expert_out"], d["perm"], d["w"], d["shared"], res2,
+                                d["gamma_post"], d["gamma_pre"], d["eps"], out=out2)
+    torch.cuda.synchronize()
+    assert_bits_equal(inputs.u16(res), inputs.u16(res2), "residual after 3 calls")
+    assert_bits_equal(inputs.u16(out), inputs.u16(out2), "out after 3 calls")
+    assert _counters_zero(ws, 4)
+
+
 def test_decline_then_fallback_gives_the_same_bits():
     """When the fused op declines, a caller that materialises the finalize and
     then reduces and normalises gets exactly the fused result: nothing owed is

@@ -32,6 +32,8 @@ EXPORTS = (
     "bn_finalize_reduce_residual_norm", "bn_reduce_only", "bn_finalize_reduce_only",
     "bn_norm_only", "bn_finalize_only", "bn_supports", "bn_check_device_error",
     "bn_last_error", "bn_status_string", "bn_version", "bn_set_tuning", "bn_query_launch",
+    "bn_finalize_workspace_bytes", "bn_finalize_reduce_norm_ws",
+    "bn_finalize_reduce_residual_norm_ws",
 )
 
 # bn_op values of the entry points, for launch_info()
@@ -110,11 +112,17 @@ def load() -> ctypes.CDLL:
             "bn_version": [],
             "bn_set_tuning": [ctypes.POINTER(_Tuning)],
             "bn_query_launch": [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_LaunchInfo)],
+            "bn_finalize_workspace_bytes": [_I, _I, _I, _I],
+            "bn_finalize_reduce_norm_ws": [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _F, _P,
+                                           dbgp, _P, ctypes.c_size_t, _P],
+            "bn_finalize_reduce_residual_norm_ws": [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _F,
+                                                    _P, dbgp, _P, ctypes.c_size_t, _P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
             fn.argtypes = args
             fn.restype = _I
+        L.bn_finalize_workspace_bytes.restype = ctypes.c_size_t
         L.bn_last_error.restype = ctypes.c_char_p
         L.bn_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -188,10 +196,39 @@ def reduce_norm(partials, residual, gamma_post, gamma_pre, eps: float, out=None,
     return out
 
 
+def finalize_workspace_bytes(R: int, T: int, k: int, H: int) -> int:
+    """Workspace bytes with which the finalize entries spread each token row
+    over many CTAs (0: that path does not serve the shape)."""
+    return int(load().bn_finalize_workspace_bytes(R, T, k, H))
+
+
+def finalize_workspace(R: int, T: int, k: int, H: int, device=None) -> Optional[torch.Tensor]:
+    """A zero-filled workspace for ``finalize_reduce_norm(..., workspace=)``
+    (uint8, on ``device``), or None when the shape does not use one.  Calls
+    leave it zeroed; one workspace serves one call at a time."""
+    n = finalize_workspace_bytes(R, T, k, H)
+    if n == 0:
+        return None
+    return torch.zeros(n, dtype=torch.uint8, device=device if device is not None else "cuda")
+
+
+def _workspace(ws, dev):
+    if ws is None:
+        return None, 0
+    if not isinstance(ws, torch.Tensor) or ws.dtype != torch.uint8 or ws.dim() != 1:
+        raise TypeError("workspace must be a 1-D torch.uint8 tensor")
+    if ws.device != dev or not ws.is_contiguous():
+        raise ValueError(f"workspace must be contiguous on {dev}")
+    return ws.data_ptr(), ws.numel()
+
+
 def finalize_reduce_norm(expert_out, perm, w, shared, residual, gamma_post, gamma_pre, eps: float,
-                         out=None, debug: Optional[Debug] = None, stream=None) -> torch.Tensor:
+                         out=None, debug: Optional[Debug] = None, stream=None,
+                         workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Per-shard MoE top-k finalize (rounded to BF16), rank-ordered FP32 sum,
-    post-RMSNorm, residual add (in place), pre-RMSNorm.  Returns ``out``."""
+    post-RMSNorm, residual add (in place), pre-RMSNorm.  Returns ``out``.
+    With a ``workspace`` (see ``finalize_workspace``) few token rows are each
+    spread over many CTAs; the results are the same."""
     L = load()
     R, T, k = perm.shape
     H = expert_out.shape[-1]
@@ -208,7 +245,13 @@ def finalize_reduce_norm(expert_out, perm, w, shared, residual, gamma_post, gamm
             _need(out, "out", torch.bfloat16, (T, H), dev))
     d = _debug(debug, R, T, H, dev, True)
     with _with_device(expert_out):
-        _check(L.bn_finalize_reduce_norm(*args, d[0] if d else None, _stream(expert_out, stream)))
+        if workspace is None:
+            _check(L.bn_finalize_reduce_norm(*args, d[0] if d else None,
+                                             _stream(expert_out, stream)))
+        else:
+            wp, wn = _workspace(workspace, dev)
+            _check(L.bn_finalize_reduce_norm_ws(*args, d[0] if d else None, wp, wn,
+                                                _stream(expert_out, stream)))
     return out
 
 
@@ -232,8 +275,10 @@ def reduce_residual_norm(partials, residual, gamma, eps: float, out=None,
 
 def finalize_reduce_residual_norm(expert_out, perm, w, shared, residual, gamma, eps: float,
                                   out=None, debug: Optional[Debug] = None,
-                                  stream=None) -> torch.Tensor:
-    """Per-shard finalize, rank-ordered sum, residual add (in place), RMSNorm."""
+                                  stream=None, workspace: Optional[torch.Tensor] = None
+                                  ) -> torch.Tensor:
+    """Per-shard finalize, rank-ordered sum, residual add (in place), RMSNorm.
+    ``workspace`` as for ``finalize_reduce_norm``."""
     L = load()
     R, T, k = perm.shape
     H = expert_out.shape[-1]
@@ -249,8 +294,13 @@ def finalize_reduce_residual_norm(expert_out, perm, w, shared, residual, gamma, 
             _need(out, "out", torch.bfloat16, (T, H), dev))
     d = _debug(debug, R, T, H, dev, True)
     with _with_device(expert_out):
-        _check(L.bn_finalize_reduce_residual_norm(*args, d[0] if d else None,
-                                                  _stream(expert_out, stream)))
+        if workspace is None:
+            _check(L.bn_finalize_reduce_residual_norm(*args, d[0] if d else None,
+                                                      _stream(expert_out, stream)))
+        else:
+            wp, wn = _workspace(workspace, dev)
+            _check(L.bn_finalize_reduce_residual_norm_ws(*args, d[0] if d else None, wp, wn,
+                                                         _stream(expert_out, stream)))
     return out
 
 

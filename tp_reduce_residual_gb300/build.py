@@ -1,10 +1,10 @@
 """Build libbeamnorm.so in-tree for sm_103a (GB300).
 
 Eight objects, one per kernel mode, are compiled from one template source in
-parallel, plus the C-ABI object; everything is compiled with ``-fmad=false``
-so that the FP32 epilogue is never contracted into FMAs ("Fuse Beam's TP
-all-reduce with its sandwich norms", "Details", "Build" bullet).  nvcc
-cross-compiles without a GPU.  The result is
+parallel, plus the small-T finalize object and the C-ABI object; everything
+is compiled with ``-fmad=false`` so that the FP32 epilogue is never
+contracted into FMAs ("Fuse Beam's TP all-reduce with its sandwich norms",
+"Details", "Build" bullet).  nvcc cross-compiles without a GPU.  The result is
 ``tp_reduce_residual_gb300/_build/libbeamnorm.so`` (git-ignored); a stamp of
 the sources and flags skips rebuilding when nothing changed.
 
@@ -45,7 +45,8 @@ MODES = {
     "fin_only": 1 | 32,
 }
 
-SOURCES = ["bn_device.cuh", "bn_internal.h", "bn_kernels.cu", "bn_abi.cu"]
+SOURCES = ["bn_device.cuh", "bn_internal.h", "bn_kernels.cu", "bn_abi.cu", "bn_wide.h",
+           "bn_wide.cu"]
 
 
 def nvcc() -> str:
@@ -93,6 +94,9 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int = 0) -> st
                      "-o", obj])
     abi_obj = os.path.join(OUT_DIR, "bn_abi.o")
     cmds.append([cc, *ARCH, *NVCC_FLAGS, *inc, "-c", os.path.join(CSRC, "bn_abi.cu"), "-o", abi_obj])
+    wide_obj = os.path.join(OUT_DIR, "bn_wide.o")
+    cmds.append([cc, *ARCH, *NVCC_FLAGS, *extra, *inc, "-c", os.path.join(CSRC, "bn_wide.cu"),
+                 "-o", wide_obj])
     jobs = jobs or min(len(cmds), max(1, os.cpu_count() or 1))
     logs = []
     with cf.ThreadPoolExecutor(max_workers=jobs) as ex:

@@ -19,6 +19,7 @@
 
 #include "../../include/beamnorm.h"
 #include "bn_internal.h"
+#include "bn_wide.h"
 
 // The device error word: one per device that loads the library.  Kernels
 // receive its address; they set bits with atomicOr and never trap.
@@ -621,6 +622,78 @@ bn_status check_epilogue(uint16_t *residual, const float *gp, const float *gq, u
     return BN_OK;
 }
 
+// ---- the finalize with a workspace: token rows spread over many CTAs --------------
+
+// Token rows up to which the many-CTA finalize serves.  Measured on GB300
+// (us per call in a CUDA graph, L2-cold; one CTA or cluster per row / many
+// CTAs per row): C4 (R=8, H=8192, k=10) T=1 10.2 / 8.65, T=2 10.3 / 8.8, T=4
+// 10.6 / 9.4, T=8 11.1 / 10.1, T=16 14.4 / 14.7, T=64 24.7 / 39.0 (an earlier
+// version); C3 (R=8, H=6144, k=8) T=1 9.15 / 7.85, T=4 9.3 / 7.8, T=8 9.9 /
+// 8.75, T=16 12.2 / 12.1.  From T=16 on the rows themselves fill the SMs.
+constexpr int kWideMaxT = 8;
+
+bool wide_serves(int R, int T, int k, int H)
+{
+    return R >= 1 && R <= kMaxR && k >= 1 && k <= kMaxK && T >= 1 && T <= kWideMaxT && H > 0 &&
+           H % 8 == 0 && H / 8 <= kWideThreads * kWideMaxCpt;
+}
+
+bn_status run_wide(Args &a, bool postnorm, void *workspace, void *stream)
+{
+    const DeviceInfo *d = nullptr;
+    BN_TRY(device_info(&d));
+    a.nchunks = a.H / 8;
+    a.err = d->err;
+    WideArgs w;
+    w.a = a;
+    w.count = static_cast<unsigned *>(workspace);
+    w.zws = reinterpret_cast<uint16_t *>(static_cast<char *>(workspace) + wide_counter_bytes(a.T));
+    w.parts = (a.R * a.nchunks + kWideThreads - 1) / kWideThreads;
+    const int cpt = a.nchunks <= kWideThreads ? 1 : 2;
+    const cudaError_t e = launch_wide(w, postnorm, cpt, g_tune_pdl.load() != 1,
+                                      reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "bn_wide_kernel");
+    return BN_OK;
+}
+
+// The two finalize entry points that take a workspace: the validation of the
+// plain ones, plus the workspace (16-byte aligned, overlapping no other
+// buffer) when it is large enough to be used.
+bn_status fin_ws(bool postnorm, const uint16_t *expert_out, const int32_t *perm, const float *w,
+                 const uint16_t *shared, int R, int T, int k, int H, uint16_t *residual,
+                 const float *gamma_post, const float *gamma_pre, float eps, uint16_t *out,
+                 const bn_debug *dbg, void *workspace, size_t workspace_bytes, void *stream)
+{
+    BN_TRY(check_shape(R, T, k, H, true));
+    if (T == 0) return BN_OK;  // nothing is read or written; pointers are not examined
+    Range reads[8], writes[8];
+    int nr = 0, nw = 0;
+    BN_TRY(check_fin_sources(expert_out, perm, w, shared, R, T, k, H, reads, &nr));
+    BN_TRY(check_epilogue(residual, gamma_post, gamma_pre, out, eps, T, H, reads, &nr, writes, &nw));
+    BN_TRY(check_debug(dbg, true));
+    debug_ranges(dbg, R, T, H, true, writes, &nw);
+    const size_t need = wide_serves(R, T, k, H) ? wide_workspace_bytes(R, T, H) : 0;
+    const bool wide = need > 0 && workspace != nullptr && workspace_bytes >= need;
+    if (wide) {
+        BN_TRY(check_ptr16(workspace, "workspace"));
+        writes[nw++] = Range{workspace, need, "workspace"};
+    }
+    BN_TRY(check_overlaps(writes, nw, reads, nr));
+    BN_TRY(check_served(R, T, k, H, true));
+    Args a = base_args(R, T, k, H, eps);
+    a.src = expert_out;
+    a.perm = perm;
+    a.w = w;
+    a.shared = shared;
+    a.residual = residual;
+    a.gamma_post = gamma_post;
+    a.gamma_pre = gamma_pre;
+    a.out = out;
+    apply_debug(a, dbg);
+    if (wide) return run_wide(a, postnorm, workspace, stream);
+    return run(postnorm ? kModeFinReduceNorm : kModeFinReduceResNorm, a, stream);
+}
+
 }  // namespace
 }  // namespace bn
 
@@ -738,6 +811,35 @@ bn_status bn_finalize_reduce_residual_norm(const uint16_t *expert_out, const int
     a.out = out;
     apply_debug(a, dbg);
     return run(kModeFinReduceResNorm, a, stream);
+}
+
+size_t bn_finalize_workspace_bytes(int R, int T, int k, int H)
+{
+    return wide_serves(R, T, k, H) ? wide_workspace_bytes(R, T, H) : 0;
+}
+
+bn_status bn_finalize_reduce_norm_ws(const uint16_t *expert_out, const int32_t *perm,
+                                     const float *w, const uint16_t *shared, int R, int T, int k,
+                                     int H, uint16_t *residual, const float *gamma_post,
+                                     const float *gamma_pre, float eps, uint16_t *out,
+                                     const bn_debug *dbg, void *workspace, size_t workspace_bytes,
+                                     void *stream)
+{
+    g_msg[0] = '\0';
+    return fin_ws(true, expert_out, perm, w, shared, R, T, k, H, residual, gamma_post, gamma_pre,
+                  eps, out, dbg, workspace, workspace_bytes, stream);
+}
+
+bn_status bn_finalize_reduce_residual_norm_ws(const uint16_t *expert_out, const int32_t *perm,
+                                              const float *w, const uint16_t *shared, int R, int T,
+                                              int k, int H, uint16_t *residual, const float *gamma,
+                                              float eps, uint16_t *out, const bn_debug *dbg,
+                                              void *workspace, size_t workspace_bytes,
+                                              void *stream)
+{
+    g_msg[0] = '\0';
+    return fin_ws(false, expert_out, perm, w, shared, R, T, k, H, residual, gamma, gamma, eps, out,
+                  dbg, workspace, workspace_bytes, stream);
 }
 
 bn_status bn_reduce_only(const uint16_t *partials, int R, int T, int H, float *sum_out, void *stream)
