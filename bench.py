@@ -241,18 +241,23 @@ def clone_set(d):
 # ---------------------------------------------------------------------------------------
 # the timed headline (our arm)
 
-def time_headline(bn, wl, T, steps, warmup, dev_index):
+def time_headline(bn, wl, T, steps, warmup, dev_index, use_workspace=False):
     """Back-to-back calls on a created stream: programmatic dependent launch
     (the next call's launch and setup overlapping the previous kernel) takes
-    effect on created streams and in graphs, not on the legacy default stream."""
+    effect on created streams and in graphs, not on the legacy default stream.
+    use_workspace: the finalize calls take a workspace (rows over many CTAs
+    where the shape is served)."""
     d = inputs.make_inputs(wl, T, device="cuda")
     res = d["residual"].clone()
     out = torch.empty_like(res)
+    ws = None
+    if use_workspace and wl.op == "finalize_reduce_norm":
+        ws = bn.finalize_workspace(wl.R, T, wl.k, wl.H, device="cuda")
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
         for _ in range(warmup):
-            call_fused(bn, d, res, out)
+            call_fused(bn, d, res, out, workspace=ws)
     torch.cuda.synchronize()
     if bn.check_device_error() != 0:
         raise RuntimeError("device error during warm-up")
@@ -266,7 +271,7 @@ def time_headline(bn, wl, T, steps, warmup, dev_index):
     with torch.cuda.stream(stream):
         start.record(stream)
         for _ in range(steps):
-            call_fused(bn, d, res, out)
+            call_fused(bn, d, res, out, workspace=ws)
         end.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -276,12 +281,12 @@ def time_headline(bn, wl, T, steps, warmup, dev_index):
     while time.time() < t_extra:
         with torch.cuda.stream(stream):
             for _ in range(20):
-                call_fused(bn, d, res, out)
+                call_fused(bn, d, res, out, workspace=ws)
         torch.cuda.synchronize()
     clocks = sampler.stop()
     if bn.check_device_error() != 0:
         raise RuntimeError("device error in the timed region")
-    del d, res, out
+    del d, res, out, ws
     torch.cuda.empty_cache()
     return elapsed_ms, clocks
 
@@ -481,6 +486,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="C4:1024")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--workspace", action="store_true",
+                    help="finalize calls of the timed loop take a workspace (T <= 8)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -512,7 +519,10 @@ def main(argv=None):
     l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_FALLBACK
     log(f"rank {rank}/{world} on {props.name}: {wl.describe(T)}, {B / 1e9:.3f} GB per call")
 
-    elapsed_ms, clocks = time_headline(bn, wl, T, args.steps, args.warmup, dev_index)
+    elapsed_ms, clocks = time_headline(bn, wl, T, args.steps, args.warmup, dev_index,
+                                       use_workspace=args.workspace)
+    with_ws = bool(args.workspace and wl.op == "finalize_reduce_norm"
+                   and bn.finalize_workspace_bytes(wl.R, T, wl.k, wl.H))
     elapsed_ms = max_over_ranks(elapsed_ms, device="cuda")
     ms_per_step = elapsed_ms / args.steps
     achieved = B / (ms_per_step * 1e-3) / 1e9
@@ -547,10 +557,12 @@ def main(argv=None):
             "io_dtype": "bf16", "data": "synthetic",
             "config": {"workload": wl.describe(T), "op": wl.op, "R": wl.R, "H": wl.H, "k": wl.k,
                        "T": T, "bytes_per_step": B, "parallelism": f"replicas x{world}",
+                       "workspace": with_ws,
                        "l2": f"inputs {B / 1e9:.2f} GB per step > L2 {l2 / 1e6:.0f} MB; no flush"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "peak_kind": peak_kind, "traffic": recorded_traffic(key)},
+                         "peak_kind": peak_kind,
+                         "traffic": None if with_ws else recorded_traffic(key)},
             "clocks": clocks,
             "gpu_launches": args.steps,
             "e2e": e2e,

@@ -626,10 +626,10 @@ bn_status check_epilogue(uint16_t *residual, const float *gp, const float *gq, u
 
 // Token rows up to which the many-CTA finalize serves.  Measured on GB300
 // (us per call in a CUDA graph, L2-cold; one CTA or cluster per row / many
-// CTAs per row): C4 (R=8, H=8192, k=10) T=1 10.2 / 8.65, T=2 10.3 / 8.8, T=4
-// 10.6 / 9.4, T=8 11.1 / 10.1, T=16 14.4 / 14.7, T=64 24.7 / 39.0 (an earlier
-// version); C3 (R=8, H=6144, k=8) T=1 9.15 / 7.85, T=4 9.3 / 7.8, T=8 9.9 /
-// 8.75, T=16 12.2 / 12.1.  From T=16 on the rows themselves fill the SMs.
+// CTAs per row): C4 (R=8, H=8192, k=10) T=1 10.2 / 8.33, T=4 10.6 / 9.3, T=8
+// 11.1 / 10.0, T=16 14.4 / 14.7, T=64 24.7 / 39.0 (an earlier version); C3
+// (R=8, H=6144, k=8) T=1 9.1 / 7.6, T=4 9.2 / 7.5, T=8 9.9 / 8.5, T=16 12.2 /
+// 12.1.  From T=16 on the rows themselves fill the SMs.
 constexpr int kWideMaxT = 8;
 
 bool wide_serves(int R, int T, int k, int H)

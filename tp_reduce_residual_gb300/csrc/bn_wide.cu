@@ -14,10 +14,10 @@
 // The sums of squares are the same compensated pairs, rounded once, so they
 // are the FP32 rounding of the exact sums here too.
 //
-// Memory ordering: every thread fences its z stores at device scope before
-// its CTA counts itself done (one atomicInc per CTA on the row's counter);
-// the CTA that takes the count to its end fences again and reads the z rows
-// through L2 (ld.global.cg).  atomicInc wraps the counter back to zero, so a
+// Memory ordering: a CTA barrier, then one device-scope fence by thread 0
+// before its atomicInc on the row's counter (the fence is cumulative over the
+// stores the barrier ordered before it); the CTA that takes the count to its
+// end fences after the count and reads the z rows through L2 (ld.global.cg).  atomicInc wraps the counter back to zero, so a
 // workspace whose counters start at zero is left at zero by every call.
 #include "bn_wide.h"
 
@@ -143,10 +143,15 @@ __global__ void __launch_bounds__(kWideThreads, 1) bn_wide_kernel(const WideArgs
     }
 
     // ---- count this CTA done on its row; the last one runs the epilogue ----
-    __threadfence();
+    // The barrier orders every thread's z stores before thread 0's fence,
+    // which makes them visible device-wide before the count (the fence is
+    // cumulative over what the barrier ordered); the counting CTA's fence
+    // after the count orders its later loads after the other CTAs' stores.
     __syncthreads();
     if (tid == 0) {
+        __threadfence();
         const unsigned old = atomicInc(w.count + t, (unsigned)(w.parts - 1));
+        __threadfence();
         s_last = old == (unsigned)(w.parts - 1) ? 1 : 0;
     }
     __syncthreads();
@@ -154,7 +159,6 @@ __global__ void __launch_bounds__(kWideThreads, 1) bn_wide_kernel(const WideArgs
         griddep_launch_dependents();
         return;
     }
-    __threadfence();
 
     // Each thread stages the gammas of its own chunks in shared memory (it
     // alone reads them back), then loads the residual and the z rows: the
