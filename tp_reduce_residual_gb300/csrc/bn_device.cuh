@@ -1,4 +1,5 @@
-// bn_device.cuh -- the one kernel template of libbeamnorm (sm_103a).
+// bn_device.cuh -- the main kernel template of libbeamnorm (sm_103a) and the
+// arithmetic helpers it shares with the small-T finalize (bn_wide.cu).
 //
 // Operation: the arithmetic epilogue of a fused tensor-parallel all-reduce
 // ("Fuse Beam's TP all-reduce with its sandwich norms", vLLM pull request

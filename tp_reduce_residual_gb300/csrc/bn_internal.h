@@ -9,7 +9,7 @@
 
 namespace bn {
 
-// Mode bits of the one kernel template.  Each served entry point is one mode.
+// Mode bits of the main kernel template.  Each served entry point is one mode.
 enum : int {
     F_FIN = 1,        // sources are gathered expert rows, finalized per shard
     F_SUM_IN = 2,     // the source is one FP32 reduced-sum row (epilogue only)
