@@ -626,10 +626,10 @@ bn_status check_epilogue(uint16_t *residual, const float *gp, const float *gq, u
 
 // Token rows up to which the many-CTA finalize serves.  Measured on GB300
 // (us per call in a CUDA graph, L2-cold; one CTA or cluster per row / many
-// CTAs per row): C4 (R=8, H=8192, k=10) T=1 10.2 / 8.33, T=4 10.6 / 9.3, T=8
-// 11.1 / 10.0, T=16 14.4 / 14.7, T=64 24.7 / 39.0 (an earlier version); C3
-// (R=8, H=6144, k=8) T=1 9.1 / 7.6, T=4 9.2 / 7.5, T=8 9.9 / 8.5, T=16 12.2 /
-// 12.1.  From T=16 on the rows themselves fill the SMs.
+// CTAs per row): C4 (R=8, H=8192, k=10) T=1 10.1 / 7.78, T=4 10.5 / 9.0, T=8
+// 11.1 / 10.0, T=16 14.4 / 14.7, T=64 24.7 / 39.0 (earlier versions); C3
+// (R=8, H=6144, k=8) T=1 9.1 / 7.13, T=4 9.2 / 7.2, T=8 9.9 / 8.5, T=16 12.2
+// / 12.1.  From T=16 on the rows themselves fill the SMs.
 constexpr int kWideMaxT = 8;
 
 bool wide_serves(int R, int T, int k, int H)
@@ -648,7 +648,19 @@ bn_status run_wide(Args &a, bool postnorm, void *workspace, void *stream)
     w.a = a;
     w.count = static_cast<unsigned *>(workspace);
     w.zws = reinterpret_cast<uint16_t *>(static_cast<char *>(workspace) + wide_counter_bytes(a.T));
-    w.parts = (a.R * a.nchunks + kWideThreads - 1) / kWideThreads;
+    // The fewest finalize tasks per CTA (a quarter, half or all of its
+    // threads) with which all CTAs still fit in one wave: each SM then pulls
+    // fewer gathered chunks at once.
+    const int tasks_total = a.R * a.nchunks;
+    w.tasks = kWideThreads;
+    for (int tasks = kWideThreads / 4; tasks < kWideThreads; tasks *= 2) {
+        const long long ctas = (long long)a.T * ((tasks_total + tasks - 1) / tasks);
+        if (d->sms > 0 && ctas <= d->sms) {
+            w.tasks = tasks;
+            break;
+        }
+    }
+    w.parts = (tasks_total + w.tasks - 1) / w.tasks;
     const int cpt = a.nchunks <= kWideThreads ? 1 : 2;
     const cudaError_t e = launch_wide(w, postnorm, cpt, g_tune_pdl.load() != 1,
                                       reinterpret_cast<cudaStream_t>(stream));

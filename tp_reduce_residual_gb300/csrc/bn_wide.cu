@@ -69,9 +69,9 @@ __device__ __forceinline__ void gamma8_smem(const float4 *g, int lc, f2 *out)
     out[3] = f2_make(y.z, y.w);
 }
 
-// Grid: T * parts CTAs; CTA b works on token row b / parts.  Its threads take
-// the tasks q = (b % parts) * kWideThreads + tid < R * nchunks of that row,
-// task q being chunk q % nchunks of shard q / nchunks.
+// Grid: T * parts CTAs; CTA b works on token row b / parts.  Its first
+// w.tasks threads take the tasks q = (b % parts) * w.tasks + tid < R * nchunks
+// of that row, task q being chunk q % nchunks of shard q / nchunks.
 template <bool POSTNORM, int CPT>
 __global__ void __launch_bounds__(kWideThreads, 1) bn_wide_kernel(const WideArgs w)
 {
@@ -92,8 +92,8 @@ __global__ void __launch_bounds__(kWideThreads, 1) bn_wide_kernel(const WideArgs
     griddep_wait();
 
     // ---- this CTA's share of the row's finalize ----
-    const int q = part * kWideThreads + tid;
-    if (q < a.R * nch) {
+    const int q = part * w.tasks + tid;
+    if (tid < w.tasks && q < a.R * nch) {
         const int r = q / nch;
         const int c = q - r * nch;
         const size_t meta = ((size_t)r * a.T + t) * (size_t)a.k;
@@ -322,7 +322,8 @@ cudaError_t prepare_wide(const void *fn, int bit)
 cudaError_t launch_wide(const WideArgs &w, bool postnorm, int cpt, bool pdl, cudaStream_t st)
 {
     const void *fn = postnorm ? dev::wide_kernel<true>(cpt) : dev::wide_kernel<false>(cpt);
-    if (!fn || w.parts < 1 || w.a.T < 1 || w.a.H > kWideThreads * kWideMaxCpt * 8)
+    if (!fn || w.parts < 1 || w.a.T < 1 || w.a.H > kWideThreads * kWideMaxCpt * 8 ||
+        w.tasks < 1 || w.tasks > kWideThreads)
         return cudaErrorInvalidValue;
     const cudaError_t e = dev::prepare_wide(fn, (postnorm ? 2 : 0) + (cpt == 2 ? 1 : 0));
     if (e != cudaSuccess) return e;

@@ -3,7 +3,7 @@
 //
 // Few token rows leave most SMs idle when one CTA or one cluster owns a row:
 // a C4 row (R=8, k=10, H=8192) is 1.4 MB of gathered copies, and 8 to 16 SMs
-// pull it at a few tens of GB/s each.  Here every CTA of a row takes
+// pull it at a few tens of GB/s each.  Here every CTA of a row takes up to
 // kWideThreads (shard, 16-byte chunk) tasks of that row's finalize with plain
 // 16-byte loads, writes the BF16 results z into a caller-provided workspace,
 // and counts itself done on the row's counter; the CTA that completes the
@@ -28,7 +28,8 @@ struct WideArgs {
     Args a;             // operands, sizes, eps, debug outputs, error word (stages unused)
     uint16_t *zws;      // workspace z rows, [T][R][H] BF16
     unsigned *count;    // workspace counters of finished CTAs, [T]; zero between calls
-    int parts;          // CTAs per token row: ceil(R * H/8 / kWideThreads)
+    int tasks;          // finalize tasks per CTA: kWideThreads, or a half or a quarter of it
+    int parts;          // CTAs per token row: ceil(R * H/8 / tasks)
 };
 
 // Dynamic shared memory of the kernel: the epilogue's gammas (FP32 [H] each).
