@@ -184,6 +184,45 @@ BN_API bn_status bn_finalize_reduce_residual_norm_ws(const uint16_t *expert_out,
                                               void *workspace, size_t workspace_bytes,
                                               void *stream);
 
+/* ---- the same finalize for callers that cannot allocate -------------------- */
+
+/* bn_finalize_reduce_norm_ws without a caller workspace: the library uses its
+ * own scratch, a static device array of 2 MiB (2097152 bytes).
+ *
+ * Who needs it: a caller that is handed only the op's input and output
+ * tensors and may not allocate device memory itself -- for example a serving
+ * engine whose memory pool has already reserved nearly all of HBM and owns
+ * every allocation, a plugin hook of an inference runtime that passes in and
+ * out pointers and no workspace slot, or a latency-critical path where
+ * cudaMalloc's implicit device synchronisation is not acceptable.
+ *
+ * Arguments, results and errors are those of bn_finalize_reduce_norm_ws.  The
+ * call allocates nothing (no cudaMalloc or cudaFree) and serves the shapes the
+ * many-CTA finalize serves (1 <= T <= 8, H <= 8192) whose workspace fits the
+ * scratch (bn_finalize_workspace_bytes(R, T, k, H) <= 2 MiB); any other valid
+ * shape gives BN_ERR_UNSUPPORTED with nothing enqueued (bn_last_error says
+ * why; bn_finalize_reduce_norm needs no scratch at all).
+ *
+ * The scratch:
+ *   - is reserved on a device by the first call there, which also looks up its
+ *     address once with that device current; make that first call before any
+ *     stream capture.  It then stays reserved on that device until the process
+ *     exits.
+ *   - is shared by every call of this entry point in the process and keeps the
+ *     last call's contents; each call clears the row counters it needs on
+ *     `stream` before its kernel.  Calls whose work may overlap on the GPU
+ *     (different streams without ordering between them) race on the scratch
+ *     and give wrong results: order them, or give them bn_finalize_reduce_norm_ws
+ *     with a workspace each.
+ * The pages describe no such entry point: it has no counterpart there. */
+BN_API bn_status bn_finalize_reduce_norm_noalloc(const uint16_t *expert_out,
+                                                 const int32_t *perm, const float *w,
+                                                 const uint16_t *shared, int R, int T, int k,
+                                                 int H, uint16_t *residual,
+                                                 const float *gamma_post, const float *gamma_pre,
+                                                 float eps, uint16_t *out, const bn_debug *dbg,
+                                                 void *stream);
+
 /* ---- unfused pieces (the decline / fallback path and its measurement) --- */
 
 /* Rank-ordered FP32 sum only: sum_out [T, H] FP32 = s. */

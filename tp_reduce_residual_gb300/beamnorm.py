@@ -33,7 +33,7 @@ EXPORTS = (
     "bn_norm_only", "bn_finalize_only", "bn_supports", "bn_check_device_error",
     "bn_last_error", "bn_status_string", "bn_version", "bn_set_tuning", "bn_query_launch",
     "bn_finalize_workspace_bytes", "bn_finalize_reduce_norm_ws",
-    "bn_finalize_reduce_residual_norm_ws",
+    "bn_finalize_reduce_residual_norm_ws", "bn_finalize_reduce_norm_noalloc",
 )
 
 # bn_op values of the entry points, for launch_info()
@@ -117,6 +117,8 @@ def load() -> ctypes.CDLL:
                                            dbgp, _P, ctypes.c_size_t, _P],
             "bn_finalize_reduce_residual_norm_ws": [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _F,
                                                     _P, dbgp, _P, ctypes.c_size_t, _P],
+            "bn_finalize_reduce_norm_noalloc": [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _F, _P,
+                                                dbgp, _P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -252,6 +254,41 @@ def finalize_reduce_norm(expert_out, perm, w, shared, residual, gamma_post, gamm
             wp, wn = _workspace(workspace, dev)
             _check(L.bn_finalize_reduce_norm_ws(*args, d[0] if d else None, wp, wn,
                                                 _stream(expert_out, stream)))
+    return out
+
+
+def finalize_reduce_norm_noalloc(expert_out, perm, w, shared, residual, gamma_post, gamma_pre,
+                                 eps: float, out=None, debug: Optional[Debug] = None,
+                                 stream=None) -> torch.Tensor:
+    """``finalize_reduce_norm`` with each token row spread over many CTAs,
+    using the library's own static scratch instead of a caller workspace.
+
+    For callers that are handed only the op's tensors and may not allocate
+    device memory (an engine whose pool owns all of HBM, a plugin hook with no
+    workspace slot).  The library call allocates nothing; ``out`` is allocated
+    here only when it is not given.  It serves 1 <= T <= 8 and H <= 8192 with
+    at most 2 MiB of scratch and raises BN_ERR_UNSUPPORTED otherwise.  The
+    first call on a device looks up the scratch's address: make it before any
+    stream capture.  Calls that may overlap on the GPU share the scratch and
+    race; order them."""
+    L = load()
+    R, T, k = perm.shape
+    H = expert_out.shape[-1]
+    dev = expert_out.device
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    args = (_need(expert_out, "expert_out", torch.bfloat16, (R, T * k, H), dev),
+            _need(perm, "perm", torch.int32, (R, T, k), dev),
+            _need(w, "w", torch.float32, (R, T, k), dev),
+            _opt(shared, "shared", torch.bfloat16, (R, T, H), dev), R, T, k, H,
+            _need(residual, "residual", torch.bfloat16, (T, H), dev),
+            _need(gamma_post, "gamma_post", torch.float32, (H,), dev),
+            _need(gamma_pre, "gamma_pre", torch.float32, (H,), dev), float(eps),
+            _need(out, "out", torch.bfloat16, (T, H), dev))
+    d = _debug(debug, R, T, H, dev, True)
+    with _with_device(expert_out):
+        _check(L.bn_finalize_reduce_norm_noalloc(*args, d[0] if d else None,
+                                                 _stream(expert_out, stream)))
     return out
 
 

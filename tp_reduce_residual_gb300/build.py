@@ -46,7 +46,7 @@ MODES = {
 }
 
 SOURCES = ["bn_device.cuh", "bn_internal.h", "bn_kernels.cu", "bn_abi.cu", "bn_wide.h",
-           "bn_wide.cu"]
+           "bn_wide.cu", "bn_noalloc.cu"]
 
 
 def nvcc() -> str:
@@ -97,6 +97,9 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int = 0) -> st
     wide_obj = os.path.join(OUT_DIR, "bn_wide.o")
     cmds.append([cc, *ARCH, *NVCC_FLAGS, *extra, *inc, "-c", os.path.join(CSRC, "bn_wide.cu"),
                  "-o", wide_obj])
+    noalloc_obj = os.path.join(OUT_DIR, "bn_noalloc.o")
+    cmds.append([cc, *ARCH, *NVCC_FLAGS, *inc, "-c", os.path.join(CSRC, "bn_noalloc.cu"),
+                 "-o", noalloc_obj])
     jobs = jobs or min(len(cmds), max(1, os.cpu_count() or 1))
     logs = []
     with cf.ThreadPoolExecutor(max_workers=jobs) as ex:

@@ -854,6 +854,59 @@ bn_status bn_finalize_reduce_residual_norm_ws(const uint16_t *expert_out, const 
                   dbg, workspace, workspace_bytes, stream);
 }
 
+// The many-CTA finalize for callers that cannot allocate: its workspace is the
+// library's own static scratch (bn_noalloc.cu).  The checks are those of the
+// workspace entry, then the scratch limit; the counters are cleared on the
+// stream just before the kernel.
+bn_status bn_finalize_reduce_norm_noalloc(const uint16_t *expert_out, const int32_t *perm,
+                                          const float *w, const uint16_t *shared, int R, int T,
+                                          int k, int H, uint16_t *residual,
+                                          const float *gamma_post, const float *gamma_pre,
+                                          float eps, uint16_t *out, const bn_debug *dbg,
+                                          void *stream)
+{
+    g_msg[0] = '\0';
+    BN_TRY(check_shape(R, T, k, H, true));
+    if (T == 0) return BN_OK;  // nothing is read or written; pointers are not examined
+    Range reads[8], writes[8];
+    int nr = 0, nw = 0;
+    BN_TRY(check_fin_sources(expert_out, perm, w, shared, R, T, k, H, reads, &nr));
+    BN_TRY(check_epilogue(residual, gamma_post, gamma_pre, out, eps, T, H, reads, &nr, writes, &nw));
+    BN_TRY(check_debug(dbg, true));
+    debug_ranges(dbg, R, T, H, true, writes, &nw);
+    BN_TRY(check_overlaps(writes, nw, reads, nr));
+    BN_TRY(check_served(R, T, k, H, true));
+    if (!wide_serves(R, T, k, H))
+        return fail(BN_ERR_UNSUPPORTED,
+                    "bn_finalize_reduce_norm_noalloc serves 1 <= T <= %d and H <= %d (got T=%d, "
+                    "H=%d); bn_finalize_reduce_norm needs no scratch for this shape",
+                    kWideMaxT, kWideThreads * kWideMaxCpt * 8, T, H);
+    const size_t need = wide_workspace_bytes(R, T, H);
+    if (need > kNoAllocScratchBytes)
+        return fail(BN_ERR_UNSUPPORTED,
+                    "R=%d T=%d H=%d needs %zu bytes of scratch, above the library's static "
+                    "maximum of %zu bytes",
+                    R, T, H, need, kNoAllocScratchBytes);
+    void *scratch = nullptr;
+    cudaError_t e = noalloc_scratch(&scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "looking up the static scratch");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // the row counters must start at zero (the z rows are written before they are read)
+    e = cudaMemsetAsync(scratch, 0, wide_counter_bytes(T), st);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch counters");
+    Args a = base_args(R, T, k, H, eps);
+    a.src = expert_out;
+    a.perm = perm;
+    a.w = w;
+    a.shared = shared;
+    a.residual = residual;
+    a.gamma_post = gamma_post;
+    a.gamma_pre = gamma_pre;
+    a.out = out;
+    apply_debug(a, dbg);
+    return run_wide(a, true, scratch, stream);
+}
+
 bn_status bn_reduce_only(const uint16_t *partials, int R, int T, int H, float *sum_out, void *stream)
 {
     g_msg[0] = '\0';

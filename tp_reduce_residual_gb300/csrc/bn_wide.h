@@ -47,4 +47,15 @@ inline size_t wide_workspace_bytes(int R, int T, int H)
 // pre-RMSNorm; cpt is the epilogue's chunks per thread (1, 2 or 4).
 cudaError_t launch_wide(const WideArgs &w, bool postnorm, int cpt, bool pdl, cudaStream_t st);
 
+// Size of the library-owned scratch behind bn_finalize_reduce_norm_noalloc
+// (a static device array, bn_noalloc.cu): 2 MiB, enough for the workspace of
+// every shape the many-CTA finalize serves with R <= 15 (R = 16, T = 8,
+// H = 8192 needs 256 bytes more and is declined).
+constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;
+
+// Device address of that scratch on the current device.  The first call on a
+// device looks it up (cudaGetSymbolAddress, with that device current); later
+// calls return the cached address.  Allocates nothing.
+cudaError_t noalloc_scratch(void **ptr);
+
 }  // namespace bn
