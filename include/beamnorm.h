@@ -33,9 +33,16 @@
  *   residual add:  h = residual[t] + y;  residual[t] = bf16(h)      (in place)
  *   pre-RMSNorm:   ss2 = sum_h h^2;  r2 = 1 / sqrt(ss2 / H + eps);
  *                  out[t] = bf16((h * r2) * gamma_pre)
- * The sums of squares are the FP32 rounding of the exact sum (the kernels
- * accumulate exact products in a compensated pair), so results do not depend
- * on how the row is split across threads.
+ * The sums of squares are compensated: each square's rounding error and each
+ * addition's are carried in a second FP32 accumulator, and the pair is rounded
+ * once.  That is as accurate as a sum carried in twice the precision: beyond
+ * the final rounding it is off the exact sum by at most about (n * 2^-24)^2
+ * relative and typically by about sqrt(n) * 2^-48, so it is the FP32 rounding
+ * of the exact sum unless that lies within such a distance of a rounding
+ * boundary (or squares fall below the FP32 normal range, |s| < 2^-63, where a
+ * product's error is itself rounded).  So results practically never depend on
+ * how a row is split across threads.  A sum beyond the FP32 range is +inf,
+ * as the exact sum rounded.
  *
  * Conventions for every entry point:
  *   - BF16 tensors are passed as uint16_t bit patterns.  All tensors are dense,

@@ -63,8 +63,11 @@ def assert_bits_equal(actual: np.ndarray, expected: np.ndarray, what: str = ""):
     ai = a.view(np.uint32) if a.dtype == np.float32 else a.view(np.uint16)
     ei = e.view(np.uint32) if e.dtype == np.float32 else e.view(np.uint16)
     bad = ai != ei
+    # a NaN equals any NaN (its sign and payload are not part of the result)
     if a.dtype == np.float32:
         bad &= ~(np.isnan(a) & np.isnan(e))
+    else:
+        bad &= ~(is_nan_bf16(ai) & is_nan_bf16(ei))
     if bad.any():
         idx = np.unravel_index(int(np.argmax(bad)), bad.shape)
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements differ; first at "
@@ -72,10 +75,20 @@ def assert_bits_equal(actual: np.ndarray, expected: np.ndarray, what: str = ""):
 
 
 def assert_rel_close(actual: np.ndarray, expected: np.ndarray, rtol: float, what: str = ""):
+    """Within rtol relative where the expected value is finite; identical
+    infinities and NaN == NaN elsewhere."""
     a = np.asarray(actual, dtype=np.float64)
     e = np.asarray(expected, dtype=np.float64)
+    fin = np.isfinite(e)
+    same = (np.isnan(a) & np.isnan(e)) | (np.isinf(e) & (a == e))
+    if not np.all(same | fin):
+        idx = np.unravel_index(int(np.argmax(~(same | fin))), e.shape)
+        raise AssertionError(f"{what}: expected {e[idx]} at {idx}, got {a[idx]}")
+    a, e = a[fin], e[fin]
+    if not np.all(np.isfinite(a)):
+        raise AssertionError(f"{what}: a non-finite value where the expected one is finite")
     rel = np.abs(a - e) / np.maximum(np.abs(e), 1e-30)
     if rel.size and rel.max() > rtol:
-        idx = np.unravel_index(int(rel.argmax()), rel.shape)
-        raise AssertionError(f"{what}: relative error {rel.max():.3e} > {rtol:.1e} at {idx}: "
-                             f"{a[idx]} vs {e[idx]}")
+        i = int(rel.argmax())
+        raise AssertionError(f"{what}: relative error {rel.max():.3e} > {rtol:.1e} at finite "
+                             f"element {i}: {a[i]} vs {e[i]}")

@@ -1,11 +1,12 @@
 """GPU-vs-oracle comparison helpers for the parity tests and the smoke check.
 
 Inputs come from the seeded generator (on the GPU for large cases); the
-oracle gets host copies of the same bytes.  For large T the oracle computes a
-sample of token rows: the sampled rows' operands (their shard rows, or their
-gathered expert rows with the perm renumbered) are copied into a compact input
-set, which the oracle processes exactly as it would the full one, since every
-token row depends only on its own operands.
+oracle gets host copies of the same bytes.  A block of token rows can be
+handed to the oracle on its own: the rows' operands (their shard rows, or
+their gathered expert rows with the perm renumbered) are copied into a
+compact input set, which the oracle processes exactly as it would the full
+one, since every token row depends only on its own operands.  Large cases
+run the oracle on every row this way, in blocks on a pool of host threads.
 
 Acceptance (per element): the FP32 reduced sum and the per-shard BF16
 finalize results bit-exact; the sums of squares within 1e-5 relative; the BF16
@@ -32,23 +33,36 @@ def gpu_inputs(wl, T, seed=None, with_shared=True):
     return inputs.make_inputs(wl, T, device="cuda", seed=seed, with_shared=with_shared)
 
 
+SENTINEL_BF16 = 0x4049      # 3.140625: a finite prefill for outputs that may be NaN
+SENTINEL_F32 = 1234.5
+
+
 def _nan_like(shape, dtype):
     if dtype == torch.bfloat16:
         return torch.full(shape, NAN_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
     return torch.full(shape, float("nan"), dtype=dtype, device="cuda")
 
 
-def run_fused(d, single: bool = False, debug: bool = True, stream=None, workspace=None) -> dict:
-    """One fused call on a copy of the residual; outputs prefilled with NaN.
-    ``workspace`` goes to the finalize entries (their many-CTA path)."""
+def _sentinel_like(shape, dtype):
+    if dtype == torch.bfloat16:
+        return torch.full(shape, SENTINEL_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    return torch.full(shape, SENTINEL_F32, dtype=dtype, device="cuda")
+
+
+def run_fused(d, single: bool = False, debug: bool = True, stream=None, workspace=None,
+              prefill: str = "nan") -> dict:
+    """One fused call on a copy of the residual; outputs prefilled with NaN
+    (``prefill="sentinel"``: a finite value, for inputs whose results may be
+    NaN).  ``workspace`` goes to the finalize entries (their many-CTA path)."""
     op, R, T, H, k = d["op"], d["R"], d["T"], d["H"], d["k"]
     fin = op == "finalize_reduce_norm"
+    fill = _nan_like if prefill == "nan" else _sentinel_like
     res = d["residual"].clone()
-    out = _nan_like((T, H), torch.bfloat16)
+    out = fill((T, H), torch.bfloat16)
     dbg = None
     if debug:
-        dbg = bn.Debug(sum=_nan_like((T, H), torch.float32), ss=_nan_like((T, 2), torch.float32),
-                       z=_nan_like((R, T, H), torch.bfloat16) if fin else None)
+        dbg = bn.Debug(sum=fill((T, H), torch.float32), ss=fill((T, 2), torch.float32),
+                       z=fill((R, T, H), torch.bfloat16) if fin else None)
     if not fin:
         if single:
             bn.reduce_residual_norm(d["partials"], res, d["gamma_pre"], d["eps"], out=out, debug=dbg,
@@ -108,6 +122,44 @@ def run_oracle(d, rows: Optional[Sequence[int]] = None, single: bool = False) ->
                                        flags=flags, want_z=True)
 
 
+def _oracle_host(h: dict, single: bool) -> dict:
+    flags = oracle.SINGLE_NORM if single else 0
+    if h["op"] == "reduce_norm":
+        return oracle.reduce_norm(h["partials"], h["residual"], h["gamma_post"], h["gamma_pre"],
+                                  h["eps"], flags=flags)
+    return oracle.finalize_reduce_norm(h["expert_out"], h["perm"], h["w"], h.get("shared"),
+                                       h["residual"], h["gamma_post"], h["gamma_pre"], h["eps"],
+                                       flags=flags, want_z=True)
+
+
+def run_oracle_all_rows(d, single: bool = False, block: int = 64, workers: int = 0) -> dict:
+    """Oracle results for every token row, computed in blocks of rows on a
+    pool of host threads.  Each block is a self-contained input set (the
+    rows' own operands, see ``compact``) and each oracle call is the plain
+    single-threaded C code; the ctypes call releases the interpreter lock, so
+    blocks run side by side.  Same result as ``run_oracle(d)``."""
+    import concurrent.futures as cf
+    import os
+
+    T = d["T"]
+    workers = workers or max(1, min(16, os.cpu_count() or 1))
+    blocks = [list(range(i, min(T, i + block))) for i in range(0, T, block)]
+    parts = [None] * len(blocks)
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        pending = {}
+        for i, rows in enumerate(blocks):
+            h = inputs.to_numpy(compact(d, rows))
+            pending[ex.submit(_oracle_host, h, single)] = i
+            if len(pending) >= 2 * workers:   # bound the host copies in flight
+                done, _ = cf.wait(pending, return_when=cf.FIRST_COMPLETED)
+                for f in done:
+                    parts[pending.pop(f)] = f.result()
+        for f in cf.as_completed(pending):
+            parts[pending[f]] = f.result()
+    return {key: np.concatenate([p[key] for p in parts], axis=1 if key == "z" else 0)
+            for key in parts[0]}
+
+
 def compare(g: dict, ref: dict, rows: Optional[Sequence[int]] = None, what: str = "") -> dict:
     """Assert the acceptance bar; return exact-match statistics."""
     sel = slice(None) if rows is None else np.asarray(rows)
@@ -124,12 +176,3 @@ def compare(g: dict, ref: dict, rows: Optional[Sequence[int]] = None, what: str 
     stats["out_exact"] = float(np.mean(bf16_ulp_diff(g["out"][sel], ref["out"]) == 0))
     stats["residual_exact"] = float(np.mean(bf16_ulp_diff(g["residual_out"][sel], ref["residual_out"]) == 0))
     return stats
-
-
-def sample_rows(T: int, n: int, seed: int = 0) -> list:
-    """First, last and evenly spread random rows (sorted, unique)."""
-    if T <= n:
-        return list(range(T))
-    rng = np.random.default_rng(seed)
-    rows = set([0, T - 1, T // 2]) | set(rng.choice(T, size=n - 3, replace=False).tolist())
-    return sorted(rows)[:n]

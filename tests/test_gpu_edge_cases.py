@@ -1,0 +1,186 @@
+"""The method's edge cases through the CUDA path, against the oracle (GB300).
+
+Each input set puts one edge case per token row (tp_reduce_residual_gb300.inputs
+.edge_inputs): signed zeros, negated shard pairs that sum to +0, the
+rank-order witness (1, 2^-24, 2^-24) that sums to 1 only in rank order, BF16
+subnormals, constant rows, rows whose sums of squares leave the FP32 range,
+shards holding +-inf and NaN, and a finalize whose weighted products cancel
+exactly (a guard against any fused multiply-add in the finalize).  Every
+entry point that runs these rows is compared with the oracle element by
+element, with the bar of the other parity tests (sum and z bit-exact, NaN ==
+NaN; sums of squares within 1e-5 relative, identical infinities; outputs within
+1 BF16 ulp).  Outputs are prefilled with a finite sentinel, so a NaN result
+is one the kernel wrote.
+
+Sources: "Fuse Beam's TP all-reduce with its sandwich norms" (vLLM pull request
+62366), section Claims (FP32 epilogue, finalize before the reduction keeping
+the local BF16 rounding) and section Details (no FMA contraction).
+"""
+import numpy as np
+import pytest
+import torch
+
+from tests import parity
+from tests.helpers import assert_bits_equal, f32_from_bf16
+from tp_reduce_residual_gb300 import beamnorm as bn
+from tp_reduce_residual_gb300 import build as nbuild
+from tp_reduce_residual_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+KINDS = inputs.EDGE_KINDS
+# the many-CTA finalize serves at most 8 token rows
+WS_KINDS = ("neg_zero", "neg_pairs", "witness", "subnormal", "overflow_post", "overflow_pre",
+            "inf_nan", "cancel")
+EPS0_KINDS = ("normal", "constant", "zero", "neg_pairs")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "the GPU tests need a CUDA device"
+    nbuild.build()
+    bn.load()
+    bn.set_tuning()
+    yield
+    bn.set_tuning()
+
+
+def _check_known_values(d, g, kinds, single):
+    """What the method fixes exactly, asserted on the GPU results themselves."""
+    R, H = d["R"], d["H"]
+    fin = d["op"] == "finalize_reduce_norm"
+    shared = fin and d.get("shared") is not None
+    res_in = inputs.u16(d["residual"])
+    lanes = np.arange(H)
+    for t, kind in enumerate(kinds):
+        sb = g["sum"][t].view(np.uint32)
+        zero_sum = False
+        if kind == "witness":
+            want = np.where(lanes % 2 == 0, 1.0, -1.0).astype(np.float32)
+            assert_bits_equal(g["sum"][t], want, f"row {t}: rank-order witness sum")
+        elif kind == "neg_zero":
+            # -0 + -0 stays -0; a +0 anywhere (another shard, the shared row) makes +0
+            neg = np.where(lanes % 2 == 0, not shared, R == 1 and not shared)
+            assert np.all(sb == np.where(neg, 0x80000000, 0)), f"row {t}: signed zeros"
+            zero_sum = True
+        elif kind == "neg_pairs" or (kind == "cancel" and fin and d["k"] >= 2):
+            assert np.all(sb == 0), f"row {t} ({kind}): the sum is not +0"
+            zero_sum = True
+            if kind == "cancel":
+                assert np.all(g["z"][:, t] == 0), f"row {t}: the cancelling finalize is not +0"
+        elif kind == "constant" and not single:
+            assert np.all(g["sum"][t] == 1024.0)
+            assert g["ss"][t, 0] == np.float32(H * 2.0 ** 20), g["ss"][t]
+        elif kind == "overflow_post" and not single:
+            assert np.isinf(g["ss"][t, 0]), f"row {t}: post-norm sum of squares {g['ss'][t, 0]}"
+            assert np.all(np.isfinite(f32_from_bf16(g["out"][t])))
+            assert np.all(np.isfinite(f32_from_bf16(g["residual_out"][t])))
+        elif kind == "overflow_pre":
+            assert np.isinf(g["ss"][t, 1]), f"row {t}: pre-norm sum of squares {g['ss'][t, 1]}"
+            assert np.all(np.isfinite(f32_from_bf16(g["residual_out"][t])))
+        if zero_sum:
+            # y (or s itself) is a signed zero: the residual comes back unchanged
+            assert np.all((g["residual_out"][t] & 0x7FFF) == (res_in[t] & 0x7FFF)), kind
+    if single:
+        assert np.all(g["ss"][:, 0] == 0.0)
+
+
+REDUCE = [
+    # (R, H, single)
+    (1, 1000, False), (1, 1000, True), (3, 256, False), (4, 5120, False), (4, 5120, True),
+    (8, 8192, False), (8, 8192, True), (2, 32768, False),
+]
+
+
+@pytest.mark.parametrize("R,H,single", REDUCE)
+def test_reduce_edge_cases_match_oracle(R, H, single):
+    d = inputs.edge_inputs("reduce_norm", R, H, KINDS, seed=100 + R + H)
+    g = parity.run_fused(d, single=single, prefill="sentinel")
+    parity.compare(g, parity.run_oracle(d, single=single), what=f"edge reduce R={R} H={H}")
+    _check_known_values(d, g, KINDS, single)
+
+
+FINALIZE = [
+    # (R, k, H, with_shared, single)
+    (1, 1, 1000, False, False), (2, 2, 256, True, False), (4, 4, 5120, False, False),
+    (4, 4, 5120, True, True), (8, 4, 8192, True, False), (8, 8, 6144, False, True),
+]
+
+
+@pytest.mark.parametrize("R,k,H,with_shared,single", FINALIZE)
+def test_finalize_edge_cases_match_oracle(R, k, H, with_shared, single):
+    d = inputs.edge_inputs("finalize_reduce_norm", R, H, KINDS, k=k, seed=200 + R + H,
+                           with_shared=with_shared)
+    g = parity.run_fused(d, single=single, prefill="sentinel")
+    parity.compare(g, parity.run_oracle(d, single=single), what=f"edge finalize R={R} k={k} H={H}")
+    _check_known_values(d, g, KINDS, single)
+
+
+@pytest.mark.parametrize("tuning", [dict(split=1, cluster_size=1), dict(split=1, cluster_size=4),
+                                    dict(split=2, cluster_size=2), dict(cluster_size=8)],
+                         ids=["one-CTA", "columns-x4", "shards-x2", "cluster-x8"])
+def test_edge_cases_on_every_row_split(tuning):
+    """The same rows through the column split (1 or 4 CTAs a row), the shard
+    split and an 8-CTA cluster: the cluster exchanges carry infinite and NaN
+    partial sums of squares too."""
+    for op in ("reduce_norm", "finalize_reduce_norm"):
+        d = inputs.edge_inputs(op, 4, 5120, KINDS, k=2, seed=300, with_shared=True)
+        try:
+            bn.set_tuning(**(tuning if op.startswith("finalize") else
+                             {"cluster_size": tuning.get("cluster_size", 0)}))
+            g = parity.run_fused(d, prefill="sentinel")
+        finally:
+            bn.set_tuning()
+        parity.compare(g, parity.run_oracle(d), what=f"edge {op} {tuning}")
+        _check_known_values(d, g, KINDS, False)
+
+
+@pytest.mark.parametrize("single", [False, True])
+@pytest.mark.parametrize("R,k,H", [(8, 4, 8192), (3, 2, 1000), (8, 8, 6144)])
+def test_workspace_finalize_edge_cases(R, k, H, single):
+    d = inputs.edge_inputs("finalize_reduce_norm", R, H, WS_KINDS, k=k, seed=400 + R + H,
+                           with_shared=True)
+    ws = bn.finalize_workspace(R, len(WS_KINDS), k, H, device="cuda")
+    assert ws is not None
+    g = parity.run_fused(d, single=single, workspace=ws, prefill="sentinel")
+    parity.compare(g, parity.run_oracle(d, single=single), what=f"edge workspace R={R} H={H}")
+    _check_known_values(d, g, WS_KINDS, single)
+
+
+@pytest.mark.parametrize("op", ["reduce_norm", "finalize_reduce_norm"])
+def test_split_and_materialised_finalize_edge_cases(op):
+    """The unfused pieces on the same rows: the FP32 sum, then the epilogue;
+    and the materialised per-shard finalize."""
+    d = inputs.edge_inputs(op, 4, 1000, KINDS, k=4, seed=500, with_shared=True)
+    ref = parity.run_oracle(d)
+    if op == "reduce_norm":
+        s = bn.reduce_only(d["partials"])
+    else:
+        s = bn.finalize_reduce_only(d["expert_out"], d["perm"], d["w"], d["shared"])
+        z = bn.finalize_only(d["expert_out"], d["perm"], d["w"], d["shared"])
+        torch.cuda.synchronize()
+        assert_bits_equal(inputs.u16(z), ref["z"], "materialised z")
+    res = d["residual"].clone()
+    ss = parity._sentinel_like((d["T"], 2), torch.float32)
+    out = bn.norm_only(s, res, d["gamma_post"], d["gamma_pre"], d["eps"], debug=bn.Debug(ss=ss))
+    assert bn.check_device_error() == 0
+    g = {"sum": s.cpu().numpy(), "ss": ss.cpu().numpy(), "out": inputs.u16(out),
+         "residual_out": inputs.u16(res)}
+    parity.compare(g, ref, what=f"edge split {op}")
+
+
+@pytest.mark.parametrize("op,single", [("reduce_norm", False), ("reduce_norm", True),
+                                       ("finalize_reduce_norm", False)])
+def test_eps_zero_with_an_all_zero_row(op, single):
+    """eps = 0: an all-zero row (and a row of negated pairs) has a zero sum of
+    squares, so its RMS factor is 1/0 = inf and 0 * inf gives NaN on both
+    sides; the other rows are unaffected."""
+    d = inputs.edge_inputs(op, 4, 5120, EPS0_KINDS, k=2, seed=600, eps=0.0)
+    g = parity.run_fused(d, single=single, prefill="sentinel")
+    ref = parity.run_oracle(d, single=single)
+    parity.compare(g, ref, what=f"eps=0 {op}")
+    if not single:
+        zero_row = EPS0_KINDS.index("zero")
+        assert np.all(np.isnan(f32_from_bf16(g["out"][zero_row])))
+        normal_row = EPS0_KINDS.index("normal")
+        assert np.all(np.isfinite(f32_from_bf16(g["out"][normal_row])))

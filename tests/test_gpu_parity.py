@@ -94,17 +94,16 @@ def test_single_norm_variants(op):
 # ---- the five workloads at their full sizes ------------------------------------------
 
 SWEEP = [(wl.index, T) for wl in inputs.WORKLOADS for T in wl.tokens]
-FULL_ORACLE_LIMIT = 256    # tokens up to which the oracle checks every row
-SAMPLE = 48                # rows the oracle checks above that
 
 
 @pytest.mark.parametrize("idx,T", SWEEP, ids=[f"C{i}-T{T}" for i, T in SWEEP])
 def test_workload_parity(idx, T):
+    """Every token row of every workload at its full size, in the launch shape
+    the benchmark times, against the oracle."""
     wl = inputs.WORKLOADS[idx]
     d = parity.gpu_inputs(wl, T)
     g = parity.run_fused(d)
-    rows = None if T <= FULL_ORACLE_LIMIT else parity.sample_rows(T, SAMPLE, seed=T)
-    stats = parity.compare(g, parity.run_oracle(d, rows=rows), rows=rows, what=wl.describe(T))
+    stats = parity.compare(g, parity.run_oracle_all_rows(d), what=wl.describe(T))
     # the compensated sums of squares are the correctly rounded exact sums:
     # nearly all match the oracle's double accumulation bit for bit
     assert stats["ss_exact"] >= 0.99, stats

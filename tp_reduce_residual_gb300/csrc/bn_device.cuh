@@ -27,8 +27,11 @@
 //     coalesced stores of the BF16 outputs.
 //   * A sum of squares is accumulated as a compensated pair (exact products via
 //     one explicit fma for the error term, two-sum for the additions), combined
-//     in a fixed warp/block/cluster tree, and rounded once: the result is the
-//     FP32 rounding of the exact sum, independent of the row's split.
+//     in a fixed warp/block/cluster tree, and rounded once: as accurate as a
+//     sum in twice the precision (typically within sqrt(n) * 2^-48 relative
+//     of the exact sum before the final rounding), so it is the FP32 rounding
+//     of the exact sum except right at a rounding boundary; a sum beyond the
+//     FP32 range is +inf.
 //   * Cluster partial sums (and the shard split's z rows) travel through
 //     distributed shared memory as st.async remote stores whose completion
 //     the receiving CTA's mbarrier counts in bytes -- no global scratch.
@@ -422,6 +425,15 @@ __device__ __forceinline__ void fold2(f2 S2, f2 E2, float &S, float &E)
     combine(S, E, s1, e1);
 }
 
+// The rounded value of a compensated pair.  A sum of non-negative squares
+// whose running part S has left the FP32 range is +inf (NaN if an operand was
+// NaN); its error part E then holds inf - inf = NaN, so S itself is the
+// result -- as for the exactly accumulated sum rounded once.
+__device__ __forceinline__ float pair_value(float S, float E)
+{
+    return S < __int_as_float(0x7f800000) ? S + E : S;
+}
+
 __device__ __forceinline__ void warp_tree(float &S, float &E)
 {
 #pragma unroll
@@ -491,7 +503,7 @@ __device__ __forceinline__ float row_sum_squares(f2 S2, f2 E2, int &nred, const 
         for (uint32_t c = 1; c < cs; ++c) combine(S, E, slots[c].x, slots[c].y);
     }
     ++nred;
-    return S + E;
+    return pair_value(S, E);
 }
 
 // SPLITR (finalize modes only): the cs CTAs of a cluster split a token row by

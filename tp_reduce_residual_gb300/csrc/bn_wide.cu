@@ -11,8 +11,11 @@
 //   y     = (s * r1) * gamma_post,  r1 = 1/sqrt(sum(s^2)/H + eps)   (sandwich only)
 //   h     = residual + y  ->  residual = bf16(h)
 //   out   = bf16((h * r2) * gamma_pre),  r2 = 1/sqrt(sum(h^2)/H + eps)
-// The sums of squares are the same compensated pairs, rounded once, so they
-// are the FP32 rounding of the exact sums here too.
+// The sums of squares are the same compensated pairs (TwoProduct and TwoSum
+// errors carried in a second accumulator), combined in a fixed tree and
+// rounded once, as in the main kernel; like them they are the FP32 rounding of
+// the exact sum except right at a rounding boundary (they are as accurate as a
+// sum carried in twice the precision).
 //
 // Memory ordering: a CTA barrier, then one device-scope fence by thread 0
 // before its atomicInc on the row's counter (the fence is cumulative over the
@@ -46,7 +49,7 @@ __device__ __forceinline__ float cta_sum_squares(f2 S2, f2 E2, float2 *red, int 
     warp_tree(S, E);
     S = __shfl_sync(0xffffffffu, S, 0);
     E = __shfl_sync(0xffffffffu, E, 0);
-    return S + E;
+    return pair_value(S, E);
 }
 
 // 16 bytes global -> shared without a register round trip (completion: wait_all).

@@ -179,3 +179,143 @@ def algorithmic_bytes(op: str, R: int, T: int, H: int, k: int = 0, split: bool =
     if split:
         b += 8 * T * H
     return b
+
+
+# ---------------------------------------------------------------------------------------
+# edge cases of the method: special values and exactly known sums, one kind per token row
+
+EDGE_KINDS = ("normal", "neg_zero", "neg_pairs", "witness", "subnormal", "constant",
+              "overflow_post", "overflow_pre", "inf_nan", "cancel")
+
+
+def _bf16_exact(x: np.ndarray) -> np.ndarray:
+    """FP32 values rounded to BF16 (PyTorch's rounding), returned as FP32."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.float().numpy()
+
+
+def _edge_row(kind: str, R: int, H: int, rng: np.random.Generator):
+    """Shard values [R, H] and residual [H] (FP32, exact in BF16) of one row."""
+    p = np.zeros((R, H), dtype=np.float32)
+    res = _bf16_exact(rng.standard_normal(H).astype(np.float32))
+    lanes = np.arange(H)
+    if kind in ("normal", "cancel"):
+        p[:] = _bf16_exact(0.5 * rng.standard_normal((R, H)).astype(np.float32))
+    elif kind == "neg_zero":
+        # even lanes: every shard -0 (the sum stays -0); odd lanes: shard 0
+        # -0 and the others +0 (the sum is +0 once a +0 is added)
+        p[:] = 0.0
+        p[:, lanes % 2 == 0] = -0.0
+        p[0, lanes % 2 == 1] = -0.0
+    elif kind == "neg_pairs":
+        # shard 2i+1 = -(shard 2i); an odd last shard is +0: the sum is +0
+        for r in range(0, R - 1, 2):
+            p[r] = _bf16_exact(rng.standard_normal(H).astype(np.float32))
+            p[r + 1] = -p[r]
+    elif kind == "witness":
+        # (1, 2^-24, 2^-24, 0, ...) in rank order sums to 1.0 exactly (each
+        # add is a tie to even); any other order gives 1 + 2^-23.  Odd lanes
+        # carry the negated values.
+        sign = np.where(lanes % 2 == 0, 1.0, -1.0).astype(np.float32)
+        p[0] = sign
+        for r in (1, 2):
+            if r < R:
+                p[r] = sign * np.float32(2.0 ** -24)
+    elif kind == "subnormal":
+        # BF16 subnormals (exponent field 0) with random signs, residual too
+        def sub(n):
+            bits = rng.integers(1, 0x80, size=n).astype(np.uint32) << 16
+            bits |= (rng.integers(0, 2, size=n).astype(np.uint32) << 31)
+            return bits.view(np.float32)
+        p[:] = sub(R * H).reshape(R, H)
+        res = sub(H)
+    elif kind == "constant":
+        # s = 2^10 on every lane (shard 0 carries it, the rest are +0)
+        p[0] = np.float32(1024.0)
+    elif kind == "overflow_post":
+        # the sum of squares of s leaves the FP32 range
+        p[:] = _bf16_exact(1e20 * rng.standard_normal((R, H)).astype(np.float32))
+    elif kind == "overflow_pre":
+        # the sum of squares of h = residual + y leaves the FP32 range
+        p[:] = _bf16_exact(0.5 * rng.standard_normal((R, H)).astype(np.float32))
+        res = _bf16_exact(1e20 * rng.standard_normal(H).astype(np.float32))
+    elif kind == "inf_nan":
+        p[:] = _bf16_exact(0.5 * rng.standard_normal((R, H)).astype(np.float32))
+        r = 1 if R > 1 else 0
+        p[r, 3 % H] = np.inf
+        p[r, 7 % H] = -np.inf
+        p[r, 11 % H] = np.nan
+    elif kind == "zero":
+        pass
+    else:
+        raise ValueError(kind)
+    return p, res
+
+
+def edge_inputs(op: str, R: int, H: int, kinds: Sequence[str], k: int = 4, seed: int = 0,
+                eps: float = 1e-6, with_shared: bool = False, device="cuda") -> dict:
+    """One input set whose token row t is an edge case of kind ``kinds[t]``.
+
+    For reduce_norm the shard rows are the kinds' values.  For
+    finalize_reduce_norm each shard's k gathered rows all carry the value
+    and every weight is 1/k (k a power of two), so the per-shard finalize
+    reproduces the value exactly; the kind "cancel" instead gathers one
+    random row twice with weights (w, -w) (w random, its products inexact)
+    and zero weights on the other slots, so the finalize is exactly +0
+    unless a weighted product is fused into the following addition.  The
+    shared-expert rows, when present, are +0 except on "normal" rows.
+    Same dict layout as ``make_inputs``.
+    """
+    rng = np.random.default_rng(seed)
+    T = len(kinds)
+    P = np.zeros((R, T, H), dtype=np.float32)
+    res = np.zeros((T, H), dtype=np.float32)
+    for t, kind in enumerate(kinds):
+        P[:, t], res[t] = _edge_row(kind, R, H, rng)
+    gp = (1.0 + 0.1 * rng.standard_normal(H)).astype(np.float32)
+    gq = (1.0 + 0.1 * rng.standard_normal(H)).astype(np.float32)
+    d: dict = {"R": R, "T": T, "H": H, "k": k if op == "finalize_reduce_norm" else 0,
+               "eps": float(eps), "op": op, "seed": seed,
+               "residual": from_u16(_f32_bits_to_bf16(res), device),
+               "gamma_post": torch.from_numpy(gp).to(device),
+               "gamma_pre": torch.from_numpy(gq).to(device)}
+    if op == "reduce_norm":
+        d["partials"] = from_u16(_f32_bits_to_bf16(P), device)
+        return d
+    assert k >= 1 and (k & (k - 1)) == 0, "k must be a power of two"
+    X = np.repeat(P[:, :, None, :], k, axis=2)              # [R, T, k, H]
+    W = np.full((R, T, k), 1.0 / k, dtype=np.float32)
+    for t, kind in enumerate(kinds):
+        if kind == "cancel" and k >= 2:
+            for r in range(R):
+                v = _bf16_exact((1.0 + rng.random(H)).astype(np.float32))
+                X[r, t, 0] = v
+                X[r, t, 1] = v
+                w0 = np.float32(rng.uniform(0.1, 0.9))
+                W[r, t] = 0.0
+                W[r, t, 0] = w0
+                W[r, t, 1] = -w0
+    perm = np.stack([rng.permutation(T * k) for _ in range(R)]).astype(np.int32).reshape(R, T, k)
+    E = np.zeros((R, T * k, H), dtype=np.float32)
+    for r in range(R):
+        E[r, perm[r].reshape(-1)] = X[r].reshape(T * k, H)
+    d["expert_out"] = from_u16(_f32_bits_to_bf16(E), device)
+    d["perm"] = torch.from_numpy(perm).to(device)
+    d["w"] = torch.from_numpy(W).to(device)
+    if with_shared:
+        S = np.zeros((R, T, H), dtype=np.float32)
+        for t, kind in enumerate(kinds):
+            if kind == "normal":
+                S[:, t] = _bf16_exact(0.3 * rng.standard_normal((R, H)).astype(np.float32))
+        d["shared"] = from_u16(_f32_bits_to_bf16(S), device)
+    else:
+        d["shared"] = None
+    return d
+
+
+def _f32_bits_to_bf16(x: np.ndarray) -> np.ndarray:
+    """BF16 bit patterns of FP32 values that are exact in BF16 (NaN kept as NaN)."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    nan = np.isnan(x)
+    assert np.all((b[~nan] & 0xFFFF) == 0), "value not exact in BF16"
+    return np.where(nan, (b >> 16) | 0x40, b >> 16).astype(np.uint16)
