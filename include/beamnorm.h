@@ -292,6 +292,14 @@ typedef struct {
     int dependent_launch; /* 1: plain stream order, 2: programmatic dependent
                              launch (the launch and the kernel's setup overlap
                              the previous kernel in the stream) */
+    int wait_limit_polls; /* for tests of the failure path: the copy-pipeline
+                             waits give up after this many polls (the default
+                             is 2^26 polls or 2^29 SM cycles).  A call whose
+                             wait gives up sets BN_DEVERR_TIMEOUT, stores
+                             nothing more, still drains its copies and returns;
+                             its outputs are then unspecified (each within its
+                             own buffer).  Not applied to the many-CTA
+                             finalize, which never waits. */
 } bn_tuning;
 
 /* Set the overrides; NULL restores automatic choices.  BN_ERR_INVALID on an

@@ -176,3 +176,23 @@ def compare(g: dict, ref: dict, rows: Optional[Sequence[int]] = None, what: str 
     stats["out_exact"] = float(np.mean(bf16_ulp_diff(g["out"][sel], ref["out"]) == 0))
     stats["residual_exact"] = float(np.mean(bf16_ulp_diff(g["residual_out"][sel], ref["residual_out"]) == 0))
     return stats
+
+
+# ---- memory-safety substitutes: outputs inside NaN-filled guard bands -----------------
+
+def guarded(n, dtype, guard=4096):
+    """A tensor of n elements inside a NaN-filled buffer with guard bands of
+    ``guard`` bytes on each side: (buffer, tensor, guard elements)."""
+    esz = torch.tensor([], dtype=dtype).element_size()
+    g = guard // esz
+    buf = _nan_like((g + n + g,), dtype)
+    return buf, buf[g:g + n], g
+
+
+def guard_intact(buf, g, n) -> bool:
+    """True if the guard bands around the n elements are still all NaN."""
+    if buf.dtype == torch.bfloat16:
+        bits = buf.view(torch.int16)
+        return bool((bits[:g] == NAN_BF16).all() and (bits[g + n:] == NAN_BF16).all())
+    return bool(torch.isnan(buf[:g]).all() and torch.isnan(buf[g + n:]).all())
+

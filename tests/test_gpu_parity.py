@@ -532,21 +532,8 @@ def test_two_calls_update_the_residual_twice():
 
 # ---- memory safety substitutes (guard bands, NaN prefill) --------------------------------
 
-def _guarded(n, dtype, guard=4096):
-    """A tensor of n elements inside a NaN-filled buffer with guard bands."""
-    esz = torch.tensor([], dtype=dtype).element_size()
-    g = guard // esz
-    buf = parity._nan_like((g + n + g,), dtype)
-    return buf, buf[g:g + n], g
-
-
-def _guard_intact(buf, g, n):
-    bits = buf.view(torch.int16) if buf.dtype == torch.bfloat16 else buf.view(torch.int32)
-    ref = parity.NAN_BF16 if buf.dtype == torch.bfloat16 else None
-    head, tail = bits[:g], bits[g + n:]
-    if ref is not None:
-        return bool((head == ref).all() and (tail == ref).all())
-    return bool(torch.isnan(buf[:g]).all() and torch.isnan(buf[g + n:]).all())
+_guarded = parity.guarded
+_guard_intact = parity.guard_intact
 
 
 @pytest.mark.parametrize("cluster", [1, 16])

@@ -55,7 +55,8 @@ _STATUS_NAMES = {OK: "BN_OK", ERR_INVALID: "BN_ERR_INVALID", ERR_UNSUPPORTED: "B
 class _Tuning(ctypes.Structure):
     _fields_ = [("cluster_size", ctypes.c_int), ("stages", ctypes.c_int), ("threads", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int), ("wait_mode", ctypes.c_int), ("group", ctypes.c_int),
-                ("split", ctypes.c_int), ("dependent_launch", ctypes.c_int)]
+                ("split", ctypes.c_int), ("dependent_launch", ctypes.c_int),
+                ("wait_limit_polls", ctypes.c_int)]
 
 
 class _LaunchInfo(ctypes.Structure):
@@ -429,10 +430,13 @@ def check_device_error(stream=None, raise_on_error: bool = True) -> int:
 
 
 def set_tuning(cluster_size: int = 0, stages: int = 0, threads: int = 0, ctas_per_sm: int = 0,
-               wait_mode: int = 0, group: int = 0, split: int = 0, dependent_launch: int = 0) -> None:
-    """Override the launch shape for measurement sweeps (0 = automatic)."""
+               wait_mode: int = 0, group: int = 0, split: int = 0, dependent_launch: int = 0,
+               wait_limit_polls: int = 0) -> None:
+    """Override the launch shape for measurement sweeps (0 = automatic);
+    ``wait_limit_polls`` shortens the pipeline waits' limit, for tests of the
+    timeout path."""
     t = _Tuning(int(cluster_size), int(stages), int(threads), int(ctas_per_sm), int(wait_mode),
-                int(group), int(split), int(dependent_launch))
+                int(group), int(split), int(dependent_launch), int(wait_limit_polls))
     _check(load().bn_set_tuning(ctypes.byref(t)))
 
 

@@ -29,7 +29,7 @@ namespace bn {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kVersion = 10100;  // 1.1.0
 
 thread_local char g_msg[512] = "";
 
@@ -50,7 +50,7 @@ bn_status cuda_fail(cudaError_t e, const char *what)
 // ---- tuning overrides (process-wide) -------------------------------------------
 
 std::atomic<int> g_tune_cluster{0}, g_tune_stages{0}, g_tune_threads{0}, g_tune_ctas{0},
-    g_tune_wait{0}, g_tune_group{0}, g_tune_split{0}, g_tune_pdl{0};
+    g_tune_wait{0}, g_tune_group{0}, g_tune_split{0}, g_tune_pdl{0}, g_tune_polls{0};
 
 // ---- per-device state ------------------------------------------------------------
 
@@ -426,6 +426,7 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     a->gamma_stride = slice;
     a->zbuf_bytes = zbuf_bytes;
     a->spin_wait = g_tune_wait.load() == 2 ? 1 : 0;
+    a->wait_polls = g_tune_polls.load();
     a->nchunks = nchunks;
     a->err = d->err;
     return BN_OK;
@@ -1072,6 +1073,8 @@ bn_status bn_set_tuning(const bn_tuning *t)
         return fail(BN_ERR_INVALID, "split must be 0, 1 or 2");
     if (t->dependent_launch < 0 || t->dependent_launch > 2)
         return fail(BN_ERR_INVALID, "dependent_launch must be 0, 1 or 2");
+    if (t->wait_limit_polls < 0)
+        return fail(BN_ERR_INVALID, "wait_limit_polls must not be negative");
     g_tune_cluster.store(cs);
     g_tune_stages.store(t->stages);
     g_tune_threads.store(t->threads);
@@ -1080,6 +1083,7 @@ bn_status bn_set_tuning(const bn_tuning *t)
     g_tune_group.store(t->group);
     g_tune_split.store(t->split);
     g_tune_pdl.store(t->dependent_launch);
+    g_tune_polls.store(t->wait_limit_polls);
     return BN_OK;
 }
 

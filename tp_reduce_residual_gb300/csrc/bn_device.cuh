@@ -35,9 +35,11 @@
 //   * Cluster partial sums (and the shard split's z rows) travel through
 //     distributed shared memory as st.async remote stores whose completion
 //     the receiving CTA's mbarrier counts in bytes -- no global scratch.
-//   * Every wait is bounded (SM cycles and polls); on expiry the kernel records an error bit,
-//     stops issuing copies, drains the copies it has in flight, runs the rest of
-//     its control flow without waiting and without storing, and returns.
+//   * Every wait is bounded (SM cycles and polls); on expiry the kernel records an
+//     error bit, stops issuing copies, drains the copies it has in flight, runs
+//     the rest of its control flow without waiting on the copy pipeline and
+//     without storing (the cluster exchanges, which every CTA still feeds, are
+//     still waited for), and returns.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -214,11 +216,28 @@ __device__ __forceinline__ void consumer_sync(int nthreads)
 
 // ---- bounded waits --------------------------------------------------------------
 
+// Abort bits of a CTA (a shared-memory word).
+constexpr int kAbortPipe = 1;   // a wait expired: stop issuing copies, stop storing
+constexpr int kAbortDsmem = 2;  // a cluster exchange itself expired: stop waiting on exchanges
+
 struct Ctl {
-    volatile int *abort;  // shared flag: set once any wait of this CTA expired
+    volatile int *abort;  // shared abort bits of this CTA
     unsigned *err;        // device error word
     bool spin;            // poll with test_wait instead of the suspending try_wait
+    uint32_t pipe_polls;  // polls after which a pipeline wait gives up
 };
+
+// Kinds of wait.
+//   kPipe:  the copy pipeline (stage and metadata barriers).  Returns false at
+//           once while the CTA is aborting; gives up after ctl.pipe_polls polls
+//           (normally 2^26) or 2^29 SM cycles.
+//   kDsmem: the cluster exchanges (sums of squares, shard-split z rows).  They
+//           are waited for even while the CTA aborts -- every CTA still sends
+//           what it owes, so they complete, and no remote store may still be in
+//           flight into a CTA that stops waiting -- unless an exchange itself
+//           expired.
+//   kDrain: the producer's final wait for its copies in flight; never skipped.
+enum WaitKind { kPipe = 0, kDsmem = 1, kDrain = 2 };
 
 template <bool CLUSTER_ACQUIRE>
 __device__ __forceinline__ bool phase_done(uint32_t bar, uint32_t parity, bool spin)
@@ -228,22 +247,24 @@ __device__ __forceinline__ bool phase_done(uint32_t bar, uint32_t parity, bool s
 }
 
 // Wait for the phase of `bar` with parity `parity` to complete.  Returns false
-// (without waiting) once the CTA is aborting, or after the time limit, in
-// which case it records the timeout and starts the abort.
-// The clock is read only after 1024 unsuccessful polls: a wait that ends
-// quickly costs nothing but the polls themselves.
-template <bool CLUSTER_ACQUIRE, bool HONOR_ABORT>
+// without waiting when the CTA's abort bits say this kind of wait is skipped,
+// or after the kind's limit, in which case it records the timeout and sets the
+// abort bits.  The clock is read only after 1024 unsuccessful polls: a wait
+// that ends quickly costs nothing but the polls themselves.
+template <bool CLUSTER_ACQUIRE, int KIND>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl &c)
 {
+    constexpr int kSkipOn = KIND == kPipe ? kAbortPipe : KIND == kDsmem ? kAbortDsmem : 0;
     // a completed phase returns at once (its data is valid even in a CTA that
-    // is aborting); the abort flag is read only when the wait must poll
+    // is aborting); the abort bits are read only when the wait must poll
     if (phase_done<CLUSTER_ACQUIRE>(bar, parity, c.spin)) return true;
-    if (HONOR_ABORT && *c.abort) return false;
+    if (kSkipOn != 0 && (*c.abort & kSkipOn)) return false;
+    const uint32_t limit = KIND == kPipe ? c.pipe_polls : kMaxSpins;
     long long t0 = 0;
-    for (uint32_t i = 1; i < kMaxSpins; ++i) {
+    for (uint32_t i = 1; i < limit; ++i) {
         if (phase_done<CLUSTER_ACQUIRE>(bar, parity, c.spin)) return true;
         if ((i & 1023u) == 0u) {
-            if (HONOR_ABORT && *c.abort) return false;
+            if (kSkipOn != 0 && (*c.abort & kSkipOn)) return false;
             if (i == 1024u)
                 t0 = clock64();
             else if (clock64() - t0 > kWaitLimitCycles)
@@ -251,7 +272,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
         }
     }
     atomicOr(c.err, kErrTimeout);
-    *c.abort = 1;
+    atomicOr(const_cast<int *>(c.abort), KIND == kDsmem ? (kAbortPipe | kAbortDsmem) : kAbortPipe);
     return false;
 }
 
@@ -497,7 +518,7 @@ __device__ __forceinline__ float row_sum_squares(f2 S2, f2 E2, int &nred, const 
             const uint32_t d = (uint32_t)tid;
             st_async_f2(mapa(smem_addr(slots + q), d), S, E, mapa(bar, d));
         }
-        if (!wait_phase<true, true>(bar, (uint32_t)(nred >> 1) & 1u, ctl)) live = false;
+        if (!wait_phase<true, kDsmem>(bar, (uint32_t)(nred >> 1) & 1u, ctl)) live = false;
         S = slots[0].x;
         E = slots[0].y;
         for (uint32_t c = 1; c < cs; ++c) combine(S, E, slots[c].x, slots[c].y);
@@ -588,7 +609,8 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
     // setup above overlaps the previous kernel's tail.  No global load or store
     // comes before this wait.
     griddep_wait();
-    const Ctl ctl{&s_abort, a.err, a.spin_wait != 0};
+    const Ctl ctl{&s_abort, a.err, a.spin_wait != 0,
+                  a.wait_polls > 0 ? (uint32_t)a.wait_polls : kMaxSpins};
 
     // Copies per token row ("items"), in the order both sides walk them:
     //   FIN:    for each shard r: its k gathered rows, then its shared row;
@@ -647,7 +669,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                 // publish this row's gather indices and weights (all lanes)
                 bool got = true;
                 if (lane == 0)
-                    got = wait_phase<false, true>(sm.mempty0 + 8u * slot,
+                    got = wait_phase<false, kPipe>(sm.mempty0 + 8u * slot,
                                                   (((uint32_t)it >> 1) & 1u) ^ 1u, ctl);
                 got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
                 if (!got) {
@@ -682,7 +704,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                     const uint32_t fb = sm.full0 + 8u * stage;
                     if (pos == 0) {
                         n_in = items_in_stage(left);
-                        if (!wait_phase<false, true>(sm.empty0 + 8u * stage, phase ^ 1u, ctl)) return false;
+                        if (!wait_phase<false, kPipe>(sm.empty0 + 8u * stage, phase ^ 1u, ctl)) return false;
                         mbar_arrive_expect_tx(fb, bytes * (uint32_t)n_in);
                         ++issued;
                     }
@@ -740,7 +762,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
             if (pos != 0) {
                 // the armed stage never completes its byte count: give its
                 // issued copies the bounded time to land
-                wait_phase<false, false>(sm.full0 + 8u * st, ph, ctl);
+                wait_phase<false, kDrain>(sm.full0 + 8u * st, ph, ctl);
             }
             const uint32_t done_n = pos != 0 ? n - 1 : n;
             for (uint32_t i = 0; i < done_n; ++i) {
@@ -750,7 +772,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                 } else {
                     --st;
                 }
-                wait_phase<false, false>(sm.full0 + 8u * st, ph, ctl);
+                wait_phase<false, kDrain>(sm.full0 + 8u * st, ph, ctl);
             }
         }
     } else {
@@ -766,17 +788,20 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
         auto take = [&]() -> const uint8_t * {
             if (!FIN || cpos == 0) {
                 cn = items_in_stage(cleft);
-                if (!wait_phase<false, true>(sm.full0 + 8u * stage, phase, ctl)) live = false;
+                if (!wait_phase<false, kPipe>(sm.full0 + 8u * stage, phase, ctl)) live = false;
                 cbase = sm.stages + (size_t)stage * (size_t)a.stage_bytes;
             }
             return cbase + (size_t)cpos * item_bytes;
         };
+        // A warp whose wait failed never releases a stage again: the producer
+        // must not re-arm a stage whose copies it has not seen land (lane 0
+        // saw every stage it releases complete).
         auto release = [&]() {
             --cleft;
             if (!FIN || ++cpos == cn) {
                 cpos = 0;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sm.empty0 + 8u * stage);
+                if (lane == 0 && live) mbar_arrive(sm.empty0 + 8u * stage);
                 if (++stage == (uint32_t)S) {
                     stage = 0;
                     phase ^= 1u;
@@ -846,7 +871,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                 }
                 release();
             } else if constexpr (FIN && SPLITR) {
-                if (!wait_phase<false, true>(sm.mfull0 + 8u * slot, ((uint32_t)it >> 1) & 1u, ctl))
+                if (!wait_phase<false, kPipe>(sm.mfull0 + 8u * slot, ((uint32_t)it >> 1) & 1u, ctl))
                     live = false;
                 const float *wrow = sm.mw + slot * kMaxMeta;
                 // Each 16-byte chunk of every z_r this CTA finalizes goes
@@ -933,7 +958,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sm.mempty0 + 8u * slot);
                 if constexpr (REDUCE) {
-                    if (!wait_phase<true, true>(zready, (uint32_t)it & 1u, ctl)) live = false;
+                    if (!wait_phase<true, kDsmem>(zready, (uint32_t)it & 1u, ctl)) live = false;
                     // rank-ordered sum of the R z rows over this CTA's slice,
                     // all from its own shared memory
 #pragma unroll
@@ -946,7 +971,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                     }
                 }
             } else if constexpr (FIN) {
-                if (!wait_phase<false, true>(sm.mfull0 + 8u * slot, ((uint32_t)it >> 1) & 1u, ctl))
+                if (!wait_phase<false, kPipe>(sm.mfull0 + 8u * slot, ((uint32_t)it >> 1) & 1u, ctl))
                     live = false;
                 const float *wrow = sm.mw + slot * kMaxMeta;
                 for (int r = 0; r < a.R; ++r) {

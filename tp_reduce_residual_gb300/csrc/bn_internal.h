@@ -61,6 +61,7 @@ struct Args {
     int gamma_stride;         // 16-byte slots per gamma half: the largest column slice in chunks
     int zbuf_bytes;           // shard split: shared-memory bytes of one full z row
     int spin_wait;            // 1: poll barriers with test_wait; 0: try_wait
+    int wait_polls;           // polls after which a pipeline wait gives up (0: the default)
     float eps;
 };
 
