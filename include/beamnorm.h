@@ -59,9 +59,10 @@
  *     required pointer, R or k outside [1, 16], T < 0, H <= 0, H % 8 != 0, a
  *     misaligned pointer, eps negative or not finite, or an output range that
  *     overlaps an input range gives BN_ERR_INVALID.  A valid shape that is not
- *     served (H > 32768, R * k > 256, T * k >= 2^31) gives BN_ERR_UNSUPPORTED;
- *     bn_supports() predicts it, so the caller can fall back (decline) before
- *     doing any work.  T == 0 returns BN_OK after the shape checks, enqueues
+ *     served gives BN_ERR_UNSUPPORTED with nothing enqueued -- the decline: the
+ *     fused entry points serve H <= 32768, the unfused pieces (the caller's
+ *     fallback) H <= 131072, and every entry with a finalize needs
+ *     T * k < 2^31.  bn_supports() and bn_supports_op() predict it.  T == 0 returns BN_OK after the shape checks, enqueues
  *     nothing and does not examine the pointers (empty tensors may be NULL).
  *   - dbg (nullable) asks for intermediate values, for testing:
  *       dbg->sum [T,H] FP32 reduced sum s, dbg->ss [T,2] FP32 (ss1, ss2),
@@ -249,6 +250,17 @@ BN_API bn_status bn_norm_only(const float *sum, int T, int H, uint16_t *residual
                        const float *gamma_post, const float *gamma_pre, float eps,
                        uint16_t *out, const bn_debug *dbg, void *stream);
 
+/* The single-norm epilogue given the FP32 sum [T, H]: h = residual + sum,
+ * residual = bf16(h) in place, out = bf16((h * r) * gamma) with
+ * r = 1 / sqrt(sum(h^2) / H + eps).  Together with bn_reduce_only /
+ * bn_finalize_reduce_only it gives the bits of bn_reduce_residual_norm /
+ * bn_finalize_reduce_residual_norm.  dbg->ss[:,0] is 0.
+ * Source: sglang pull request 34134, description (the plain all-reduce,
+ * residual add and RMSNorm pattern; the fallback when fusion declines). */
+BN_API bn_status bn_residual_norm_only(const float *sum, int T, int H, uint16_t *residual,
+                                       const float *gamma, float eps, uint16_t *out,
+                                       const bn_debug *dbg, void *stream);
+
 /* The deferred finalize materialised on its own: z_out [R, T, H] BF16 =
  * bf16(sum_j w*x_j + shared) per shard, with no reduction.
  * Source: sglang pull request 34134, description (the deferred finalize written
@@ -315,7 +327,8 @@ typedef enum {
     BN_OP_REDUCE_ONLY = 4,
     BN_OP_FINALIZE_REDUCE_ONLY = 5,
     BN_OP_NORM_ONLY = 6,
-    BN_OP_FINALIZE_ONLY = 7
+    BN_OP_FINALIZE_ONLY = 7,
+    BN_OP_RESIDUAL_NORM_ONLY = 8
 } bn_op;
 
 /* The launch shape one call would use on the current device. */
@@ -340,6 +353,16 @@ typedef struct {
  * an all-zero *info (no launch).  Needs a CUDA device (occupancy queries). */
 BN_API bn_status bn_query_launch(bn_op op, int R, int T, int k, int H, int has_shared,
                                  bn_launch_info *info);
+
+/* 1 if entry point `op` serves this shape, 0 if it would decline (or the
+ * arguments are invalid).  k is ignored without a finalize; R is ignored by
+ * the epilogue pieces.  The unfused pieces serve rows the fused entry points
+ * decline (H up to 131072), which is what a caller falls back to.  Pure host
+ * logic.
+ * Source: "Fuse Beam's TP all-reduce with its sandwich norms", "Details"
+ * (the workspace declines shapes it does not serve); sglang pull request
+ * 34134, description (a decline must not drop the reduction still owed). */
+BN_API int bn_supports_op(bn_op op, int R, int T, int k, int H);
 
 #ifdef __cplusplus
 }

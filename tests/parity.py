@@ -50,7 +50,7 @@ def _sentinel_like(shape, dtype):
 
 
 def run_fused(d, single: bool = False, debug: bool = True, stream=None, workspace=None,
-              prefill: str = "nan") -> dict:
+              prefill: str = "nan", on_decline: str = "raise") -> dict:
     """One fused call on a copy of the residual; outputs prefilled with NaN
     (``prefill="sentinel"``: a finite value, for inputs whose results may be
     NaN).  ``workspace`` goes to the finalize entries (their many-CTA path)."""
@@ -66,19 +66,20 @@ def run_fused(d, single: bool = False, debug: bool = True, stream=None, workspac
     if not fin:
         if single:
             bn.reduce_residual_norm(d["partials"], res, d["gamma_pre"], d["eps"], out=out, debug=dbg,
-                                    stream=stream)
+                                    stream=stream, on_decline=on_decline)
         else:
             bn.reduce_norm(d["partials"], res, d["gamma_post"], d["gamma_pre"], d["eps"], out=out,
-                           debug=dbg, stream=stream)
+                           debug=dbg, stream=stream, on_decline=on_decline)
     else:
         if single:
             bn.finalize_reduce_residual_norm(d["expert_out"], d["perm"], d["w"], d["shared"], res,
                                              d["gamma_pre"], d["eps"], out=out, debug=dbg,
-                                             stream=stream, workspace=workspace)
+                                             stream=stream, workspace=workspace,
+                                             on_decline=on_decline)
         else:
             bn.finalize_reduce_norm(d["expert_out"], d["perm"], d["w"], d["shared"], res,
                                     d["gamma_post"], d["gamma_pre"], d["eps"], out=out, debug=dbg,
-                                    stream=stream, workspace=workspace)
+                                    stream=stream, workspace=workspace, on_decline=on_decline)
     bits = bn.check_device_error(stream=stream)
     assert bits == 0, bits
     r = {"out": inputs.u16(out), "residual_out": inputs.u16(res)}

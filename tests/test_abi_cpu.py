@@ -204,7 +204,7 @@ def test_query_launch_validates_on_the_host(L):
     info = bn._LaunchInfo()
     q = lambda *a: L.bn_query_launch(*a, ctypes.byref(info))
     assert L.bn_query_launch(0, 2, 8, 0, 256, 0, None) == bn.ERR_INVALID
-    assert q(8, 2, 8, 0, 256, 0) == bn.ERR_INVALID          # no such operation
+    assert q(9, 2, 8, 0, 256, 0) == bn.ERR_INVALID          # no such operation
     assert q(-1, 2, 8, 0, 256, 0) == bn.ERR_INVALID
     assert q(0, 0, 8, 0, 256, 0) == bn.ERR_INVALID          # R outside [1, 16]
     assert q(1, 8, 8, 0, 256, 1) == bn.ERR_INVALID          # finalize needs k >= 1
@@ -213,4 +213,55 @@ def test_query_launch_validates_on_the_host(L):
     info.grid = 7
     assert q(3, 8, 0, 10, 8192, 1) == bn.OK                 # T == 0: no launch, all zero
     assert info.grid == 0 and info.stages == 0
-    assert bn.OPS.index("finalize_only") == 7
+    assert bn.OPS.index("finalize_only") == 7 and bn.OPS.index("residual_norm_only") == 8
+
+
+@pytest.mark.parametrize("op,R,T,k,H,expect", [
+    # fused entry points: rows up to 32768
+    ("reduce_norm", 4, 8, 0, 32768, 1), ("reduce_norm", 4, 8, 0, 40960, 0),
+    ("finalize_reduce_norm", 2, 3, 2, 40960, 0), ("reduce_residual_norm", 2, 3, 0, 65536, 0),
+    ("finalize_reduce_residual_norm", 8, 1, 10, 8192, 1),
+    # the unfused pieces, the fallback: rows up to 131072
+    ("reduce_only", 4, 8, 0, 40960, 1), ("reduce_only", 4, 8, 0, 131072, 1),
+    ("reduce_only", 4, 8, 0, 131080, 0), ("finalize_reduce_only", 2, 3, 2, 65536, 1),
+    ("finalize_only", 2, 3, 2, 40960, 1), ("norm_only", 1, 3, 0, 131072, 1),
+    ("norm_only", 9, 3, 0, 131072, 1),            # R is ignored by the epilogue pieces
+    ("residual_norm_only", 1, 3, 0, 98304, 1), ("residual_norm_only", 1, 3, 0, 262144, 0),
+    # invalid arguments are not served either
+    ("finalize_only", 2, 3, 0, 64, 0), ("reduce_only", 17, 3, 0, 64, 0),
+    ("finalize_only", 2, 2 ** 28, 16, 64, 0),      # T * k >= 2^31
+])
+def test_supports_op(L, op, R, T, k, H, expect):
+    assert L.bn_supports_op(bn.OPS.index(op), R, T, k, H) == expect
+    if op in ("reduce_norm", "finalize_reduce_norm") and expect == 0:
+        assert L.bn_supports(R, T, k, H) == 0
+
+
+def test_supports_op_rejects_unknown_operations(L):
+    assert L.bn_supports_op(len(bn.OPS), 2, 8, 0, 256) == 0
+    assert L.bn_supports_op(-1, 2, 8, 0, 256) == 0
+
+
+def test_residual_norm_only_validates_on_the_host(L):
+    f = L.bn_residual_norm_only
+    assert f(None, 4, 64, A16 * 10, A16 * 20, 1e-6, A16 * 30, None, None) == bn.ERR_INVALID
+    assert f(A16, 4, 64, None, A16 * 20, 1e-6, A16 * 30, None, None) == bn.ERR_INVALID
+    assert f(A16, 4, 60, A16 * 10, A16 * 20, 1e-6, A16 * 30, None, None) == bn.ERR_INVALID
+    assert f(A16, 4, 64, A16 * 10, A16 * 20, -1.0, A16 * 30, None, None) == bn.ERR_INVALID
+    assert f(A16, 4, 64, A16 * 10, A16 * 20, 1e-6, A16 + 16, None, None) == bn.ERR_INVALID
+    assert "overlaps" in L.bn_last_error().decode()
+    assert f(A16, 0, 64, None, None, 1e-6, None, None, None) == bn.OK
+    big = 262144
+    assert f(A16, 1, big, A16 * 100000, A16 * 200000, 1e-6, A16 * 300000, None,
+             None) == bn.ERR_UNSUPPORTED
+    assert "unfused pieces" in L.bn_last_error().decode()
+
+
+def test_binding_rejects_an_unknown_decline_policy():
+    err = bn.BeamNormError(bn.ERR_UNSUPPORTED, "declined")
+    with pytest.raises(ValueError, match="on_decline"):
+        bn._fallback_allowed(err, "ignore")
+    assert bn._fallback_allowed(err, "fallback")
+    assert not bn._fallback_allowed(err, "raise")
+    assert not bn._fallback_allowed(bn.BeamNormError(bn.ERR_INVALID, "bad"), "fallback")
+

@@ -128,6 +128,26 @@ def test_reduce_split_equals_fused():
     assert_bits_equal(ss.cpu().numpy(), fused["ss"], "ss")
 
 
+@pytest.mark.parametrize("op", ["reduce_norm", "finalize_reduce_norm"])
+def test_single_norm_split_equals_fused(op):
+    """The single-norm pattern unfused: the FP32 sum, then residual_norm_only."""
+    wl = inputs.custom(op, 4, 5120, 3 if op != "reduce_norm" else 0, partial_std=0.3)
+    d = parity.gpu_inputs(wl, 29, seed=41)
+    fused = parity.run_fused(d, single=True)
+    if op == "reduce_norm":
+        s = bn.reduce_only(d["partials"])
+    else:
+        s = bn.finalize_reduce_only(d["expert_out"], d["perm"], d["w"], d["shared"])
+    res = d["residual"].clone()
+    ss = torch.full((29, 2), float("nan"), device="cuda")
+    out = bn.residual_norm_only(s, res, d["gamma_pre"], d["eps"], debug=bn.Debug(ss=ss))
+    torch.cuda.synchronize()
+    assert_bits_equal(s.cpu().numpy(), fused["sum"], "sum")
+    assert_bits_equal(inputs.u16(res), fused["residual_out"], "residual_out")
+    assert_bits_equal(inputs.u16(out), fused["out"], "out")
+    assert_bits_equal(ss.cpu().numpy(), fused["ss"], "ss")
+
+
 @pytest.mark.parametrize("with_shared", [True, False])
 def test_finalize_split_equals_fused(with_shared):
     wl = inputs.WORKLOADS[4]
@@ -276,6 +296,38 @@ def test_decline_then_fallback_gives_the_same_bits():
     assert_bits_equal(inputs.u16(out), fused["out"], "out")
 
 
+DECLINED = [
+    # (op, R, T, k, H, with_shared, single): shapes the fused entry points decline
+    ("finalize_reduce_norm", 2, 3, 2, 40960, True, False),
+    ("finalize_reduce_norm", 3, 2, 4, 65536, False, True),
+    ("reduce_norm", 4, 5, 0, 40960, False, False),
+    ("reduce_norm", 2, 3, 0, 131072, False, True),
+    ("finalize_reduce_norm", 1, 2, 1, 131072, True, False),
+]
+
+
+@pytest.mark.parametrize("op,R,T,k,H,with_shared,single", DECLINED)
+def test_declined_shape_falls_back_to_the_unfused_pieces(op, R, T, k, H, with_shared, single):
+    """A fused call declines a row it does not serve: it enqueues nothing, so
+    the reduction is still owed.  The caller's fallback (the binding's
+    on_decline="fallback") materialises the finalize, sums the shards and runs
+    the epilogue on the FP32 sum, with the oracle's results."""
+    assert not bn.supports(R, T, k, H)
+    pieces = (["finalize_only"] if k else []) + ["reduce_only"] + \
+        ["residual_norm_only" if single else "norm_only"]
+    for piece in pieces:
+        assert bn.supports_op(piece, R, T, H, k), piece
+    wl = inputs.custom(op, R, H, k, partial_std=0.3, shared_std=0.3)
+    d = parity.gpu_inputs(wl, T, seed=700 + R + T, with_shared=with_shared)
+    with pytest.raises(bn.BeamNormError) as e:
+        parity.run_fused(d, single=single)
+    assert e.value.status == bn.ERR_UNSUPPORTED
+    g = parity.run_fused(d, single=single, on_decline="fallback")
+    ref = parity.run_oracle(d, single=single)
+    parity.compare(g, ref, what=f"fallback {op} R={R} T={T} k={k} H={H}")
+    assert bn.check_device_error() == 0
+
+
 # ---- launch shapes, streams, graphs ------------------------------------------------------
 
 @pytest.mark.parametrize("cluster,stages,threads,ctas,wait,group", [
@@ -348,6 +400,23 @@ def test_reduce_planner_balances_rows_per_sm():
         assert (i["threads"], i["chunks_per_thread"], i["resident_ctas"]) == (192, 4, 3 * sms)
     i = bn.launch_info("reduce_norm", 4, 256, 5120)
     assert i["threads"] == 192 and i["resident_ctas"] == 2 * sms and i["grid"] == 256
+
+
+@pytest.mark.gpu
+def test_every_piece_has_a_launch_up_to_its_maximum():
+    """The unfused pieces serve rows the fused entry points decline: the
+    planner finds a launch (clusters of up to 16 CTAs) wherever
+    bn_supports_op accepts the shape."""
+    for H in (32776, 40960, 65536, 98304, 131072):
+        for R, k in ((1, 1), (8, 10), (16, 16)):
+            for T in (1, 7, 300, 5000):
+                for op in ("reduce_only", "norm_only", "residual_norm_only"):
+                    assert bn.supports_op(op, R, T, H)
+                    bn.launch_info(op, R, T, H)
+                for op in ("finalize_reduce_only", "finalize_only"):
+                    assert bn.supports_op(op, R, T, H, k)
+                    bn.launch_info(op, R, T, H, k)
+                    bn.launch_info(op, R, T, H, k, has_shared=False)
 
 
 @pytest.mark.gpu

@@ -34,12 +34,13 @@ EXPORTS = (
     "bn_last_error", "bn_status_string", "bn_version", "bn_set_tuning", "bn_query_launch",
     "bn_finalize_workspace_bytes", "bn_finalize_reduce_norm_ws",
     "bn_finalize_reduce_residual_norm_ws", "bn_finalize_reduce_norm_noalloc",
+    "bn_residual_norm_only", "bn_supports_op",
 )
 
 # bn_op values of the entry points, for launch_info()
 OPS = ("reduce_norm", "finalize_reduce_norm", "reduce_residual_norm",
        "finalize_reduce_residual_norm", "reduce_only", "finalize_reduce_only", "norm_only",
-       "finalize_only")
+       "finalize_only", "residual_norm_only")
 
 
 class BeamNormError(RuntimeError):
@@ -105,6 +106,8 @@ def load() -> ctypes.CDLL:
             "bn_reduce_only": [_P, _I, _I, _I, _P, _P],
             "bn_finalize_reduce_only": [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P],
             "bn_norm_only": [_P, _I, _I, _P, _P, _P, _F, _P, dbgp, _P],
+            "bn_residual_norm_only": [_P, _I, _I, _P, _P, _F, _P, dbgp, _P],
+            "bn_supports_op": [_I, _I, _I, _I, _I],
             "bn_finalize_only": [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P],
             "bn_supports": [_I, _I, _I, _I],
             "bn_check_device_error": [_P, ctypes.POINTER(ctypes.c_uint)],
@@ -179,10 +182,57 @@ def _with_device(t: torch.Tensor):
     return torch.cuda.device(t.device)
 
 
+# ---- the decline and its fallback ----------------------------------------------------
+#
+# A fused entry point that does not serve a shape declines: it returns
+# BN_ERR_UNSUPPORTED and enqueues nothing, so the whole reduction is still
+# owed.  With on_decline="fallback" the wrappers below then run the unfused
+# pieces, which serve larger rows: the deferred finalize is materialised
+# (finalize_only), the shards are summed (reduce_only), and the epilogue runs
+# on the FP32 sum (norm_only, or residual_norm_only for the single norm).  The
+# bits are those the fused call would give.  The temporaries (z, the FP32 sum)
+# are allocated here, on the call's stream.
+
+def _fallback_allowed(err: "BeamNormError", on_decline: str) -> bool:
+    if on_decline not in ("raise", "fallback"):
+        raise ValueError(f"on_decline must be 'raise' or 'fallback' (got {on_decline!r})")
+    return on_decline == "fallback" and err.status == ERR_UNSUPPORTED
+
+
+def _fallback(partials, z_inputs, residual, gamma_post, gamma_pre, eps, out, debug, stream,
+              single: bool):
+    ctx = torch.cuda.stream(stream) if hasattr(stream, "cuda_stream") else _nullctx()
+    with ctx:
+        if z_inputs is not None:
+            expert_out, perm, w, shared = z_inputs
+            partials = finalize_only(expert_out, perm, w, shared, stream=stream)
+            if debug is not None and debug.z is not None:
+                debug.z.copy_(partials)
+        s = reduce_only(partials, stream=stream)
+        if debug is not None and debug.sum is not None:
+            debug.sum.copy_(s)
+        dbg = Debug(ss=debug.ss) if debug is not None and debug.ss is not None else None
+        if single:
+            residual_norm_only(s, residual, gamma_pre, eps, out=out, debug=dbg, stream=stream)
+        else:
+            norm_only(s, residual, gamma_post, gamma_pre, eps, out=out, debug=dbg, stream=stream)
+    return out
+
+
+class _nullctx:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
 def reduce_norm(partials, residual, gamma_post, gamma_pre, eps: float, out=None,
-                debug: Optional[Debug] = None, stream=None) -> torch.Tensor:
+                debug: Optional[Debug] = None, stream=None,
+                on_decline: str = "raise") -> torch.Tensor:
     """Rank-ordered FP32 sum of the shards, post-RMSNorm, residual add (in
-    place), pre-RMSNorm.  Returns ``out`` (BF16 [T,H])."""
+    place), pre-RMSNorm.  Returns ``out`` (BF16 [T,H]).  ``on_decline="fallback"``:
+    a shape the fused kernel declines runs as the unfused pieces instead."""
     L = load()
     R, T, H = partials.shape
     dev = partials.device
@@ -195,7 +245,13 @@ def reduce_norm(partials, residual, gamma_post, gamma_pre, eps: float, out=None,
             _need(out, "out", torch.bfloat16, (T, H), dev))
     d = _debug(debug, R, T, H, dev, False)
     with _with_device(partials):
-        _check(L.bn_reduce_norm(*args, d[0] if d else None, _stream(partials, stream)))
+        try:
+            _check(L.bn_reduce_norm(*args, d[0] if d else None, _stream(partials, stream)))
+        except BeamNormError as e:
+            if not _fallback_allowed(e, on_decline):
+                raise
+            return _fallback(partials, None, residual, gamma_post, gamma_pre, eps, out, debug,
+                             stream, single=False)
     return out
 
 
@@ -227,11 +283,13 @@ def _workspace(ws, dev):
 
 def finalize_reduce_norm(expert_out, perm, w, shared, residual, gamma_post, gamma_pre, eps: float,
                          out=None, debug: Optional[Debug] = None, stream=None,
-                         workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+                         workspace: Optional[torch.Tensor] = None,
+                         on_decline: str = "raise") -> torch.Tensor:
     """Per-shard MoE top-k finalize (rounded to BF16), rank-ordered FP32 sum,
     post-RMSNorm, residual add (in place), pre-RMSNorm.  Returns ``out``.
     With a ``workspace`` (see ``finalize_workspace``) few token rows are each
-    spread over many CTAs; the results are the same."""
+    spread over many CTAs; the results are the same.  ``on_decline="fallback"``:
+    a declined shape materialises the finalize and runs the unfused pieces."""
     L = load()
     R, T, k = perm.shape
     H = expert_out.shape[-1]
@@ -248,13 +306,19 @@ def finalize_reduce_norm(expert_out, perm, w, shared, residual, gamma_post, gamm
             _need(out, "out", torch.bfloat16, (T, H), dev))
     d = _debug(debug, R, T, H, dev, True)
     with _with_device(expert_out):
-        if workspace is None:
-            _check(L.bn_finalize_reduce_norm(*args, d[0] if d else None,
-                                             _stream(expert_out, stream)))
-        else:
-            wp, wn = _workspace(workspace, dev)
-            _check(L.bn_finalize_reduce_norm_ws(*args, d[0] if d else None, wp, wn,
-                                                _stream(expert_out, stream)))
+        try:
+            if workspace is None:
+                _check(L.bn_finalize_reduce_norm(*args, d[0] if d else None,
+                                                 _stream(expert_out, stream)))
+            else:
+                wp, wn = _workspace(workspace, dev)
+                _check(L.bn_finalize_reduce_norm_ws(*args, d[0] if d else None, wp, wn,
+                                                    _stream(expert_out, stream)))
+        except BeamNormError as e:
+            if not _fallback_allowed(e, on_decline):
+                raise
+            return _fallback(None, (expert_out, perm, w, shared), residual, gamma_post, gamma_pre,
+                             eps, out, debug, stream, single=False)
     return out
 
 
@@ -294,8 +358,10 @@ def finalize_reduce_norm_noalloc(expert_out, perm, w, shared, residual, gamma_po
 
 
 def reduce_residual_norm(partials, residual, gamma, eps: float, out=None,
-                         debug: Optional[Debug] = None, stream=None) -> torch.Tensor:
-    """Rank-ordered sum, residual add (in place), RMSNorm; no post-norm."""
+                         debug: Optional[Debug] = None, stream=None,
+                         on_decline: str = "raise") -> torch.Tensor:
+    """Rank-ordered sum, residual add (in place), RMSNorm; no post-norm.
+    ``on_decline`` as for ``reduce_norm``."""
     L = load()
     R, T, H = partials.shape
     dev = partials.device
@@ -307,16 +373,23 @@ def reduce_residual_norm(partials, residual, gamma, eps: float, out=None,
             _need(out, "out", torch.bfloat16, (T, H), dev))
     d = _debug(debug, R, T, H, dev, False)
     with _with_device(partials):
-        _check(L.bn_reduce_residual_norm(*args, d[0] if d else None, _stream(partials, stream)))
+        try:
+            _check(L.bn_reduce_residual_norm(*args, d[0] if d else None,
+                                             _stream(partials, stream)))
+        except BeamNormError as e:
+            if not _fallback_allowed(e, on_decline):
+                raise
+            return _fallback(partials, None, residual, None, gamma, eps, out, debug, stream,
+                             single=True)
     return out
 
 
 def finalize_reduce_residual_norm(expert_out, perm, w, shared, residual, gamma, eps: float,
                                   out=None, debug: Optional[Debug] = None,
-                                  stream=None, workspace: Optional[torch.Tensor] = None
-                                  ) -> torch.Tensor:
+                                  stream=None, workspace: Optional[torch.Tensor] = None,
+                                  on_decline: str = "raise") -> torch.Tensor:
     """Per-shard finalize, rank-ordered sum, residual add (in place), RMSNorm.
-    ``workspace`` as for ``finalize_reduce_norm``."""
+    ``workspace`` and ``on_decline`` as for ``finalize_reduce_norm``."""
     L = load()
     R, T, k = perm.shape
     H = expert_out.shape[-1]
@@ -332,13 +405,19 @@ def finalize_reduce_residual_norm(expert_out, perm, w, shared, residual, gamma, 
             _need(out, "out", torch.bfloat16, (T, H), dev))
     d = _debug(debug, R, T, H, dev, True)
     with _with_device(expert_out):
-        if workspace is None:
-            _check(L.bn_finalize_reduce_residual_norm(*args, d[0] if d else None,
-                                                      _stream(expert_out, stream)))
-        else:
-            wp, wn = _workspace(workspace, dev)
-            _check(L.bn_finalize_reduce_residual_norm_ws(*args, d[0] if d else None, wp, wn,
-                                                         _stream(expert_out, stream)))
+        try:
+            if workspace is None:
+                _check(L.bn_finalize_reduce_residual_norm(*args, d[0] if d else None,
+                                                          _stream(expert_out, stream)))
+            else:
+                wp, wn = _workspace(workspace, dev)
+                _check(L.bn_finalize_reduce_residual_norm_ws(*args, d[0] if d else None, wp, wn,
+                                                             _stream(expert_out, stream)))
+        except BeamNormError as e:
+            if not _fallback_allowed(e, on_decline):
+                raise
+            return _fallback(None, (expert_out, perm, w, shared), residual, None, gamma, eps,
+                             out, debug, stream, single=True)
     return out
 
 
@@ -393,6 +472,25 @@ def norm_only(sum_, residual, gamma_post, gamma_pre, eps: float, out=None,
     return out
 
 
+def residual_norm_only(sum_, residual, gamma, eps: float, out=None,
+                       debug: Optional[Debug] = None, stream=None) -> torch.Tensor:
+    """The single-norm epilogue given the FP32 sum [T,H]: residual add (in
+    place) and RMSNorm."""
+    L = load()
+    T, H = sum_.shape
+    dev = sum_.device
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    args = (_need(sum_, "sum", torch.float32, (T, H), dev), T, H,
+            _need(residual, "residual", torch.bfloat16, (T, H), dev),
+            _need(gamma, "gamma", torch.float32, (H,), dev), float(eps),
+            _need(out, "out", torch.bfloat16, (T, H), dev))
+    d = _debug(debug, 1, T, H, dev, False)
+    with _with_device(sum_):
+        _check(L.bn_residual_norm_only(*args, d[0] if d else None, _stream(sum_, stream)))
+    return out
+
+
 def finalize_only(expert_out, perm, w, shared, z_out=None, stream=None) -> torch.Tensor:
     """The deferred finalize materialised: z [R,T,H] BF16 per shard, no reduction."""
     L = load()
@@ -414,6 +512,11 @@ def finalize_only(expert_out, perm, w, shared, z_out=None, stream=None) -> torch
 def supports(R: int, T: int, k: int, H: int) -> bool:
     """True if the fused entry points serve this shape (k = 0: reduce entries)."""
     return bool(load().bn_supports(int(R), int(T), int(k), int(H)))
+
+
+def supports_op(op: str, R: int, T: int, H: int, k: int = 0) -> bool:
+    """True if entry point ``op`` (a name of OPS) serves this shape."""
+    return bool(load().bn_supports_op(OPS.index(op), int(R), int(T), int(k), int(H)))
 
 
 def check_device_error(stream=None, raise_on_error: bool = True) -> int:

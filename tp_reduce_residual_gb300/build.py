@@ -1,7 +1,8 @@
 """Build libbeamnorm.so in-tree for sm_103a (GB300).
 
-Eight objects, one per kernel mode, are compiled from one template source in
-parallel, plus the small-T finalize object and the C-ABI object; everything
+Nine objects, one per kernel mode, are compiled from one template source in
+parallel, plus the small-T finalize object, the static-scratch object and the
+C-ABI object; everything
 is compiled with ``-fmad=false`` so that the FP32 epilogue is never
 contracted into FMAs ("Fuse Beam's TP all-reduce with its sandwich norms",
 "Details", "Build" bullet).  nvcc cross-compiles without a GPU.  The result is
@@ -43,6 +44,7 @@ MODES = {
     "fin_reduce_only": 1 | 16,
     "norm_only": 2 | 4 | 8,
     "fin_only": 1 | 32,
+    "resnorm_only": 2 | 8,
 }
 
 SOURCES = ["bn_device.cuh", "bn_internal.h", "bn_kernels.cu", "bn_abi.cu", "bn_wide.h",

@@ -133,9 +133,16 @@ bn_status check_shape(int R, int T, int k, int H, bool fin)
     return BN_OK;
 }
 
-bn_status check_served(int R, int T, int k, int H, bool fin)
+// A valid shape that is not served is declined.  The fused entry points serve
+// rows up to kMaxH; the unfused pieces, which the caller falls back to when a
+// fused call declines, split a row over clusters of up to 16 CTAs and serve
+// rows up to kMaxPieceH.
+bn_status check_served(int R, int T, int k, int H, bool fin, bool piece = false)
 {
-    if (H > kMaxH) return fail(BN_ERR_UNSUPPORTED, "H=%d above the served maximum %d", H, kMaxH);
+    const int max_h = piece ? kMaxPieceH : kMaxH;
+    if (H > max_h)
+        return fail(BN_ERR_UNSUPPORTED, "H=%d above the served maximum %d of the %s", H, max_h,
+                    piece ? "unfused pieces" : "fused entry points");
     if (fin && R * k > kMaxMeta)
         return fail(BN_ERR_UNSUPPORTED, "R*k=%d above the served maximum %d", R * k, kMaxMeta);
     if (fin && (long long)T * k >= (1LL << 31))
@@ -200,7 +207,18 @@ const ModeOps kOps[] = {
     {kModeFinReduceOnly, launch_fin_reduce_only, occupancy_fin_reduce_only, "finalize_reduce_only"},
     {kModeNormOnly, launch_norm_only, occupancy_norm_only, "norm_only"},
     {kModeFinOnly, launch_fin_only, occupancy_fin_only, "finalize_only"},
+    {kModeResNormOnly, launch_resnorm_only, occupancy_resnorm_only, "residual_norm_only"},
 };
+
+// The operations of bn_op, in its order.
+const int kModeOfOp[] = {kModeReduceNorm,       kModeFinReduceNorm, kModeReduceResNorm,
+                         kModeFinReduceResNorm, kModeReduceOnly,    kModeFinReduceOnly,
+                         kModeNormOnly,         kModeFinOnly,       kModeResNormOnly};
+constexpr int kNumOps = (int)(sizeof kModeOfOp / sizeof kModeOfOp[0]);
+
+// The unfused pieces: the modes that write the FP32 sum or the finalize
+// results, or that start from the FP32 sum.
+bool is_piece(int mode) { return (mode & (F_SUM_OUT | F_Z_OUT | F_SUM_IN)) != 0; }
 
 const ModeOps &ops_for(int mode)
 {
@@ -919,7 +937,7 @@ bn_status bn_reduce_only(const uint16_t *partials, int R, int T, int H, float *s
     BN_TRY(check_ptr16(sum_out, "sum_out"));
     writes[nw++] = Range{sum_out, (size_t)T * H * 4, "sum_out"};
     BN_TRY(check_overlaps(writes, nw, reads, nr));
-    BN_TRY(check_served(R, T, 1, H, false));
+    BN_TRY(check_served(R, T, 1, H, false, true));
     Args a = base_args(R, T, 0, H, 0.f);
     a.src = partials;
     a.sum_out = sum_out;
@@ -939,7 +957,7 @@ bn_status bn_finalize_reduce_only(const uint16_t *expert_out, const int32_t *per
     BN_TRY(check_ptr16(sum_out, "sum_out"));
     writes[nw++] = Range{sum_out, (size_t)T * H * 4, "sum_out"};
     BN_TRY(check_overlaps(writes, nw, reads, nr));
-    BN_TRY(check_served(R, T, k, H, true));
+    BN_TRY(check_served(R, T, k, H, true, true));
     Args a = base_args(R, T, k, H, 0.f);
     a.src = expert_out;
     a.perm = perm;
@@ -966,7 +984,7 @@ bn_status bn_norm_only(const float *sum, int T, int H, uint16_t *residual, const
         writes[nw++] = Range{dbg->ss, (size_t)T * 8, "dbg->ss"};
     }
     BN_TRY(check_overlaps(writes, nw, reads, nr));
-    BN_TRY(check_served(1, T, 1, H, false));
+    BN_TRY(check_served(1, T, 1, H, false, true));
     Args a = base_args(1, T, 0, H, eps);
     a.sum_in = sum;
     a.residual = residual;
@@ -975,6 +993,34 @@ bn_status bn_norm_only(const float *sum, int T, int H, uint16_t *residual, const
     a.out = out;
     if (dbg) a.ss_out = dbg->ss;
     return run(kModeNormOnly, a, stream);
+}
+
+bn_status bn_residual_norm_only(const float *sum, int T, int H, uint16_t *residual,
+                                const float *gamma, float eps, uint16_t *out, const bn_debug *dbg,
+                                void *stream)
+{
+    g_msg[0] = '\0';
+    BN_TRY(check_shape(1, T, 1, H, false));
+    if (T == 0) return BN_OK;  // nothing is read or written; pointers are not examined
+    Range reads[8], writes[8];
+    int nr = 0, nw = 0;
+    BN_TRY(check_ptr16(sum, "sum"));
+    reads[nr++] = Range{sum, (size_t)T * H * 4, "sum"};
+    BN_TRY(check_epilogue(residual, gamma, gamma, out, eps, T, H, reads, &nr, writes, &nw));
+    if (dbg && dbg->ss) {
+        BN_TRY(check_ptr16(dbg->ss, "dbg->ss"));
+        writes[nw++] = Range{dbg->ss, (size_t)T * 8, "dbg->ss"};
+    }
+    BN_TRY(check_overlaps(writes, nw, reads, nr));
+    BN_TRY(check_served(1, T, 1, H, false, true));
+    Args a = base_args(1, T, 0, H, eps);
+    a.sum_in = sum;
+    a.residual = residual;
+    a.gamma_post = gamma;
+    a.gamma_pre = gamma;
+    a.out = out;
+    if (dbg) a.ss_out = dbg->ss;
+    return run(kModeResNormOnly, a, stream);
 }
 
 bn_status bn_finalize_only(const uint16_t *expert_out, const int32_t *perm, const float *w,
@@ -990,7 +1036,7 @@ bn_status bn_finalize_only(const uint16_t *expert_out, const int32_t *perm, cons
     BN_TRY(check_ptr16(z_out, "z_out"));
     writes[nw++] = Range{z_out, (size_t)R * T * H * 2, "z_out"};
     BN_TRY(check_overlaps(writes, nw, reads, nr));
-    BN_TRY(check_served(R, T, k, H, true));
+    BN_TRY(check_served(R, T, k, H, true, true));
     Args a = base_args(R, T, k, H, 0.f);
     a.src = expert_out;
     a.perm = perm;
@@ -1005,6 +1051,18 @@ int bn_supports(int R, int T, int k, int H)
     const bool fin = k > 0;
     if (check_shape(R, T, fin ? k : 1, H, fin) != BN_OK) return 0;
     if (check_served(R, T, fin ? k : 1, H, fin) != BN_OK) return 0;
+    g_msg[0] = '\0';
+    return 1;
+}
+
+int bn_supports_op(bn_op op, int R, int T, int k, int H)
+{
+    if ((int)op < 0 || (int)op >= kNumOps) return 0;
+    const int mode = kModeOfOp[(int)op];
+    const bool fin = (mode & F_FIN) != 0;
+    if (mode & F_SUM_IN) R = 1;  // the epilogue pieces read one FP32 row
+    if (check_shape(R, T, fin ? k : 1, H, fin) != BN_OK) return 0;
+    if (check_served(R, T, fin ? k : 1, H, fin, is_piece(mode)) != BN_OK) return 0;
     g_msg[0] = '\0';
     return 1;
 }
@@ -1093,17 +1151,13 @@ bn_status bn_query_launch(bn_op op, int R, int T, int k, int H, int has_shared,
     g_msg[0] = '\0';
     BN_REQUIRE(info != nullptr, "info is NULL");
     std::memset(info, 0, sizeof *info);
-    static const int kModeOf[] = {kModeReduceNorm,    kModeFinReduceNorm, kModeReduceResNorm,
-                                  kModeFinReduceResNorm, kModeReduceOnly, kModeFinReduceOnly,
-                                  kModeNormOnly,      kModeFinOnly};
-    BN_REQUIRE((int)op >= 0 && (int)op < (int)(sizeof kModeOf / sizeof kModeOf[0]),
-               "op=%d is not an operation", (int)op);
-    const int mode = kModeOf[(int)op];
+    BN_REQUIRE((int)op >= 0 && (int)op < kNumOps, "op=%d is not an operation", (int)op);
+    const int mode = kModeOfOp[(int)op];
     const bool fin = (mode & F_FIN) != 0;
     if (mode & F_SUM_IN) R = 1;  // norm_only reads one FP32 row
     BN_TRY(check_shape(R, T, fin ? k : 1, H, fin));
     if (T == 0) return BN_OK;
-    BN_TRY(check_served(R, T, fin ? k : 1, H, fin));
+    BN_TRY(check_served(R, T, fin ? k : 1, H, fin, is_piece(mode)));
     Args a = base_args(R, T, fin ? k : 0, H, 0.f);
     // only the presence of the shared rows matters to the shape; the address
     // is a marker that is never dereferenced (nothing is launched)

@@ -27,11 +27,13 @@ constexpr int kModeReduceOnly = F_SUM_OUT;
 constexpr int kModeFinReduceOnly = F_FIN | F_SUM_OUT;
 constexpr int kModeNormOnly = F_SUM_IN | F_POSTNORM | F_RESNORM;
 constexpr int kModeFinOnly = F_FIN | F_Z_OUT;
+constexpr int kModeResNormOnly = F_SUM_IN | F_RESNORM;
 
 constexpr int kMaxR = 16;
 constexpr int kMaxK = 16;
 constexpr int kMaxMeta = 256;        // R * k slots staged per token row
-constexpr int kMaxH = 32768;
+constexpr int kMaxH = 32768;         // fused entry points (whole-row epilogue in one launch)
+constexpr int kMaxPieceH = 131072;   // unfused pieces (the fallback when a fused call declines)
 constexpr int kMaxConsumers = 512;   // consumer threads per CTA
 constexpr int kMaxStages = 64;
 constexpr int kMaxCluster = 16;
@@ -122,6 +124,7 @@ BN_DECLARE_MODE(reduce_only)
 BN_DECLARE_MODE(fin_reduce_only)
 BN_DECLARE_MODE(norm_only)
 BN_DECLARE_MODE(fin_only)
+BN_DECLARE_MODE(resnorm_only)
 #undef BN_DECLARE_MODE
 
 }  // namespace bn

@@ -1,7 +1,7 @@
 // bn_kernels.cu -- instantiates the kernel template for one mode.
 //
 // Compiled once per mode with -DBN_MODE_NAME=<name> -DBN_MODE_VALUE=<bits>
-// (the build compiles the eight modes as eight objects in parallel), always
+// (the build compiles the nine modes as nine objects in parallel), always
 // with -fmad=false: the FP32 epilogue must not be contracted into FMAs
 // ("Fuse Beam's TP all-reduce with its sandwich norms", "Details", "Build").
 #include <cuda_runtime.h>
