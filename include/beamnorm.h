@@ -155,8 +155,11 @@ BN_API bn_status bn_finalize_reduce_residual_norm(const uint16_t *expert_out, co
 /* Bytes of workspace with which bn_finalize_reduce_norm_ws and
  * bn_finalize_reduce_residual_norm_ws spread each token row over many CTAs,
  * or 0 when that path does not serve the shape (it serves 1 <= T <= 8 and
- * H <= 8192, where one CTA or one cluster per token row leaves most SMs idle).  Pure host logic: the counters (T words, padded to 256 bytes)
- * then the per-shard BF16 finalize results [T, R, H]. */
+ * H <= 8192, where one CTA or one cluster per token row leaves most SMs
+ * idle).  Pure host logic.  Layout: the counters (T words, padded to 256
+ * bytes), then the per-shard BF16 finalize results [T, R, H].
+ * Source: "Fuse Beam's TP all-reduce with its sandwich norms", "Details"
+ * (the fused op runs on a workspace sized for the shapes it serves). */
 BN_API size_t bn_finalize_workspace_bytes(int R, int T, int k, int H);
 
 /* bn_finalize_reduce_norm with a workspace.
@@ -173,7 +176,9 @@ BN_API size_t bn_finalize_workspace_bytes(int R, int T, int k, int H);
  * The results are those of bn_finalize_reduce_norm: the same per-shard BF16
  * rounding, rank-ordered FP32 sum and norms.  The workspace must not overlap
  * any other buffer of the call (BN_ERR_INVALID).
- * Sources: as bn_finalize_reduce_norm. */
+ * Sources: "Fuse Beam's TP all-reduce with its sandwich norms", "Claims" and
+ * "Details" (the fused op's workspace); sglang pull request 34134,
+ * description. */
 BN_API bn_status bn_finalize_reduce_norm_ws(const uint16_t *expert_out, const int32_t *perm,
                                      const float *w, const uint16_t *shared,
                                      int R, int T, int k, int H,
@@ -222,7 +227,8 @@ BN_API bn_status bn_finalize_reduce_residual_norm_ws(const uint16_t *expert_out,
  *     (different streams without ordering between them) race on the scratch
  *     and give wrong results: order them, or give them bn_finalize_reduce_norm_ws
  *     with a workspace each.
- * The pages describe no such entry point: it has no counterpart there. */
+ * Source: none -- the pages describe no such entry point; it has no
+ * counterpart there. */
 BN_API bn_status bn_finalize_reduce_norm_noalloc(const uint16_t *expert_out,
                                                  const int32_t *perm, const float *w,
                                                  const uint16_t *shared, int R, int T, int k,
@@ -233,11 +239,17 @@ BN_API bn_status bn_finalize_reduce_norm_noalloc(const uint16_t *expert_out,
 
 /* ---- unfused pieces (the decline / fallback path and its measurement) --- */
 
-/* Rank-ordered FP32 sum only: sum_out [T, H] FP32 = s. */
+/* Rank-ordered FP32 sum only: sum_out [T, H] FP32 = s.  Rows up to H = 131072.
+ * Source: "Fuse Beam's TP all-reduce with its sandwich norms", "Claims" (the
+ * all-reduce the epilogue follows); sglang pull request 34134, description
+ * (the unfused path a declined call falls back to). */
 BN_API bn_status bn_reduce_only(const uint16_t *partials, int R, int T, int H,
                          float *sum_out, void *stream);
 
-/* Per-shard finalize rounded to BF16, then the rank-ordered FP32 sum only. */
+/* Per-shard finalize rounded to BF16, then the rank-ordered FP32 sum only.
+ * Rows up to H = 131072.
+ * Source: "Fuse Beam's TP all-reduce with its sandwich norms", "Claims" (the
+ * finalize before the reduction keeps each shard's BF16 rounding). */
 BN_API bn_status bn_finalize_reduce_only(const uint16_t *expert_out, const int32_t *perm,
                                   const float *w, const uint16_t *shared,
                                   int R, int T, int k, int H, float *sum_out,
@@ -245,7 +257,9 @@ BN_API bn_status bn_finalize_reduce_only(const uint16_t *expert_out, const int32
 
 /* The sandwich epilogue given the FP32 sum [T, H] (post-norm, residual add,
  * pre-norm).  Together with bn_reduce_only / bn_finalize_reduce_only it gives
- * the same bits as the fused entry points. */
+ * the same bits as the fused entry points.  Rows up to H = 131072.
+ * Source: "Fuse Beam's TP all-reduce with its sandwich norms", "Claims" (the
+ * FP32 norm-residual-norm epilogue). */
 BN_API bn_status bn_norm_only(const float *sum, int T, int H, uint16_t *residual,
                        const float *gamma_post, const float *gamma_pre, float eps,
                        uint16_t *out, const bn_debug *dbg, void *stream);
@@ -272,22 +286,37 @@ BN_API bn_status bn_finalize_only(const uint16_t *expert_out, const int32_t *per
 /* ---- queries and errors ------------------------------------------------ */
 
 /* 1 if the fused entry points serve this shape (k = 0 for the reduce-only
- * entries), 0 if the caller must fall back.  Pure host logic. */
+ * entries), 0 if the caller must fall back.  Pure host logic.
+ * Source: "Fuse Beam's TP all-reduce with its sandwich norms", "Details"
+ * (the fused op declines shapes it does not serve). */
 BN_API int bn_supports(int R, int T, int k, int H);
 
 /* Synchronises `stream`, reads the device-side error bits of the current
  * device into *bits (nullable), clears them, and returns BN_ERR_DEVICE if any
- * bit was set, BN_ERR_CUDA if the synchronisation failed, else BN_OK. */
+ * bit was set, BN_ERR_CUDA if the synchronisation failed, else BN_OK.
+ * Source: sglang pull request 34134, NextN follow-up (a path that cannot do
+ * its work fails loudly rather than silently). */
 BN_API bn_status bn_check_device_error(void *stream, unsigned *bits);
 
-/* Message describing the last failure on the calling thread ("" if none). */
+/* Message describing the last failure on the calling thread ("" if none).
+ * Source: no passage: library utility. */
 BN_API const char *bn_last_error(void);
 
-/* Name of a status code. */
+/* Name of a status code.
+ * Source: no passage: library utility. */
 BN_API const char *bn_status_string(bn_status status);
 
-/* Library version, major * 10000 + minor * 100 + patch. */
+/* Library version, major * 10000 + minor * 100 + patch.
+ * Source: no passage: library utility. */
 BN_API int bn_version(void);
+
+/* Does nothing, and may be called at any time.  The library allocates no
+ * memory it would have to release: its device state (the error word, the
+ * static scratch of bn_finalize_reduce_norm_noalloc) is static device memory,
+ * released with the CUDA context; the host state is static too.  Provided so
+ * that a caller can pair it with the first call.
+ * Source: no passage: library utility. */
+BN_API void bn_shutdown(void);
 
 /* Launch-shape overrides for measurement sweeps (process-wide).  Every field
  * 0 means automatic.  Results do not depend on these settings, only speed. */
@@ -315,7 +344,8 @@ typedef struct {
 } bn_tuning;
 
 /* Set the overrides; NULL restores automatic choices.  BN_ERR_INVALID on an
- * out-of-range field (nothing changes then). */
+ * out-of-range field (nothing changes then).
+ * Source: no passage: library utility (measurement sweeps and tests). */
 BN_API bn_status bn_set_tuning(const bn_tuning *tuning);
 
 /* The operations of the entry points above, for bn_query_launch. */
@@ -350,7 +380,8 @@ typedef struct {
  * k is ignored by the operations without a finalize; has_shared says whether
  * the finalize call would pass a shared-expert row.  Shape errors and
  * declines are reported as by the entry point itself; T == 0 gives BN_OK and
- * an all-zero *info (no launch).  Needs a CUDA device (occupancy queries). */
+ * an all-zero *info (no launch).  Needs a CUDA device (occupancy queries).
+ * Source: no passage: library utility (measurement sweeps and tests). */
 BN_API bn_status bn_query_launch(bn_op op, int R, int T, int k, int H, int has_shared,
                                  bn_launch_info *info);
 

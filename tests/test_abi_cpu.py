@@ -38,6 +38,20 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, name), name
 
 
+def test_every_declaration_cites_its_passage():
+    """Each entry point's comment names the passage that defines it, or says
+    that none does ("no passage: library utility", "no counterpart")."""
+    text = open(HEADER).read()
+    for m in re.finditer(r"/\*((?:(?!\*/).)*)\*/\s*BN_API\s+[\w\s\*]+?\b(bn_\w+)\s*\(", text, re.S):
+        comment, name = " ".join(m.group(1).replace("*", " ").split()), m.group(2)
+        assert re.search(r"Sources?:", comment), f"{name}: no Source line"
+        assert ("pull request" in comment or "sandwich norms" in comment
+                or "no passage" in comment or "no counterpart" in comment), \
+            f"{name}: the Source line names no page"
+    cited = set(re.findall(r"\*/\s*BN_API\s+[\w\s\*]+?\b(bn_\w+)\s*\(", text))
+    assert cited == set(declared_symbols()), set(declared_symbols()) - cited
+
+
 def test_library_is_built_for_sm103a():
     # the build passes exactly one -gencode, for sm_103a
     assert nbuild.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -34,7 +34,7 @@ EXPORTS = (
     "bn_last_error", "bn_status_string", "bn_version", "bn_set_tuning", "bn_query_launch",
     "bn_finalize_workspace_bytes", "bn_finalize_reduce_norm_ws",
     "bn_finalize_reduce_residual_norm_ws", "bn_finalize_reduce_norm_noalloc",
-    "bn_residual_norm_only", "bn_supports_op",
+    "bn_residual_norm_only", "bn_supports_op", "bn_shutdown",
 )
 
 # bn_op values of the entry points, for launch_info()
@@ -128,6 +128,8 @@ def load() -> ctypes.CDLL:
             fn = getattr(L, name)
             fn.argtypes = args
             fn.restype = _I
+        L.bn_shutdown.argtypes = []
+        L.bn_shutdown.restype = None
         L.bn_finalize_workspace_bytes.restype = ctypes.c_size_t
         L.bn_last_error.restype = ctypes.c_char_p
         L.bn_status_string.restype = ctypes.c_char_p

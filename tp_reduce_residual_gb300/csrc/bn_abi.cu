@@ -1108,6 +1108,8 @@ const char *bn_status_string(bn_status status)
 
 int bn_version(void) { return kVersion; }
 
+void bn_shutdown(void) {}
+
 bn_status bn_set_tuning(const bn_tuning *t)
 {
     g_msg[0] = '\0';

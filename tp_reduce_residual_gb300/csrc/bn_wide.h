@@ -44,7 +44,7 @@ inline size_t wide_workspace_bytes(int R, int T, int H)
 
 // Enqueue the kernel: grid T * parts CTAs of kWideThreads threads.  postnorm
 // selects the sandwich (post-RMSNorm before the residual add) or the single
-// pre-RMSNorm; cpt is the epilogue's chunks per thread (1, 2 or 4).
+// pre-RMSNorm; cpt is the epilogue's chunks per thread (1 or 2, kWideMaxCpt).
 cudaError_t launch_wide(const WideArgs &w, bool postnorm, int cpt, bool pdl, cudaStream_t st);
 
 // Size of the library-owned scratch behind bn_finalize_reduce_norm_noalloc
