@@ -329,7 +329,9 @@ typedef struct {
     int wait_mode;     /* 1: suspending try_wait, 2: polling test_wait */
     int group;         /* row copies per pipeline stage, at most 64; the finalize
                           modes only (the other modes carry one copy a stage) */
-    int split;         /* finalize rows: 1 split by columns, 2 split by shard */
+    int split;         /* finalize rows: 1 split by columns, 2 split by shard,
+                          3 one cluster per row with one (shard, chunk) task per
+                          thread (the fused finalize entries) */
     int dependent_launch; /* 1: plain stream order, 2: programmatic dependent
                              launch (the launch and the kernel's setup overlap
                              the previous kernel in the stream) */
@@ -363,7 +365,10 @@ typedef enum {
 
 /* The launch shape one call would use on the current device. */
 typedef struct {
-    int split;                /* 1: a cluster of R CTAs splits each row by shard */
+    int split;                /* 1: a cluster splits each row by shard; 2: a cluster
+                                 splits each row by column slices with one
+                                 (shard, chunk) finalize task per thread, and
+                                 chunks_per_thread is then the tasks per thread */
     int cluster_size;         /* CTAs per token row */
     int threads;              /* threads per CTA: consumer threads + one producer warp */
     int chunks_per_thread;    /* 16-byte chunks of the CTA's slice per consumer thread */

@@ -192,7 +192,7 @@ def test_set_tuning_validates(L):
     assert st(0, 0, 0, 9, 0, 0) == bn.ERR_INVALID
     assert st(0, 0, 0, 0, 3, 0) == bn.ERR_INVALID
     assert st(0, 0, 0, 0, 0, 65) == bn.ERR_INVALID
-    assert st(0, 0, 0, 0, 0, 0, 3) == bn.ERR_INVALID
+    assert st(0, 0, 0, 0, 0, 0, 4) == bn.ERR_INVALID
     assert st(0, 0, 0, 0, 0, 0, 0, 3) == bn.ERR_INVALID
     assert st(0, 0, 0, 0, 0, 0, 0, 0, -1) == bn.ERR_INVALID
     assert st(16, 8, 256, 2, 2, 4, 2, 1) == bn.OK

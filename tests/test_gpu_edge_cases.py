@@ -117,8 +117,10 @@ def test_finalize_edge_cases_match_oracle(R, k, H, with_shared, single):
 
 
 @pytest.mark.parametrize("tuning", [dict(split=1, cluster_size=1), dict(split=1, cluster_size=4),
-                                    dict(split=2, cluster_size=2), dict(cluster_size=8)],
-                         ids=["one-CTA", "columns-x4", "shards-x2", "cluster-x8"])
+                                    dict(split=2, cluster_size=2), dict(cluster_size=8),
+                                    dict(split=3, cluster_size=16), dict(split=3, cluster_size=2)],
+                         ids=["one-CTA", "columns-x4", "shards-x2", "cluster-x8", "tasks-x16",
+                              "tasks-x2"])
 def test_edge_cases_on_every_row_split(tuning):
     """The same rows through the column split (1 or 4 CTAs a row), the shard
     split and an 8-CTA cluster: the cluster exchanges carry infinite and NaN

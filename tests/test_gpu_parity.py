@@ -362,10 +362,15 @@ def test_launch_query_is_coherent(op, R, T, k, H):
     assert i["threads"] % 32 == 0 and 64 <= i["threads"] <= 512 + 32
     assert i["grid"] > 0 and i["grid"] % i["cluster_size"] == 0
     assert i["grid"] // i["cluster_size"] <= T
-    assert i["stages"] >= 2 and i["stage_bytes"] % 128 == 0 and i["group"] >= 1
+    if i["split"] == 2:
+        # one cluster per row, one (shard, chunk) task per thread: no pipeline
+        assert op.startswith("finalize") and i["grid"] == T * i["cluster_size"]
+        assert i["chunks_per_thread"] in (1, 2) and i["stages"] == 0
+    else:
+        assert i["stages"] >= 2 and i["stage_bytes"] % 128 == 0 and i["group"] >= 1
     assert i["resident_ctas"] >= i["grid"]
     assert i["smem_bytes"] <= props.shared_memory_per_block_optin
-    if i["split"]:
+    if i["split"] == 1:
         assert op.startswith("finalize") and R % i["cluster_size"] == 0
     try:
         bn.set_tuning(stages=2, split=1 if op.startswith("finalize") else 0)
@@ -474,6 +479,69 @@ def test_shard_split_matches_column_split_and_oracle(R, T, k, H, with_shared, si
         for key in ("sum", "ss", "z", "out", "residual_out"):
             assert_bits_equal(g[key], base[key], f"cs={c} {key}")
     parity.compare(base, parity.run_oracle(d, single=single), what=f"split R={R} T={T} k={k} H={H}")
+
+
+CLUSTER_TASKS = [
+    # (R, T, k, H, with_shared, single, cluster size)
+    (8, 1, 10, 8192, True, False, 16),
+    (8, 4, 10, 8192, True, False, 16),
+    (8, 8, 10, 8192, False, False, 8),
+    (8, 3, 8, 6144, True, True, 16),
+    (2, 7, 3, 1000, True, False, 4),      # 125 chunks: slices of 31 and 32 chunks
+    (16, 3, 16, 4096, True, False, 8),    # R*k = 256, two tasks per thread
+    (1, 5, 1, 64, False, False, 2),
+    (3, 40, 5, 2048, True, True, 16),     # more rows than resident clusters
+]
+
+
+@pytest.mark.parametrize("R,T,k,H,with_shared,single,cs", CLUSTER_TASKS)
+def test_cluster_task_split_matches_oracle(R, T, k, H, with_shared, single, cs):
+    """A cluster of cs CTAs per row, one (shard, chunk) finalize task per
+    thread, each CTA's finalize results summed and normalised on its column
+    slice, the sums of squares exchanged across the cluster: the bits of the
+    other row splits and the oracle's results."""
+    wl = inputs.custom("finalize_reduce_norm", R, H, k, partial_std=0.3, shared_std=0.3)
+    d = parity.gpu_inputs(wl, T, seed=800 + R * 13 + T, with_shared=with_shared)
+    op = "finalize_reduce_residual_norm" if single else "finalize_reduce_norm"
+    try:
+        bn.set_tuning(split=3, cluster_size=cs)
+        info = bn.launch_info(op, R, T, H, k, has_shared=with_shared)
+        assert info["split"] == 2 and info["cluster_size"] == cs, info
+        assert info["grid"] == T * cs
+        g = parity.run_fused(d, single=single)
+    finally:
+        bn.set_tuning()
+    base = parity.run_fused(d, single=single)
+    for key in ("sum", "z"):
+        assert_bits_equal(g[key], base[key], key)
+    parity.compare(g, parity.run_oracle(d, single=single), what=f"cluster tasks R={R} T={T} H={H}")
+
+
+def test_cluster_task_split_flags_bad_perm_and_stays_in_bounds():
+    R, T, k, H = 4, 5, 3, 1000
+    wl = inputs.custom("finalize_reduce_norm", R, H, k, partial_std=0.3)
+    d = parity.gpu_inputs(wl, T, seed=5)
+    bad = d["perm"].clone()
+    bad[1, 2, 0] = T * k + 3
+    ob, out, og = parity.guarded(T * H, torch.bfloat16)
+    sb, s, sg = parity.guarded(T * H, torch.float32)
+    qb, ss, qg = parity.guarded(T * 2, torch.float32)
+    zb, z, zg = parity.guarded(R * T * H, torch.bfloat16)
+    rb, res, rg = parity.guarded(T * H, torch.bfloat16)
+    res.copy_(d["residual"].reshape(-1))
+    try:
+        bn.set_tuning(split=3, cluster_size=8)
+        bn.finalize_reduce_norm(d["expert_out"], bad, d["w"], d["shared"], res.view(T, H),
+                                d["gamma_post"], d["gamma_pre"], d["eps"], out=out.view(T, H),
+                                debug=bn.Debug(sum=s.view(T, H), ss=ss.view(T, 2), z=z.view(R, T, H)))
+        assert bn.check_device_error(raise_on_error=False) == bn.DEVERR_PERM_RANGE
+    finally:
+        bn.set_tuning()
+    for buf, gd, n in ((ob, og, T * H), (sb, sg, T * H), (qb, qg, T * 2), (zb, zg, R * T * H),
+                       (rb, rg, T * H)):
+        assert parity.guard_intact(buf, gd, n)
+    assert not torch.isnan(out.float()).any() and not torch.isnan(s).any()
+    assert not torch.isnan(z.float()).any() and not torch.isnan(ss).any()
 
 
 @pytest.mark.parametrize("cs", [8, 4, 2])

@@ -48,7 +48,7 @@ MODES = {
 }
 
 SOURCES = ["bn_device.cuh", "bn_internal.h", "bn_kernels.cu", "bn_abi.cu", "bn_wide.h",
-           "bn_wide.cu", "bn_noalloc.cu"]
+           "bn_wide.cu", "bn_noalloc.cu", "bn_cluster.h", "bn_cluster.cu"]
 
 
 def nvcc() -> str:
@@ -99,6 +99,9 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int = 0) -> st
     wide_obj = os.path.join(OUT_DIR, "bn_wide.o")
     cmds.append([cc, *ARCH, *NVCC_FLAGS, *extra, *inc, "-c", os.path.join(CSRC, "bn_wide.cu"),
                  "-o", wide_obj])
+    cluster_obj = os.path.join(OUT_DIR, "bn_cluster.o")
+    cmds.append([cc, *ARCH, *NVCC_FLAGS, *extra, *inc, "-c", os.path.join(CSRC, "bn_cluster.cu"),
+                 "-o", cluster_obj])
     noalloc_obj = os.path.join(OUT_DIR, "bn_noalloc.o")
     cmds.append([cc, *ARCH, *NVCC_FLAGS, *inc, "-c", os.path.join(CSRC, "bn_noalloc.cu"),
                  "-o", noalloc_obj])

@@ -18,6 +18,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/beamnorm.h"
+#include "bn_cluster.h"
 #include "bn_internal.h"
 #include "bn_wide.h"
 
@@ -553,9 +554,79 @@ bn_status plan(int mode, Args *a, Launch *l)
     return fail(BN_ERR_UNSUPPORTED, "no resident CTA for this shape");
 }
 
+// ---- the finalize with each row over a cluster, one task per thread --------------
+
+// Token rows up to which the fused finalize entries take the cluster path
+// when the planner leaves the choice to it, provided the clusters of all T
+// rows fit on the device at once.  Measured on GB300 (us per call in a CUDA
+// graph, L2-cold; cluster path with 16 CTAs a row / the default of the day):
+// R=8, H=8192, k=10 at T=1 5.67 / 10.28 (shard split), T=4 6.75 / 10.47,
+// T=16 20.5 / 14.3 (16-CTA clusters take two waves; with 8-CTA clusters
+// 19.5); R=8, H=6144, k=8 at T=1 5.07 / 8.85, T=16 18.4 / 12.1.
+constexpr int kClusterFinMaxT = 8;
+
+struct ClusterPlan {
+    int cs, tpt, resident;
+    size_t smem;
+};
+
+// The largest cluster (16, 8, 4 or 2 CTAs) whose CTAs take at most two
+// (shard, chunk) tasks per thread and whose clusters the device holds at once
+// for the T rows (on request, any cluster that is resident at all).
+bool plan_cluster_fin(int mode, const Args &a, const DeviceInfo *d, ClusterPlan *p)
+{
+    if (mode != kModeFinReduceNorm && mode != kModeFinReduceResNorm) return false;
+    const int pref = g_tune_split.load();
+    if (pref != 0 && pref != 3) return false;
+    if (pref == 0 && a.T > kClusterFinMaxT) return false;
+    const int want_cs = g_tune_cluster.load();
+    const int nch = a.H / 8;
+    for (int cs = kMaxCluster; cs >= 2; cs /= 2) {
+        if (want_cs > 0 && cs != want_cs) continue;
+        const int slice = (nch + cs - 1) / cs;
+        if (nch < cs || slice > kClusterThreads) continue;
+        const int tasks = a.R * slice;
+        const int tpt = (tasks + kClusterThreads - 1) / kClusterThreads;
+        if (tpt > kClusterMaxTpt) continue;
+        const size_t smem = cluster_smem_bytes(a.R, slice);
+        if ((long long)smem > (long long)d->smem_optin - 2048) continue;
+        cudaError_t e = cudaSuccess;
+        const int res = cluster_fin_resident((mode & F_POSTNORM) != 0, tpt, cs, smem, &e);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (res <= 0 || (pref == 0 && res < a.T)) continue;
+        *p = ClusterPlan{cs, tpt, res, smem};
+        return true;
+    }
+    return false;
+}
+
+bn_status run_cluster_fin(int mode, Args &a, const DeviceInfo *d, const ClusterPlan &cp,
+                          void *stream)
+{
+    a.nchunks = a.H / 8;
+    a.err = d->err;
+    ClusterArgs c;
+    c.a = a;
+    c.tasks = a.R * ((a.nchunks + cp.cs - 1) / cp.cs);
+    const cudaError_t e = launch_cluster_fin(c, (mode & F_POSTNORM) != 0, cp.tpt, cp.cs,
+                                             g_tune_pdl.load() != 1,
+                                             reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "bn_cluster_fin_kernel");
+    return BN_OK;
+}
+
 bn_status run(int mode, Args &a, void *stream)
 {
     if (a.T == 0) return BN_OK;
+    {
+        const DeviceInfo *d = nullptr;
+        BN_TRY(device_info(&d));
+        ClusterPlan cp;
+        if (plan_cluster_fin(mode, a, d, &cp)) return run_cluster_fin(mode, a, d, cp, stream);
+    }
     Launch l;
     BN_TRY(plan(mode, &a, &l));
     cudaError_t e = ops_for(mode).launch(a, l, reinterpret_cast<cudaStream_t>(stream));
@@ -1129,8 +1200,8 @@ bn_status bn_set_tuning(const bn_tuning *t)
         return fail(BN_ERR_INVALID, "wait_mode must be 0, 1 or 2");
     if (t->group < 0 || t->group > 64)
         return fail(BN_ERR_INVALID, "group must be in [0, 64]");
-    if (t->split < 0 || t->split > 2)
-        return fail(BN_ERR_INVALID, "split must be 0, 1 or 2");
+    if (t->split < 0 || t->split > 3)
+        return fail(BN_ERR_INVALID, "split must be 0, 1, 2 or 3");
     if (t->dependent_launch < 0 || t->dependent_launch > 2)
         return fail(BN_ERR_INVALID, "dependent_launch must be 0, 1 or 2");
     if (t->wait_limit_polls < 0)
@@ -1165,6 +1236,21 @@ bn_status bn_query_launch(bn_op op, int R, int T, int k, int H, int has_shared,
     // is a marker that is never dereferenced (nothing is launched)
     static const uint16_t kSharedMarker[8] = {};
     a.shared = (fin && has_shared) ? kSharedMarker : nullptr;
+    {
+        const DeviceInfo *d = nullptr;
+        BN_TRY(device_info(&d));
+        ClusterPlan cp;
+        if (plan_cluster_fin(mode, a, d, &cp)) {
+            info->split = 2;
+            info->cluster_size = cp.cs;
+            info->threads = kClusterThreads;
+            info->chunks_per_thread = cp.tpt;
+            info->grid = T * cp.cs;
+            info->resident_ctas = cp.resident * cp.cs;
+            info->smem_bytes = (int)cp.smem;
+            return BN_OK;
+        }
+    }
     Launch l;
     BN_TRY(plan(mode, &a, &l));
     int resident = 0;

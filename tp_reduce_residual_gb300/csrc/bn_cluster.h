@@ -1,0 +1,43 @@
+// bn_cluster.h -- the finalize at small T with each token row spread over a
+// thread-block cluster (internal to libbeamnorm; not installed).
+//
+// One cluster of cs CTAs per token row; CTA q owns the column slice
+// [q*nch/cs, (q+1)*nch/cs) of 16-byte chunks.  Each of its threads takes one
+// (shard, chunk) task of that slice -- up to TPT tasks -- and gathers the k
+// expert chunks and the shared-expert chunk with plain 16-byte loads, all in
+// flight at once.  The BF16 finalize results stay in the CTA's shared memory,
+// where the slice's threads sum them in rank order and run the epilogue; the
+// two row-wide sums of squares cross the cluster as one asynchronous remote
+// store per CTA pair, counted on the receiver's barrier.  Nothing goes through
+// global memory but the inputs and the outputs.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "bn_internal.h"
+
+namespace bn {
+
+constexpr int kClusterThreads = 512;   // threads per CTA: finalize tasks, then the slice's epilogue
+constexpr int kClusterMaxTpt = 2;      // finalize tasks per thread
+
+struct ClusterArgs {
+    Args a;        // operands, sizes, eps, debug outputs, error word (pipeline fields unused)
+    int tasks;     // R * largest slice: the finalize tasks of one CTA
+};
+
+// Dynamic shared memory: the slice's finalize results, [R][slice] 16-byte chunks.
+inline size_t cluster_smem_bytes(int R, int slice) { return (size_t)R * (size_t)slice * 16u; }
+
+// Enqueue one cluster of cs CTAs per token row (grid T * cs).  postnorm
+// selects the sandwich or the single pre-RMSNorm; tpt is 1 or 2.
+cudaError_t launch_cluster_fin(const ClusterArgs &c, bool postnorm, int tpt, int cs, bool pdl,
+                               cudaStream_t st);
+
+// Clusters of this shape the device holds at once (0 if none), for the planner.
+int cluster_fin_resident(bool postnorm, int tpt, int cs, size_t smem, cudaError_t *err);
+
+}  // namespace bn
