@@ -384,7 +384,7 @@ def test_launch_query_is_coherent(op, R, T, k, H):
 def test_reduce_planner_balances_rows_per_sm():
     """One CTA per reduce row: the planner takes 512-thread CTAs when an SM then
     runs at least as many consumer threads and takes no more rows, with a gain
-    in one (R=8, H=8192 at T=1024 and 4096; R=8, H=16384), keeps the default
+    in one (R=8, H=8192 at T=1024 and 4096; R=4, H=12288), keeps the default
     where both tie (T=256), where the wide CTA runs fewer threads (R=4,
     H=5120) or would hold one chunk per thread (H=4096), and sizes the ring
     for the CTAs that actually share an SM when rows are fewer than CTA slots."""
@@ -396,8 +396,13 @@ def test_reduce_planner_balances_rows_per_sm():
         assert (i["threads"], i["chunks_per_thread"], i["cluster_size"]) == (544, 2, 1)
     i = bn.launch_info("reduce_norm", 8, 256, 8192)
     assert (i["threads"], i["chunks_per_thread"]) == (288, 4)
+    # rows wider than 1536 chunks split over a cluster (R=8, H=16384: two CTAs)
     i = bn.launch_info("reduce_norm", 8, 1024, 16384)
-    assert (i["threads"], i["chunks_per_thread"]) == (544, 4)
+    assert (i["threads"], i["chunks_per_thread"], i["cluster_size"]) == (288, 4, 2)
+    i = bn.launch_info("reduce_norm", 4, 1024, 12288)
+    assert (i["threads"], i["chunks_per_thread"], i["cluster_size"]) == (416, 4, 1)
+    i = bn.launch_info("finalize_reduce_norm", 8, 256, 16384, 8)
+    assert (i["chunks_per_thread"], i["cluster_size"]) == (2, 2)
     i = bn.launch_info("reduce_norm", 8, 1024, 4096)
     assert (i["threads"], i["chunks_per_thread"]) == (288, 2)
     for T in (1024, 4096):

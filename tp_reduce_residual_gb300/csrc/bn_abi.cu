@@ -343,8 +343,13 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     // chunks one CTA's threads must cover: the column slice, or the whole row
     // when a cluster splits rows by shard
     const int nch_max = split ? nchunks : (nchunks + cs - 1) / cs;
+    // At most 4 chunks per thread (2 for the finalize modes): above that a
+    // slice takes more threads (up to 512), then a larger cluster.  The
+    // 8-chunk kernels spilled (finalize 900-1500 bytes, its 4-chunk kernels
+    // 30-90) and lost to wider splits (see plan()).
+    const int max_cpt = fin ? kMaxCptFin : kMaxCpt;
     int cpt = 1;
-    while (cpt < 8 && (nch_max + cpt - 1) / cpt > cap) cpt *= 2;
+    while (cpt < max_cpt && (nch_max + cpt - 1) / cpt > cap) cpt *= 2;
     const int consumers = round_up((nch_max + cpt - 1) / cpt, 32);
     if (consumers > kMaxConsumers)
         return fail(BN_ERR_UNSUPPORTED, "row of %d chunks needs %d consumer threads", nch_max, consumers);
@@ -528,9 +533,20 @@ bn_status plan(int mode, Args *a, Launch *l)
 
     const int want_cs = g_tune_cluster.load();
     int cs = want_cs;
-    if (cs <= 0)
+    if (cs <= 0) {
         cs = (mode & F_FIN) ? auto_cluster(T, nchunks, d->sms, (long long)loads_per_row(mode, *a, false, 1) * 2 * H)
                             : auto_cluster_reduce(T, nchunks, d->sms);
+        // Wide rows split over a cluster until a CTA's slice is at most 1024
+        // chunks (finalize) or 1536 (the others).  Measured on GB300 (us per
+        // call, CUDA graph, L2-cold; the smallest cluster that fits shared
+        // memory / this rule): reduce R=8 H=16384 T=1024 68.0 / 64.5, R=8
+        // H=32768 T=300 63.4 / 42.1, R=4 H=24576 T=1024 146.7 / 74.6 (R=4
+        // H=12288 stays one CTA a row: 33.5, against 38.0 with two);
+        // finalize R=8 k=8 H=16384 T=256 135.4 / 114.7, R=8 k=4 H=32768 T=64
+        // 46.8 / 37.8, R=4 k=2 H=12288 T=1024 87.6 / 84.3.
+        const int max_slice = (mode & F_FIN) ? 1024 : 1536;
+        while (cs < kMaxCluster && (nchunks + cs - 1) / cs > max_slice) cs *= 2;
+    }
     if (cs > nchunks) cs = 1;
     // A slice too wide for one CTA's shared memory (gamma slots and two
     // stages: reduce rows above about 19 K elements at one CTA per row) takes

@@ -35,6 +35,8 @@ constexpr int kMaxMeta = 256;        // R * k slots staged per token row
 constexpr int kMaxH = 32768;         // fused entry points (whole-row epilogue in one launch)
 constexpr int kMaxPieceH = 131072;   // unfused pieces (the fallback when a fused call declines)
 constexpr int kMaxConsumers = 512;   // consumer threads per CTA
+constexpr int kMaxCpt = 4;           // 16-byte chunks per consumer thread: 1, 2 or 4
+constexpr int kMaxCptFin = 2;        // the same for the finalize modes: 1 or 2
 constexpr int kMaxStages = 64;
 constexpr int kMaxCluster = 16;
 
@@ -72,7 +74,7 @@ struct Launch {
     int split;       // 1: the CTAs of a cluster split a row by shard (finalize modes)
     int cluster;     // CTAs per token row (thread-block cluster size)
     int consumers;   // consumer threads per CTA (multiple of 32)
-    int cpt;         // 16-byte chunks per consumer thread: 1, 2, 4 or 8
+    int cpt;         // 16-byte chunks per consumer thread: 1, 2 or 4
     int grid;        // CTAs (a multiple of cluster)
     size_t smem;     // dynamic shared memory bytes
     int pdl;         // 1: programmatic dependent launch (setup overlaps the previous kernel)

@@ -29,8 +29,10 @@ const void *kernel_by_cpt(int cpt)
     switch (cpt) {
     case 1: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 1, SPLIT, FULL>);
     case 2: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 2, SPLIT, FULL>);
-    case 4: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 4, SPLIT, FULL>);
-    case 8: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 8, SPLIT, FULL>);
+    case 4:
+        // the planner takes at most kMaxCptFin chunks per thread in the finalize modes
+        if constexpr ((kMode & F_FIN) == 0) return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 4, SPLIT, FULL>);
+        return nullptr;
     default: return nullptr;
     }
 }
@@ -50,7 +52,7 @@ const void *kernel_for(int cpt, int split, int full)
 
 int cpt_index(int cpt, int split, int full)
 {
-    return (cpt == 1 ? 0 : cpt == 2 ? 1 : cpt == 4 ? 2 : 3) + (split ? 4 : 0) + (full ? 8 : 0);
+    return (cpt == 1 ? 0 : cpt == 2 ? 1 : 2) + (split ? 4 : 0) + (full ? 8 : 0);
 }
 
 // Function attributes are per device: set them once per (device, cpt).
