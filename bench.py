@@ -39,6 +39,8 @@ from tp_reduce_residual_gb300 import inputs  # noqa: E402
 
 METRIC = "µs/call and achieved HBM GB/s (% of GB300 peak) vs tokens T, per H/R/top-k"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0       # GB300 HBM3e nominal, the peak the workload's target names
+L2_ROTATION = 8                # rotate over input sets covering at least this many L2s
 L2_BYTES_FALLBACK = 129 * 1024 * 1024
 
 
@@ -215,6 +217,13 @@ def workload_bytes(wl, T, split=False, with_shared=True):
     return inputs.algorithmic_bytes(wl.op, wl.R, T, wl.H, wl.k, split=split, with_shared=with_shared)
 
 
+def line_config(wl, T, B, world, with_ws, l2):
+    """The workload description both arms print (the same keys and values)."""
+    return {"workload": wl.describe(T), "op": wl.op, "R": wl.R, "H": wl.H, "k": wl.k, "T": T,
+            "bytes_per_step": B, "parallelism": f"replicas x{world}", "workspace": with_ws,
+            "l2": f"inputs {B / 1e9:.2f} GB per step > L2 {l2 / 1e6:.0f} MB; no flush"}
+
+
 def call_fused(bn, d, res, out, stream=None, workspace=None):
     if d["op"] == "reduce_norm":
         bn.reduce_norm(d["partials"], res, d["gamma_post"], d["gamma_pre"], d["eps"], out=out,
@@ -386,7 +395,7 @@ def sweep(bn, peak, l2_bytes, max_sets=64):
         for T in wl.tokens:
             B = workload_bytes(wl, T)
             base = inputs.make_inputs(wl, T, device="cuda")
-            n_sets = int(min(max_sets, max(1, math.ceil(4 * l2_bytes / B))))
+            n_sets = int(min(max_sets, max(1, math.ceil(L2_ROTATION * l2_bytes / B))))
             sets = [base] + [clone_set(base) for _ in range(n_sets - 1)]
             outs = [torch.empty_like(base["residual"]) for _ in range(n_sets)]
             hot = graph_time_us([lambda: call_fused(bn, base, base["residual"], outs[0])] * 20)
@@ -397,7 +406,9 @@ def sweep(bn, peak, l2_bytes, max_sets=64):
             row = {"workload": wl.describe(T), "cfg": f"C{wl.index}", "T": T, "bytes": B,
                    "us_cold": round(cold, 3), "us_hot": round(hot, 3),
                    "gbs_cold": round(B / cold / 1e3, 1), "frac_cold": round(B / cold / 1e3 / peak, 4),
-                   "l2_cold": bool(n_sets * B >= 4 * l2_bytes)}
+                   "frac_cold_nominal": round(B / cold / 1e3 / NOMINAL_HBM_GBS, 4),
+                   "input_sets": n_sets,
+                   "l2_cold": bool(n_sets * B >= L2_ROTATION * l2_bytes)}
             if wl.op == "finalize_reduce_norm" and bn.finalize_workspace_bytes(wl.R, T, wl.k, wl.H):
                 # the same calls with a workspace: each token row over many CTAs
                 ws = bn.finalize_workspace(wl.R, T, wl.k, wl.H, device="cuda")
@@ -450,12 +461,11 @@ def oracle_sample_time(wl, T, target_s, seed_rows=0):
     import numpy as np
 
     import oracle
-    from tests import parity
 
     d = inputs.make_inputs(wl, T, device="cuda")
 
     def run(rows):
-        c = inputs.to_numpy(parity.compact(d, rows))
+        c = inputs.to_numpy(inputs.select_rows(d, rows))
         t0 = time.perf_counter()
         if wl.op == "reduce_norm":
             oracle.reduce_norm(c["partials"], c["residual"], c["gamma_post"], c["gamma_pre"], c["eps"])
@@ -555,13 +565,12 @@ def main(argv=None):
             "us_per_call": round(ms_per_step * 1000.0, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "io_dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl.describe(T), "op": wl.op, "R": wl.R, "H": wl.H, "k": wl.k,
-                       "T": T, "bytes_per_step": B, "parallelism": f"replicas x{world}",
-                       "workspace": with_ws,
-                       "l2": f"inputs {B / 1e9:.2f} GB per step > L2 {l2 / 1e6:.0f} MB; no flush"},
+            "config": line_config(wl, T, B, world, with_ws, l2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_kind": peak_kind,
+                         "peak_nominal": NOMINAL_HBM_GBS,
+                         "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                          "traffic": None if with_ws else recorded_traffic(key)},
             "clocks": clocks,
             "gpu_launches": args.steps,
@@ -580,7 +589,6 @@ def main_reference(args, rank, world, wl, T, B):
     import numpy as np
 
     import oracle
-    from tests import parity
 
     torch.manual_seed(0)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
@@ -591,7 +599,7 @@ def main_reference(args, rank, world, wl, T, B):
 
     def sample(n):
         rows = sorted(rng.choice(Tg, size=n, replace=False).tolist())
-        return inputs.to_numpy(parity.compact(d, rows))
+        return inputs.to_numpy(inputs.select_rows(d, rows))
 
     def run(c):
         if wl.op == "reduce_norm":
@@ -615,16 +623,19 @@ def main_reference(args, rank, world, wl, T, B):
     secs = time.perf_counter() - t0
     Bn = workload_bytes(wl, n)
     value = Bn * args.steps / secs / 1e9
+    l2 = L2_BYTES_FALLBACK
+    if torch.cuda.is_available():
+        l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 0) or L2_BYTES_FALLBACK
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs / args.steps * 1000.0, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": wl.describe(T), "op": wl.op, "R": wl.R, "H": wl.H, "k": wl.k, "T": T,
-                   "bytes_per_step": Bn},
+        "config": line_config(wl, T, B, world, False, l2),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{n} token rows of {wl.describe(T)} per step", "host": host_cpu()},
+                         "sample": f"{n} token rows of {wl.describe(T)} per step "
+                                   f"({Bn} algorithmic bytes)", "host": host_cpu()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

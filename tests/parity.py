@@ -93,21 +93,7 @@ def run_fused(d, single: bool = False, debug: bool = True, stream=None, workspac
 
 def compact(d, rows: Sequence[int]) -> dict:
     """The operands of the selected token rows as a self-contained input set."""
-    idx = torch.as_tensor(list(rows), dtype=torch.long, device=d["residual"].device)
-    n = idx.numel()
-    c = {key: d[key] for key in ("op", "R", "H", "k", "eps", "gamma_post", "gamma_pre")}
-    c["T"] = n
-    c["residual"] = d["residual"][idx].contiguous()
-    if d["op"] == "reduce_norm":
-        c["partials"] = d["partials"][:, idx].contiguous()
-    else:
-        R, k = d["R"], d["k"]
-        rows_used = d["perm"][:, idx, :].long().reshape(R, n * k)
-        c["expert_out"] = torch.stack([d["expert_out"][r][rows_used[r]] for r in range(R)]).contiguous()
-        c["perm"] = torch.arange(n * k, dtype=torch.int32, device=idx.device).reshape(1, n, k).repeat(R, 1, 1)
-        c["w"] = d["w"][:, idx].contiguous()
-        c["shared"] = None if d["shared"] is None else d["shared"][:, idx].contiguous()
-    return c
+    return inputs.select_rows(d, rows)
 
 
 def run_oracle(d, rows: Optional[Sequence[int]] = None, single: bool = False) -> dict:

@@ -142,6 +142,31 @@ def make_inputs(wl: Workload, T: int, device="cpu", seed: Optional[int] = None,
     return d
 
 
+def select_rows(d: dict, rows: Sequence[int]) -> dict:
+    """The operands of the selected token rows as a self-contained input set.
+
+    Every token row depends only on its own operands: its shard rows, or its
+    gathered expert rows, weights and shared-expert rows.  Those are copied
+    into a compact set whose perm is renumbered to the copied rows, so the set
+    gives, row for row, the results of the selected rows of the full one.
+    """
+    idx = torch.as_tensor(list(rows), dtype=torch.long, device=d["residual"].device)
+    n = idx.numel()
+    c = {key: d[key] for key in ("op", "R", "H", "k", "eps", "gamma_post", "gamma_pre")}
+    c["T"] = n
+    c["residual"] = d["residual"][idx].contiguous()
+    if d["op"] == "reduce_norm":
+        c["partials"] = d["partials"][:, idx].contiguous()
+    else:
+        R, k = d["R"], d["k"]
+        rows_used = d["perm"][:, idx, :].long().reshape(R, n * k)
+        c["expert_out"] = torch.stack([d["expert_out"][r][rows_used[r]] for r in range(R)]).contiguous()
+        c["perm"] = torch.arange(n * k, dtype=torch.int32, device=idx.device).reshape(1, n, k).repeat(R, 1, 1)
+        c["w"] = d["w"][:, idx].contiguous()
+        c["shared"] = None if d["shared"] is None else d["shared"][:, idx].contiguous()
+    return c
+
+
 def u16(t: torch.Tensor) -> np.ndarray:
     """BF16 torch tensor -> numpy uint16 bit patterns (host copy)."""
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
