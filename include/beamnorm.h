@@ -329,9 +329,9 @@ typedef struct {
     int wait_mode;     /* 1: suspending try_wait, 2: polling test_wait */
     int group;         /* row copies per pipeline stage, at most 64; the finalize
                           modes only (the other modes carry one copy a stage) */
-    int split;         /* finalize rows: 1 split by columns, 2 split by shard,
+    int split;         /* 1 split rows by columns, 2 finalize rows by shard,
                           3 one cluster per row with one (shard, chunk) task per
-                          thread (the fused finalize entries) */
+                          thread (the fused entry points) */
     int dependent_launch; /* 1: plain stream order, 2: programmatic dependent
                              launch (the launch and the kernel's setup overlap
                              the previous kernel in the stream) */

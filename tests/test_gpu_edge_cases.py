@@ -129,7 +129,8 @@ def test_edge_cases_on_every_row_split(tuning):
         d = inputs.edge_inputs(op, 4, 5120, KINDS, k=2, seed=300, with_shared=True)
         try:
             bn.set_tuning(**(tuning if op.startswith("finalize") else
-                             {"cluster_size": tuning.get("cluster_size", 0)}))
+                             {"cluster_size": tuning.get("cluster_size", 0),
+                              "split": tuning.get("split", 0) if tuning.get("split") != 2 else 0}))
             g = parity.run_fused(d, prefill="sentinel")
         finally:
             bn.set_tuning()

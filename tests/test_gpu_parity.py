@@ -364,7 +364,8 @@ def test_launch_query_is_coherent(op, R, T, k, H):
     assert i["grid"] // i["cluster_size"] <= T
     if i["split"] == 2:
         # one cluster per row, one (shard, chunk) task per thread: no pipeline
-        assert op.startswith("finalize") and i["grid"] == T * i["cluster_size"]
+        assert op in ("reduce_norm", "reduce_residual_norm", "finalize_reduce_norm",
+                      "finalize_reduce_residual_norm") and i["grid"] == T * i["cluster_size"]
         assert i["chunks_per_thread"] in (1, 2) and i["stages"] == 0
     else:
         assert i["stages"] >= 2 and i["stage_bytes"] % 128 == 0 and i["group"] >= 1
@@ -373,7 +374,7 @@ def test_launch_query_is_coherent(op, R, T, k, H):
     if i["split"] == 1:
         assert op.startswith("finalize") and R % i["cluster_size"] == 0
     try:
-        bn.set_tuning(stages=2, split=1 if op.startswith("finalize") else 0)
+        bn.set_tuning(stages=2, split=1)
         j = bn.launch_info(op, R, T, H, k)
     finally:
         bn.set_tuning()
@@ -520,6 +521,37 @@ def test_cluster_task_split_matches_oracle(R, T, k, H, with_shared, single, cs):
     for key in ("sum", "z"):
         assert_bits_equal(g[key], base[key], key)
     parity.compare(g, parity.run_oracle(d, single=single), what=f"cluster tasks R={R} T={T} H={H}")
+
+
+CLUSTER_REDUCE = [
+    # (R, T, H, single, cluster size)
+    (4, 1, 5120, False, 16),
+    (8, 3, 8192, True, 16),
+    (16, 2, 8192, False, 16),     # two tasks per thread
+    (3, 5, 1000, False, 4),       # ragged slices
+    (1, 4, 64, True, 2),
+    (8, 30, 4096, False, 8),      # more rows than resident clusters
+]
+
+
+@pytest.mark.parametrize("R,T,H,single,cs", CLUSTER_REDUCE)
+def test_cluster_split_of_reduce_rows_matches_oracle(R, T, H, single, cs):
+    """The reduce entry points on the cluster path: each task loads one
+    shard's partial chunk into the slice's shared rows; the rank-ordered sum,
+    the norms and the exchanges are those of the finalize flavour."""
+    wl = inputs.custom("reduce_norm", R, H, partial_std=0.5, row_scale=True)
+    d = parity.gpu_inputs(wl, T, seed=850 + R * 7 + T)
+    op = "reduce_residual_norm" if single else "reduce_norm"
+    try:
+        bn.set_tuning(split=3, cluster_size=cs)
+        info = bn.launch_info(op, R, T, H)
+        assert info["split"] == 2 and info["cluster_size"] == cs and info["grid"] == T * cs, info
+        g = parity.run_fused(d, single=single)
+    finally:
+        bn.set_tuning()
+    base = parity.run_fused(d, single=single)
+    assert_bits_equal(g["sum"], base["sum"], "sum")
+    parity.compare(g, parity.run_oracle(d, single=single), what=f"cluster reduce R={R} T={T} H={H}")
 
 
 def test_cluster_task_split_flags_bad_perm_and_stays_in_bounds():

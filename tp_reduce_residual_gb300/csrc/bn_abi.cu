@@ -580,6 +580,14 @@ bn_status plan(int mode, Args *a, Launch *l)
 // T=16 20.5 / 14.3 (16-CTA clusters take two waves; with 8-CTA clusters
 // 19.5); R=8, H=6144, k=8 at T=1 5.07 / 8.85, T=16 18.4 / 12.1.
 constexpr int kClusterFinMaxT = 8;
+// The same for the fused reduce entry points, whose CTAs must also keep at
+// least kClusterReduceMinTasks (shard, chunk) loads: light rows are faster on
+// the main kernel.  Measured on GB300 (us per call, CUDA graph, L2-cold; main
+// kernel / cluster path): R=8, H=8192 at T=1 4.55 / 3.34 (16 CTAs), T=8 5.03
+// / 4.43 (8 CTAs); R=4, H=5120 at T=1 3.77 / 3.19 (8), T=8 3.83 / 3.48 (8);
+// R=2, H=256 at T=8 2.60 / 2.83 (4); every case slower at T=64.
+constexpr int kClusterReduceMaxT = 8;
+constexpr int kClusterReduceMinTasks = 256;
 
 struct ClusterPlan {
     int cs, tpt, resident;
@@ -587,14 +595,18 @@ struct ClusterPlan {
 };
 
 // The largest cluster (16, 8, 4 or 2 CTAs) whose CTAs take at most two
-// (shard, chunk) tasks per thread and whose clusters the device holds at once
-// for the T rows (on request, any cluster that is resident at all).
+// (shard, chunk) tasks per thread (reduce rows: at least 256 tasks a CTA) and
+// whose clusters the device holds at once for the T rows (on request, any
+// cluster that is resident at all).
 bool plan_cluster_fin(int mode, const Args &a, const DeviceInfo *d, ClusterPlan *p)
 {
-    if (mode != kModeFinReduceNorm && mode != kModeFinReduceResNorm) return false;
+    const bool fin = (mode & F_FIN) != 0;
+    if (mode != kModeFinReduceNorm && mode != kModeFinReduceResNorm && mode != kModeReduceNorm &&
+        mode != kModeReduceResNorm)
+        return false;
     const int pref = g_tune_split.load();
     if (pref != 0 && pref != 3) return false;
-    if (pref == 0 && a.T > kClusterFinMaxT) return false;
+    if (pref == 0 && a.T > (fin ? kClusterFinMaxT : kClusterReduceMaxT)) return false;
     const int want_cs = g_tune_cluster.load();
     const int nch = a.H / 8;
     for (int cs = kMaxCluster; cs >= 2; cs /= 2) {
@@ -604,10 +616,11 @@ bool plan_cluster_fin(int mode, const Args &a, const DeviceInfo *d, ClusterPlan 
         const int tasks = a.R * slice;
         const int tpt = (tasks + kClusterThreads - 1) / kClusterThreads;
         if (tpt > kClusterMaxTpt) continue;
+        if (!fin && pref == 0 && tasks < kClusterReduceMinTasks) continue;
         const size_t smem = cluster_smem_bytes(a.R, slice);
         if ((long long)smem > (long long)d->smem_optin - 2048) continue;
         cudaError_t e = cudaSuccess;
-        const int res = cluster_fin_resident((mode & F_POSTNORM) != 0, tpt, cs, smem, &e);
+        const int res = cluster_fin_resident(fin, (mode & F_POSTNORM) != 0, tpt, cs, smem, &e);
         if (e != cudaSuccess) {
             cudaGetLastError();
             continue;
@@ -627,7 +640,8 @@ bn_status run_cluster_fin(int mode, Args &a, const DeviceInfo *d, const ClusterP
     ClusterArgs c;
     c.a = a;
     c.tasks = a.R * ((a.nchunks + cp.cs - 1) / cp.cs);
-    const cudaError_t e = launch_cluster_fin(c, (mode & F_POSTNORM) != 0, cp.tpt, cp.cs,
+    const cudaError_t e = launch_cluster_fin(c, (mode & F_FIN) != 0, (mode & F_POSTNORM) != 0,
+                                             cp.tpt, cp.cs,
                                              g_tune_pdl.load() != 1,
                                              reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "bn_cluster_fin_kernel");

@@ -77,10 +77,12 @@ __device__ __forceinline__ void gamma8_regs(const float *g, f2 *out)
 }
 
 // Grid: T clusters of cs CTAs; cluster t works on token row t, CTA q of it on
-// the chunks [c0, c0 + slice) of that row.  Thread i takes the finalize tasks
+// the chunks [c0, c0 + slice) of that row.  Thread i takes the tasks
 // i + j * kClusterThreads (j < TPT) below R * slice: shard task / slice, chunk
-// task % slice.  The first `slice` threads then run the epilogue, one chunk each.
-template <bool POSTNORM, int TPT>
+// task % slice.  A task finalizes that chunk of that shard (FIN), or copies the
+// shard's partial chunk (the reduce entry points).  The first `slice` threads
+// then run the epilogue, one chunk each.
+template <bool FIN, bool POSTNORM, int TPT>
 __global__ void __launch_bounds__(kClusterThreads, 1) bn_cluster_fin_kernel(const ClusterArgs ca)
 {
     const Args &a = ca.a;
@@ -132,7 +134,12 @@ __global__ void __launch_bounds__(kClusterThreads, 1) bn_cluster_fin_kernel(cons
 #pragma unroll
     for (int i = 0; i < TPT; ++i) {
         const int task = tid + i * kClusterThreads;
-        if (task < a.R * slice) {
+        if (!FIN && task < a.R * slice) {
+            const int r = task / slice;
+            const int lc = task - r * slice;
+            zsm[r * slice + lc] =
+                __ldg(reinterpret_cast<const uint4 *>(a.src + ((size_t)r * a.T + t) * H) + c0 + lc);
+        } else if (FIN && task < a.R * slice) {
             const int r = task / slice;
             const int lc = task - r * slice;
             const size_t meta = ((size_t)r * a.T + t) * (size_t)a.k;
@@ -236,12 +243,12 @@ __global__ void __launch_bounds__(kClusterThreads, 1) bn_cluster_fin_kernel(cons
     if (cs > 1) cluster_sync_all();
 }
 
-template <bool POSTNORM>
+template <bool FIN, bool POSTNORM>
 const void *cluster_kernel(int tpt)
 {
     switch (tpt) {
-    case 1: return reinterpret_cast<const void *>(&bn_cluster_fin_kernel<POSTNORM, 1>);
-    case 2: return reinterpret_cast<const void *>(&bn_cluster_fin_kernel<POSTNORM, 2>);
+    case 1: return reinterpret_cast<const void *>(&bn_cluster_fin_kernel<FIN, POSTNORM, 1>);
+    case 2: return reinterpret_cast<const void *>(&bn_cluster_fin_kernel<FIN, POSTNORM, 2>);
     default: return nullptr;
     }
 }
@@ -272,14 +279,15 @@ cudaError_t prepare_cluster(const void *fn, int bit)
     return cudaSuccess;
 }
 
-const void *kernel_for(bool postnorm, int tpt, cudaError_t *e)
+const void *kernel_for(bool fin, bool postnorm, int tpt, cudaError_t *e)
 {
-    const void *fn = postnorm ? cluster_kernel<true>(tpt) : cluster_kernel<false>(tpt);
+    const void *fn = fin ? (postnorm ? cluster_kernel<true, true>(tpt) : cluster_kernel<true, false>(tpt))
+                         : (postnorm ? cluster_kernel<false, true>(tpt) : cluster_kernel<false, false>(tpt));
     if (!fn) {
         *e = cudaErrorInvalidValue;
         return nullptr;
     }
-    *e = prepare_cluster(fn, (postnorm ? 2 : 0) + (tpt == 2 ? 1 : 0));
+    *e = prepare_cluster(fn, (fin ? 4 : 0) + (postnorm ? 2 : 0) + (tpt == 2 ? 1 : 0));
     return *e == cudaSuccess ? fn : nullptr;
 }
 
@@ -308,14 +316,14 @@ void fill(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, int grid, int cs, 
 }  // namespace
 }  // namespace dev
 
-cudaError_t launch_cluster_fin(const ClusterArgs &c, bool postnorm, int tpt, int cs, bool pdl,
-                               cudaStream_t st)
+cudaError_t launch_cluster_fin(const ClusterArgs &c, bool fin, bool postnorm, int tpt, int cs,
+                               bool pdl, cudaStream_t st)
 {
     if (cs < 1 || cs > kMaxCluster || c.a.T < 1 || c.a.nchunks < cs ||
         c.tasks > kClusterThreads * tpt || (c.a.nchunks + cs - 1) / cs > kClusterThreads)
         return cudaErrorInvalidValue;
     cudaError_t e;
-    const void *fn = dev::kernel_for(postnorm, tpt, &e);
+    const void *fn = dev::kernel_for(fin, postnorm, tpt, &e);
     if (!fn) return e;
     const int slice = (c.a.nchunks + cs - 1) / cs;
     cudaLaunchConfig_t cfg;
@@ -325,9 +333,9 @@ cudaError_t launch_cluster_fin(const ClusterArgs &c, bool postnorm, int tpt, int
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-int cluster_fin_resident(bool postnorm, int tpt, int cs, size_t smem, cudaError_t *err)
+int cluster_fin_resident(bool fin, bool postnorm, int tpt, int cs, size_t smem, cudaError_t *err)
 {
-    const void *fn = dev::kernel_for(postnorm, tpt, err);
+    const void *fn = dev::kernel_for(fin, postnorm, tpt, err);
     if (!fn) return 0;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];

@@ -5,7 +5,8 @@
 // [q*nch/cs, (q+1)*nch/cs) of 16-byte chunks.  Each of its threads takes one
 // (shard, chunk) task of that slice -- up to TPT tasks -- and gathers the k
 // expert chunks and the shared-expert chunk with plain 16-byte loads, all in
-// flight at once.  The BF16 finalize results stay in the CTA's shared memory,
+// flight at once (for the reduce entry points a task loads the shard's
+// partial chunk).  The BF16 finalize results stay in the CTA's shared memory,
 // where the slice's threads sum them in rank order and run the epilogue; the
 // two row-wide sums of squares cross the cluster as one asynchronous remote
 // store per CTA pair, counted on the receiver's barrier.  Nothing goes through
@@ -32,12 +33,13 @@ struct ClusterArgs {
 // Dynamic shared memory: the slice's finalize results, [R][slice] 16-byte chunks.
 inline size_t cluster_smem_bytes(int R, int slice) { return (size_t)R * (size_t)slice * 16u; }
 
-// Enqueue one cluster of cs CTAs per token row (grid T * cs).  postnorm
-// selects the sandwich or the single pre-RMSNorm; tpt is 1 or 2.
-cudaError_t launch_cluster_fin(const ClusterArgs &c, bool postnorm, int tpt, int cs, bool pdl,
-                               cudaStream_t st);
+// Enqueue one cluster of cs CTAs per token row (grid T * cs).  fin selects the
+// finalize tasks (expert rows) or the partial rows of the reduce entry points;
+// postnorm the sandwich or the single pre-RMSNorm; tpt is 1 or 2.
+cudaError_t launch_cluster_fin(const ClusterArgs &c, bool fin, bool postnorm, int tpt, int cs,
+                               bool pdl, cudaStream_t st);
 
 // Clusters of this shape the device holds at once (0 if none), for the planner.
-int cluster_fin_resident(bool postnorm, int tpt, int cs, size_t smem, cudaError_t *err);
+int cluster_fin_resident(bool fin, bool postnorm, int tpt, int cs, size_t smem, cudaError_t *err);
 
 }  // namespace bn
