@@ -577,9 +577,10 @@ bn_status plan(int mode, Args *a, Launch *l)
 // rows fit on the device at once.  Measured on GB300 (us per call in a CUDA
 // graph, L2-cold; cluster path with 16 CTAs a row / the default of the day):
 // R=8, H=8192, k=10 at T=1 5.67 / 10.28 (shard split), T=4 6.75 / 10.47,
-// T=16 20.5 / 14.3 (16-CTA clusters take two waves; with 8-CTA clusters
-// 19.5); R=8, H=6144, k=8 at T=1 5.07 / 8.85, T=16 18.4 / 12.1.
-constexpr int kClusterFinMaxT = 8;
+// T=12 10.34 / 11.59 (8-CTA clusters), T=16 20.5 / 14.3 (16-CTA clusters take
+// two waves; with 8-CTA clusters 19.5, with 4 and four tasks a thread 17.1);
+// R=8, H=6144, k=8 at T=1 5.07 / 8.85, T=16 18.4 / 12.1.
+constexpr int kClusterFinMaxT = 15;
 // The same for the fused reduce entry points, whose CTAs must also keep at
 // least kClusterReduceMinTasks (shard, chunk) loads: light rows are faster on
 // the main kernel.  Measured on GB300 (us per call, CUDA graph, L2-cold; main
