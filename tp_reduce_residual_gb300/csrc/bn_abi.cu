@@ -287,17 +287,20 @@ int auto_cluster(int T, int nchunks, int sms, long long row_bytes)
     return cs;
 }
 
-// CTAs per token row for the reduce modes: while rows are few, a cluster
-// splits each row so that more SMs work on it, as long as the CTAs of all
-// rows fit about two per SM and each keeps at least 64 chunks.  Measured on
-// GB300 (us per call, clusters of 1 / 2 / 4 / 8): C2 (R=8, H=8192) at T=1
-// 7.76 / 6.57 / 5.69 / 5.46, T=8 7.82 / 6.71 / 5.85 / 5.60, T=64 8.50 / 7.71
-// / 7.92 / 8.07; C1 (R=4, H=5120) at T=1 5.68 / 5.01 / 4.46 / 4.34, T=64
-// 5.90 / 5.35 / 5.17 / 6.19; from T=256 on one CTA per row is fastest.
-int auto_cluster_reduce(int T, int nchunks, int sms)
+// CTAs per token row for the reduce modes: while rows are few and heavy, a
+// cluster splits each row so that more SMs work on it: up to 8 CTAs, each
+// keeping at least 64 chunks, while T * CTAs * 1 KB stays within the bytes one
+// row moves.  Measured on GB300 (us per call, CUDA graph, L2-cold; clusters
+// of 1 / 2 / 4 / 8): R=8, H=8192 (180 KB a row) at T=12 6.24 / 5.74 / 5.33 /
+// 5.20, T=24 6.30 / 5.81 / 5.46 / 5.49, T=40 6.40 / 6.05 / 6.15 / 6.50, T=64
+// 6.56 / 6.53 / 7.16, T=100 7.33 / 9.57 / 8.48 / 10.48; R=4, H=5120 (70 KB)
+// at T=12 3.99 / 4.15 / 3.78 / 3.90, T=24 4.29 / 4.67 / 4.35, T=40 4.38 /
+// 4.83 / 4.66, T=64 4.50 / 4.96 / 4.98, T=100 4.79 / 5.36 / 6.03.  (T <= 8
+// takes the cluster path of bn_cluster.cu where rows are heavy enough.)
+int auto_cluster_reduce(int T, int nchunks, long long row_bytes)
 {
     int cs = 1;
-    while (cs < 8 && (long long)T * cs * 2 <= 2LL * sms && nchunks / (cs * 2) >= 64) cs *= 2;
+    while (cs < 8 && (long long)T * cs * 2 * 1024 <= row_bytes && nchunks / (cs * 2) >= 64) cs *= 2;
     return cs;
 }
 
@@ -535,7 +538,7 @@ bn_status plan(int mode, Args *a, Launch *l)
     int cs = want_cs;
     if (cs <= 0) {
         cs = (mode & F_FIN) ? auto_cluster(T, nchunks, d->sms, (long long)loads_per_row(mode, *a, false, 1) * 2 * H)
-                            : auto_cluster_reduce(T, nchunks, d->sms);
+                            : auto_cluster_reduce(T, nchunks, ((long long)loads_per_row(mode, *a, false, 1) * 2 + 4) * H);
         // Wide rows split over a cluster until a CTA's slice is at most 1024
         // chunks (finalize) or 1536 (the others).  Measured on GB300 (us per
         // call, CUDA graph, L2-cold; the smallest cluster that fits shared
