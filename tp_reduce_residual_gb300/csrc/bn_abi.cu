@@ -3,7 +3,8 @@
 //
 // Every entry point validates its arguments on the host before any CUDA call
 // and either enqueues exactly one kernel on the caller's stream or enqueues
-// nothing.  Declining a valid shape (BN_ERR_UNSUPPORTED) never does part of
+// nothing (bn_finalize_reduce_norm_noalloc first clears its scratch counters
+// with one memset on the same stream).  Declining a valid shape (BN_ERR_UNSUPPORTED) never does part of
 // the work: the caller falls back to an unfused path and owes the whole
 // reduction (sglang pull request 34134, description: a decline must not skip
 // the owed all-reduce).
