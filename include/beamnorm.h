@@ -319,7 +319,9 @@ BN_API int bn_version(void);
 BN_API void bn_shutdown(void);
 
 /* Launch-shape overrides for measurement sweeps (process-wide).  Every field
- * 0 means automatic.  Results do not depend on these settings, only speed. */
+ * 0 means automatic.  Results do not depend on these settings, only speed
+ * (tiny_pass aside, which can change the debug sums of squares of rows of
+ * tiny values and nothing else). */
 typedef struct {
     int cluster_size;  /* CTAs per token row, at most 16 (a shard split takes
                           one that divides R) */
@@ -343,6 +345,14 @@ typedef struct {
                              its outputs are then unspecified (each within its
                              own buffer).  Not applied to the many-CTA
                              finalize, which never waits. */
+    int tiny_pass;        /* the second pass over a row whose sum of squares is
+                             below 2^-80 (its squares near or below FP32's
+                             subnormal range, where the one-pass compensated
+                             sum is off by up to H * 2^-150): 1 never, 2
+                             always.  Automatic: for eps < 2^-50 only, the
+                             one range of eps where the pass can change an
+                             output; elsewhere it would change only the debug
+                             sums of squares. */
 } bn_tuning;
 
 /* Set the overrides; NULL restores automatic choices.  BN_ERR_INVALID on an
@@ -381,7 +391,9 @@ typedef struct {
 } bn_launch_info;
 
 /* Fill *info with the launch shape that `op` would use for this shape on the
- * current device, under the current tuning overrides; nothing is enqueued.
+ * current device, under the current tuning overrides, for eps >= 2^-50 (the
+ * kernels of smaller eps, see bn_tuning.tiny_pass, may take another shape);
+ * nothing is enqueued.
  * k is ignored by the operations without a finalize; has_shared says whether
  * the finalize call would pass a shared-expert row.  Shape errors and
  * declines are reported as by the entry point itself; T == 0 gives BN_OK and

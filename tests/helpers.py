@@ -74,9 +74,16 @@ def assert_bits_equal(actual: np.ndarray, expected: np.ndarray, what: str = ""):
                              f"{idx}: actual {a[idx]!r} expected {e[idx]!r}")
 
 
-def assert_rel_close(actual: np.ndarray, expected: np.ndarray, rtol: float, what: str = ""):
-    """Within rtol relative where the expected value is finite; identical
-    infinities and NaN == NaN elsewhere."""
+SUBNORMAL_STEP = 2.0 ** -149  # the FP32 subnormal spacing
+
+
+def assert_rel_close(actual: np.ndarray, expected: np.ndarray, rtol: float, what: str = "",
+                     floor: float = SUBNORMAL_STEP):
+    """Within rtol relative where the expected value is finite, or within the
+    absolute ``floor`` where that is larger (by default one FP32 subnormal
+    step, 2^-149: expected values in or near the subnormal range, whose
+    rounding grid is coarser than rtol); identical infinities and NaN == NaN
+    elsewhere."""
     a = np.asarray(actual, dtype=np.float64)
     e = np.asarray(expected, dtype=np.float64)
     fin = np.isfinite(e)
@@ -87,8 +94,10 @@ def assert_rel_close(actual: np.ndarray, expected: np.ndarray, rtol: float, what
     a, e = a[fin], e[fin]
     if not np.all(np.isfinite(a)):
         raise AssertionError(f"{what}: a non-finite value where the expected one is finite")
-    rel = np.abs(a - e) / np.maximum(np.abs(e), 1e-30)
-    if rel.size and rel.max() > rtol:
-        i = int(rel.argmax())
-        raise AssertionError(f"{what}: relative error {rel.max():.3e} > {rtol:.1e} at finite "
-                             f"element {i}: {a[i]} vs {e[i]}")
+    err = np.abs(a - e)
+    over = err / np.maximum(rtol * np.abs(e), floor)
+    if over.size and over.max() > 1.0:
+        i = int(over.argmax())
+        raise AssertionError(f"{what}: error {err[i]:.3e} (relative {err[i] / max(abs(e[i]), 1e-300):.3e})"
+                             f" > max({rtol:.1e} relative, {floor:.3e}) at finite element {i}: "
+                             f"{a[i]!r} vs {e[i]!r}")

@@ -9,8 +9,11 @@ one, since every token row depends only on its own operands.  Large cases
 run the oracle on every row this way, in blocks on a pool of host threads.
 
 Acceptance (per element): the FP32 reduced sum and the per-shard BF16
-finalize results bit-exact; the sums of squares within 1e-5 relative; the BF16
-output and updated residual within 1 BF16 ulp (+0 == -0, NaN == NaN).
+finalize results bit-exact; the sums of squares within 1e-5 relative, or
+within H * 2^-149 absolute where that is larger (the one-pass compensated sum
+over squares in FP32's subnormal range, which the kernels run for eps >=
+2^-50; the kernels for smaller eps meet 2^-149); the BF16 output and updated
+residual within 1 BF16 ulp (+0 == -0, NaN == NaN).
 """
 from __future__ import annotations
 
@@ -20,7 +23,8 @@ import numpy as np
 import torch
 
 import oracle
-from tests.helpers import assert_bf16_close, assert_bits_equal, assert_rel_close, bf16_ulp_diff
+from tests.helpers import (SUBNORMAL_STEP, assert_bf16_close, assert_bits_equal, assert_rel_close,
+                           bf16_ulp_diff)
 from tp_reduce_residual_gb300 import beamnorm as bn
 from tp_reduce_residual_gb300 import inputs
 
@@ -147,8 +151,11 @@ def run_oracle_all_rows(d, single: bool = False, block: int = 64, workers: int =
             for key in parts[0]}
 
 
-def compare(g: dict, ref: dict, rows: Optional[Sequence[int]] = None, what: str = "") -> dict:
-    """Assert the acceptance bar; return exact-match statistics."""
+def compare(g: dict, ref: dict, rows: Optional[Sequence[int]] = None, what: str = "",
+            ss_floor: Optional[float] = None) -> dict:
+    """Assert the acceptance bar; return exact-match statistics.  ``ss_floor``
+    replaces the sums of squares' absolute floor H * 2^-149 (2^-149 for the
+    calls that run the second pass over rows of tiny values)."""
     sel = slice(None) if rows is None else np.asarray(rows)
     stats = {}
     if "sum" in g:
@@ -156,7 +163,9 @@ def compare(g: dict, ref: dict, rows: Optional[Sequence[int]] = None, what: str 
     if "z" in g and "z" in ref:
         assert_bits_equal(g["z"][:, sel], ref["z"], f"{what} z")
     if "ss" in g:
-        assert_rel_close(g["ss"][sel], ref["ss"], SS_RTOL, f"{what} ss")
+        H = ref["out"].shape[-1]
+        floor = H * SUBNORMAL_STEP if ss_floor is None else ss_floor
+        assert_rel_close(g["ss"][sel], ref["ss"], SS_RTOL, f"{what} ss", floor=floor)
         stats["ss_exact"] = float(np.mean(g["ss"][sel].view(np.uint32) == ref["ss"].view(np.uint32)))
     assert_bf16_close(g["residual_out"][sel], ref["residual_out"], MAX_ULP, f"{what} residual_out")
     assert_bf16_close(g["out"][sel], ref["out"], MAX_ULP, f"{what} out")

@@ -59,7 +59,7 @@ def test_library_is_built_for_sm103a():
 
 
 def test_version_and_status_strings(L):
-    assert L.bn_version() == 10100
+    assert L.bn_version() == 10200
     assert L.bn_status_string(0) == b"BN_OK"
     assert L.bn_status_string(2) == b"BN_ERR_UNSUPPORTED"
     assert L.bn_status_string(99) == b"unknown status"
@@ -195,8 +195,11 @@ def test_set_tuning_validates(L):
     assert st(0, 0, 0, 0, 0, 0, 4) == bn.ERR_INVALID
     assert st(0, 0, 0, 0, 0, 0, 0, 3) == bn.ERR_INVALID
     assert st(0, 0, 0, 0, 0, 0, 0, 0, -1) == bn.ERR_INVALID
+    assert st(0, 0, 0, 0, 0, 0, 0, 0, 0, 3) == bn.ERR_INVALID
+    assert st(0, 0, 0, 0, 0, 0, 0, 0, 0, -1) == bn.ERR_INVALID
     assert st(16, 8, 256, 2, 2, 4, 2, 1) == bn.OK
     assert st(0, 0, 0, 0, 0, 0, 0, 0, 3) == bn.OK
+    assert st(0, 0, 0, 0, 0, 0, 0, 0, 0, 2) == bn.OK
     assert L.bn_set_tuning(None) == bn.OK
 
 

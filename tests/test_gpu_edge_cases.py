@@ -4,8 +4,10 @@ Each input set puts one edge case per token row (tp_reduce_residual_gb300.inputs
 .edge_inputs): signed zeros, negated shard pairs that sum to +0, the
 rank-order witness (1, 2^-24, 2^-24) that sums to 1 only in rank order, BF16
 subnormals, constant rows, rows whose sums of squares leave the FP32 range,
-shards holding +-inf and NaN, and a finalize whose weighted products cancel
-exactly (a guard against any fused multiply-add in the finalize).  Every
+shards holding +-inf and NaN, a finalize whose weighted products cancel
+exactly (a guard against any fused multiply-add in the finalize), and rows of
+tiny values whose squares are FP32 subnormals (their sums of squares normal,
+or subnormal).  Every
 entry point that runs these rows is compared with the oracle element by
 element, with the bar of the other parity tests (sum and z bit-exact, NaN ==
 NaN; sums of squares within 1e-5 relative, identical infinities; outputs within
@@ -21,7 +23,7 @@ import pytest
 import torch
 
 from tests import parity
-from tests.helpers import assert_bits_equal, f32_from_bf16
+from tests.helpers import SUBNORMAL_STEP, assert_bits_equal, f32_from_bf16
 from tp_reduce_residual_gb300 import beamnorm as bn
 from tp_reduce_residual_gb300 import build as nbuild
 from tp_reduce_residual_gb300 import inputs
@@ -187,3 +189,87 @@ def test_eps_zero_with_an_all_zero_row(op, single):
         assert np.all(np.isnan(f32_from_bf16(g["out"][zero_row])))
         normal_row = EPS0_KINDS.index("normal")
         assert np.all(np.isfinite(f32_from_bf16(g["out"][normal_row])))
+
+
+TINY_KINDS = ("normal", "tiny", "tiny_sub", "tiny")
+
+
+@pytest.mark.parametrize("tuning", [{}, dict(split=1, cluster_size=1), dict(split=1, cluster_size=4),
+                                    dict(split=3, cluster_size=4)],
+                         ids=["planner", "one-CTA", "columns-x4", "tasks-x4"])
+@pytest.mark.parametrize("op,single", [("reduce_norm", False), ("reduce_norm", True),
+                                       ("finalize_reduce_norm", False),
+                                       ("finalize_reduce_norm", True)])
+def test_tiny_rows_with_eps_zero(op, single, tuning):
+    """eps = 0: the RMS factor is the sum of squares' alone, so an inexact sum
+    of squares shows in every output.  Rows of values near 2^-66 and 2^-76 have
+    subnormal squares; the kernels sum such a row again with its values scaled
+    by a power of two, and must match the oracle's exactly accumulated sums
+    (rounded once to FP32) within 1e-5 relative or one subnormal step."""
+    d = inputs.edge_inputs(op, 4, 5120, TINY_KINDS, k=2, seed=700, eps=0.0, with_shared=True)
+    try:
+        if op == "finalize_reduce_norm":
+            bn.set_tuning(**tuning)
+        else:
+            bn.set_tuning(**{k: v for k, v in tuning.items() if k == "cluster_size"})
+        g = parity.run_fused(d, single=single, prefill="sentinel")
+    finally:
+        bn.set_tuning()
+    ref = parity.run_oracle(d, single=single)
+    # eps = 0 < 2^-50: the kernels with the second pass, within one subnormal step
+    parity.compare(g, ref, what=f"tiny eps=0 {op} single={single} {tuning}",
+                   ss_floor=SUBNORMAL_STEP)
+    for t, kind in enumerate(TINY_KINDS):
+        if kind == "tiny":
+            assert np.all(np.isfinite(f32_from_bf16(g["residual_out"][t]))), kind
+            # a normal sum of squares whose squares are all subnormal
+            col = 1 if single else 0
+            assert 2.0 ** -126 <= ref["ss"][t, col] < 2.0 ** -80, ref["ss"][t]
+            assert np.all(np.isfinite(f32_from_bf16(g["out"][t])))
+        if kind == "tiny_sub":
+            assert 0 < ref["ss"][t, 1 if single else 0] < 2.0 ** -126, ref["ss"][t]
+
+
+@pytest.mark.parametrize("single", [False, True])
+def test_workspace_finalize_tiny_rows(single):
+    """The many-CTA finalize (caller workspace) on the same rows, eps = 0 and
+    eps = 1e-6 (where the residual sum of squares is tiny too)."""
+    for eps in (0.0, 1e-6):
+        d = inputs.edge_inputs("finalize_reduce_norm", 8, 8192, TINY_KINDS, k=4, seed=710,
+                               eps=eps, with_shared=True)
+        ws = bn.finalize_workspace(8, len(TINY_KINDS), 4, 8192, device="cuda")
+        assert ws is not None
+        g = parity.run_fused(d, single=single, workspace=ws, prefill="sentinel")
+        parity.compare(g, parity.run_oracle(d, single=single), what=f"tiny workspace eps={eps}",
+                       ss_floor=SUBNORMAL_STEP if eps == 0.0 else None)
+
+
+@pytest.mark.parametrize("eps", [2.0 ** -50, 1e-6])
+@pytest.mark.parametrize("path", ["planner", "one-CTA", "workspace"])
+def test_tiny_pass_changes_no_output_for_eps_from_2_pow_minus_50(eps, path):
+    """For eps >= 2^-50 the planner runs the kernels without the second pass:
+    a sum of squares below 2^-80 then cannot reach the RMS factor, whose sum
+    fl(fl(ss / H) + eps) rounds to eps either way.  The same rows with the
+    pass forced on and off give bit-identical outputs and residuals; the sums
+    of squares meet 2^-149 with the pass and H * 2^-149 without it."""
+    d = inputs.edge_inputs("finalize_reduce_norm", 8, 8192, TINY_KINDS, k=4, seed=720, eps=eps,
+                           with_shared=True)
+    ref = parity.run_oracle(d)
+    kw = {}
+    if path == "workspace":
+        kw["workspace"] = bn.finalize_workspace(8, len(TINY_KINDS), 4, 8192, device="cuda")
+    runs = {}
+    for tiny_pass in (1, 2):
+        try:
+            bn.set_tuning(tiny_pass=tiny_pass, **({"split": 1} if path == "one-CTA" else {}))
+            runs[tiny_pass] = parity.run_fused(d, prefill="sentinel", **kw)
+        finally:
+            bn.set_tuning()
+    parity.compare(runs[1], ref, what=f"tiny pass off eps={eps} {path}")
+    parity.compare(runs[2], ref, what=f"tiny pass on eps={eps} {path}", ss_floor=SUBNORMAL_STEP)
+    for key in ("out", "residual_out", "sum"):
+        assert np.array_equal(runs[1][key].view(np.uint8), runs[2][key].view(np.uint8)), key
+    # the automatic choice is the kernel without the pass: its results exactly
+    g = parity.run_fused(d, prefill="sentinel", **kw)
+    for key in ("out", "residual_out", "ss"):
+        assert np.array_equal(g[key].view(np.uint8), runs[1][key].view(np.uint8)), key

@@ -57,7 +57,7 @@ class _Tuning(ctypes.Structure):
     _fields_ = [("cluster_size", ctypes.c_int), ("stages", ctypes.c_int), ("threads", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int), ("wait_mode", ctypes.c_int), ("group", ctypes.c_int),
                 ("split", ctypes.c_int), ("dependent_launch", ctypes.c_int),
-                ("wait_limit_polls", ctypes.c_int)]
+                ("wait_limit_polls", ctypes.c_int), ("tiny_pass", ctypes.c_int)]
 
 
 class _LaunchInfo(ctypes.Structure):
@@ -536,12 +536,14 @@ def check_device_error(stream=None, raise_on_error: bool = True) -> int:
 
 def set_tuning(cluster_size: int = 0, stages: int = 0, threads: int = 0, ctas_per_sm: int = 0,
                wait_mode: int = 0, group: int = 0, split: int = 0, dependent_launch: int = 0,
-               wait_limit_polls: int = 0) -> None:
+               wait_limit_polls: int = 0, tiny_pass: int = 0) -> None:
     """Override the launch shape for measurement sweeps (0 = automatic);
     ``wait_limit_polls`` shortens the pipeline waits' limit, for tests of the
-    timeout path."""
+    timeout path; ``tiny_pass`` (1 never, 2 always) overrides the choice of
+    the kernels with the second pass over rows of tiny values."""
     t = _Tuning(int(cluster_size), int(stages), int(threads), int(ctas_per_sm), int(wait_mode),
-                int(group), int(split), int(dependent_launch), int(wait_limit_polls))
+                int(group), int(split), int(dependent_launch), int(wait_limit_polls),
+                int(tiny_pass))
     _check(load().bn_set_tuning(ctypes.byref(t)))
 
 

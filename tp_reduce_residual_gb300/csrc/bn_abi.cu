@@ -31,7 +31,7 @@ namespace bn {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kVersion = 10100;  // 1.1.0
+constexpr int kVersion = 10200;  // 1.2.0
 
 thread_local char g_msg[512] = "";
 
@@ -52,7 +52,19 @@ bn_status cuda_fail(cudaError_t e, const char *what)
 // ---- tuning overrides (process-wide) -------------------------------------------
 
 std::atomic<int> g_tune_cluster{0}, g_tune_stages{0}, g_tune_threads{0}, g_tune_ctas{0},
-    g_tune_wait{0}, g_tune_group{0}, g_tune_split{0}, g_tune_pdl{0}, g_tune_polls{0};
+    g_tune_wait{0}, g_tune_group{0}, g_tune_split{0}, g_tune_pdl{0}, g_tune_polls{0},
+    g_tune_tiny{0};
+
+// 1 if a call of this mode runs the kernel with the second pass over rows of
+// tiny values: modes with the norms, eps below kTinyPassEps (or NaN), unless
+// the tuning says otherwise.
+int tiny_for(int mode, float eps)
+{
+    if (!(mode & F_RESNORM)) return 0;
+    const int t = g_tune_tiny.load();
+    if (t != 0) return t == 2 ? 1 : 0;
+    return eps >= kTinyPassEps ? 0 : 1;
+}
 
 // ---- per-device state ------------------------------------------------------------
 
@@ -393,6 +405,7 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     // cpt chunks per consumer thread: the kernel without those bounds checks
     L.full = split ? (nchunks == cpt * consumers ? 1 : 0)
                    : (nchunks % cs == 0 && nchunks / cs == cpt * consumers ? 1 : 0);
+    L.tiny = a->tiny;
     // CTAs per SM that registers and threads allow (probe with a 2-stage ring)
     Launch probe = L;
     probe.cluster = 1;
@@ -512,6 +525,7 @@ bn_status plan(int mode, Args *a, Launch *l)
 {
     const DeviceInfo *d = nullptr;
     BN_TRY(device_info(&d));
+    a->tiny = tiny_for(mode, a->eps);
     const int T = a->T, H = a->H;
     const int nchunks = H / 8;
     int resident = 0;
@@ -625,7 +639,8 @@ bool plan_cluster_fin(int mode, const Args &a, const DeviceInfo *d, ClusterPlan 
         const size_t smem = cluster_smem_bytes(a.R, slice);
         if ((long long)smem > (long long)d->smem_optin - 2048) continue;
         cudaError_t e = cudaSuccess;
-        const int res = cluster_fin_resident(fin, (mode & F_POSTNORM) != 0, tpt, cs, smem, &e);
+        const int res = cluster_fin_resident(fin, (mode & F_POSTNORM) != 0, tpt,
+                                             tiny_for(mode, a.eps) != 0, cs, smem, &e);
         if (e != cudaSuccess) {
             cudaGetLastError();
             continue;
@@ -642,6 +657,7 @@ bn_status run_cluster_fin(int mode, Args &a, const DeviceInfo *d, const ClusterP
 {
     a.nchunks = a.H / 8;
     a.err = d->err;
+    a.tiny = tiny_for(mode, a.eps);
     ClusterArgs c;
     c.a = a;
     c.tasks = a.R * ((a.nchunks + cp.cs - 1) / cp.cs);
@@ -769,6 +785,7 @@ bn_status run_wide(Args &a, bool postnorm, void *workspace, void *stream)
     BN_TRY(device_info(&d));
     a.nchunks = a.H / 8;
     a.err = d->err;
+    a.tiny = tiny_for(postnorm ? kModeFinReduceNorm : kModeFinReduceResNorm, a.eps);
     WideArgs w;
     w.a = a;
     w.count = static_cast<unsigned *>(workspace);
@@ -1241,6 +1258,8 @@ bn_status bn_set_tuning(const bn_tuning *t)
         return fail(BN_ERR_INVALID, "dependent_launch must be 0, 1 or 2");
     if (t->wait_limit_polls < 0)
         return fail(BN_ERR_INVALID, "wait_limit_polls must not be negative");
+    if (t->tiny_pass < 0 || t->tiny_pass > 2)
+        return fail(BN_ERR_INVALID, "tiny_pass must be 0, 1 or 2");
     g_tune_cluster.store(cs);
     g_tune_stages.store(t->stages);
     g_tune_threads.store(t->threads);
@@ -1250,6 +1269,7 @@ bn_status bn_set_tuning(const bn_tuning *t)
     g_tune_split.store(t->split);
     g_tune_pdl.store(t->dependent_launch);
     g_tune_polls.store(t->wait_limit_polls);
+    g_tune_tiny.store(t->tiny_pass);
     return BN_OK;
 }
 
@@ -1266,7 +1286,9 @@ bn_status bn_query_launch(bn_op op, int R, int T, int k, int H, int has_shared,
     BN_TRY(check_shape(R, T, fin ? k : 1, H, fin));
     if (T == 0) return BN_OK;
     BN_TRY(check_served(R, T, fin ? k : 1, H, fin, is_piece(mode)));
-    Args a = base_args(R, T, fin ? k : 0, H, 0.f);
+    // the shape of a call with eps >= kTinyPassEps (the TINY kernels, which
+    // may hold other registers, run only below it)
+    Args a = base_args(R, T, fin ? k : 0, H, 1.0f);
     // only the presence of the shared rows matters to the shape; the address
     // is a marker that is never dereferenced (nothing is launched)
     static const uint16_t kSharedMarker[8] = {};

@@ -82,14 +82,16 @@ __device__ __forceinline__ void gamma8_regs(const float *g, f2 *out)
 // task % slice.  A task finalizes that chunk of that shard (FIN), or copies the
 // shard's partial chunk (the reduce entry points).  The first `slice` threads
 // then run the epilogue, one chunk each.
-template <bool FIN, bool POSTNORM, int TPT>
+template <bool FIN, bool POSTNORM, int TPT, bool TINY>
 __global__ void __launch_bounds__(kClusterThreads, 1) bn_cluster_fin_kernel(const ClusterArgs ca)
 {
     const Args &a = ca.a;
     extern __shared__ __align__(16) uint4 zsm[];  // [R][slice] BF16 finalize results
-    __shared__ float2 red[2][kCWarps];
-    __shared__ float2 xslot[2][kMaxCluster];
-    __shared__ __align__(8) unsigned long long xbar[2];
+    // four row reductions at most: ss1, its rescale, ss2, its rescale; each
+    // has its own warp slots, exchange slots and barrier (one phase each)
+    __shared__ float2 red[4][kCWarps];
+    __shared__ float2 xslot[4][kMaxCluster];
+    __shared__ __align__(8) unsigned long long xbar[4];
     __shared__ int s_abort;
     const int tid = (int)threadIdx.x;
     const int lane = tid & 31;
@@ -102,11 +104,11 @@ __global__ void __launch_bounds__(kClusterThreads, 1) bn_cluster_fin_kernel(cons
     const int slice = (int)(((long long)(q + 1) * nch) / (long long)cs) - c0;
     const int nwe = (slice + 31) >> 5;  // epilogue warps
     const size_t H = (size_t)a.H;
-    const uint32_t xb[2] = {smem_addr(&xbar[0]), smem_addr(&xbar[1])};
+    const uint32_t xb[4] = {smem_addr(&xbar[0]), smem_addr(&xbar[1]), smem_addr(&xbar[2]),
+                            smem_addr(&xbar[3])};
 
     if (tid == 0) {
-        mbar_init(xb[0], 1u);
-        mbar_init(xb[1], 1u);
+        for (int i = 0; i < 4; ++i) mbar_init(xb[i], 1u);
         s_abort = 0;
     }
     fence_mbarrier_init();
@@ -211,6 +213,18 @@ __global__ void __launch_bounds__(kClusterThreads, 1) bn_cluster_fin_kernel(cons
             }
             ss1 = row_sum_squares_cl(S1, E1, red[0], xslot[0], xb[0], cs, q, nwe, warp, lane, tid,
                                      ctl, live);
+            if (TINY && needs_rescale(ss1)) {  // the same on every thread of the cluster
+                const int kx = rescale_exp(ss1);
+                const float up = pow2f(kx);
+                float Sb = 0.f, Eb = 0.f;
+                if (epi) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) acc_square_scaled(Sb, Eb, s[m], up);
+                }
+                const float r = row_sum_squares_cl(f2_make(Sb, 0.f), f2_make(Eb, 0.f), red[1], xslot[1],
+                                                   xb[1], cs, q, nwe, warp, lane, tid, ctl, live);
+                ss1 = mul_sep(mul_sep(r, pow2f(-kx)), pow2f(-kx));
+            }
             const float r1 = rms_factor(ss1, a.H, a.eps);
             const f2 r1x2 = f2_make(r1, r1);
 #pragma unroll
@@ -223,8 +237,20 @@ __global__ void __launch_bounds__(kClusterThreads, 1) bn_cluster_fin_kernel(cons
             for (int m = 0; m < 4; ++m) acc_square2(S2, E2, s[m]);
             if (live) reinterpret_cast<uint4 *>(a.residual + (size_t)t * H)[gc] = round8(s);
         }
-        const float ss2 = row_sum_squares_cl(S2, E2, red[1], xslot[1], xb[1], cs, q, nwe, warp,
-                                             lane, tid, ctl, live);
+        float ss2 = row_sum_squares_cl(S2, E2, red[2], xslot[2], xb[2], cs, q, nwe, warp, lane,
+                                       tid, ctl, live);
+        if (TINY && needs_rescale(ss2)) {  // the same on every thread of the cluster
+            const int kx = rescale_exp(ss2);
+            const float up = pow2f(kx);
+            float Sb = 0.f, Eb = 0.f;
+            if (epi) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) acc_square_scaled(Sb, Eb, s[m], up);
+            }
+            const float r = row_sum_squares_cl(f2_make(Sb, 0.f), f2_make(Eb, 0.f), red[3], xslot[3],
+                                               xb[3], cs, q, nwe, warp, lane, tid, ctl, live);
+            ss2 = mul_sep(mul_sep(r, pow2f(-kx)), pow2f(-kx));
+        }
         const float r2 = rms_factor(ss2, a.H, a.eps);
         const f2 r2x2 = f2_make(r2, r2);
         if (epi && live) {
@@ -243,14 +269,21 @@ __global__ void __launch_bounds__(kClusterThreads, 1) bn_cluster_fin_kernel(cons
     if (cs > 1) cluster_sync_all();
 }
 
-template <bool FIN, bool POSTNORM>
+template <bool FIN, bool POSTNORM, bool TINY>
 const void *cluster_kernel(int tpt)
 {
     switch (tpt) {
-    case 1: return reinterpret_cast<const void *>(&bn_cluster_fin_kernel<FIN, POSTNORM, 1>);
-    case 2: return reinterpret_cast<const void *>(&bn_cluster_fin_kernel<FIN, POSTNORM, 2>);
+    case 1: return reinterpret_cast<const void *>(&bn_cluster_fin_kernel<FIN, POSTNORM, 1, TINY>);
+    case 2: return reinterpret_cast<const void *>(&bn_cluster_fin_kernel<FIN, POSTNORM, 2, TINY>);
     default: return nullptr;
     }
+}
+
+template <bool TINY>
+const void *cluster_kernel(bool fin, bool postnorm, int tpt)
+{
+    return fin ? (postnorm ? cluster_kernel<true, true, TINY>(tpt) : cluster_kernel<true, false, TINY>(tpt))
+               : (postnorm ? cluster_kernel<false, true, TINY>(tpt) : cluster_kernel<false, false, TINY>(tpt));
 }
 
 // Function attributes are per device: dynamic shared memory above the 48 KB
@@ -279,15 +312,14 @@ cudaError_t prepare_cluster(const void *fn, int bit)
     return cudaSuccess;
 }
 
-const void *kernel_for(bool fin, bool postnorm, int tpt, cudaError_t *e)
+const void *kernel_for(bool fin, bool postnorm, int tpt, bool tiny, cudaError_t *e)
 {
-    const void *fn = fin ? (postnorm ? cluster_kernel<true, true>(tpt) : cluster_kernel<true, false>(tpt))
-                         : (postnorm ? cluster_kernel<false, true>(tpt) : cluster_kernel<false, false>(tpt));
+    const void *fn = tiny ? cluster_kernel<true>(fin, postnorm, tpt) : cluster_kernel<false>(fin, postnorm, tpt);
     if (!fn) {
         *e = cudaErrorInvalidValue;
         return nullptr;
     }
-    *e = prepare_cluster(fn, (fin ? 4 : 0) + (postnorm ? 2 : 0) + (tpt == 2 ? 1 : 0));
+    *e = prepare_cluster(fn, (tiny ? 8 : 0) + (fin ? 4 : 0) + (postnorm ? 2 : 0) + (tpt == 2 ? 1 : 0));
     return *e == cudaSuccess ? fn : nullptr;
 }
 
@@ -323,7 +355,7 @@ cudaError_t launch_cluster_fin(const ClusterArgs &c, bool fin, bool postnorm, in
         c.tasks > kClusterThreads * tpt || (c.a.nchunks + cs - 1) / cs > kClusterThreads)
         return cudaErrorInvalidValue;
     cudaError_t e;
-    const void *fn = dev::kernel_for(fin, postnorm, tpt, &e);
+    const void *fn = dev::kernel_for(fin, postnorm, tpt, c.a.tiny != 0, &e);
     if (!fn) return e;
     const int slice = (c.a.nchunks + cs - 1) / cs;
     cudaLaunchConfig_t cfg;
@@ -333,9 +365,10 @@ cudaError_t launch_cluster_fin(const ClusterArgs &c, bool fin, bool postnorm, in
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-int cluster_fin_resident(bool fin, bool postnorm, int tpt, int cs, size_t smem, cudaError_t *err)
+int cluster_fin_resident(bool fin, bool postnorm, int tpt, bool tiny, int cs, size_t smem,
+                         cudaError_t *err)
 {
-    const void *fn = dev::kernel_for(fin, postnorm, tpt, err);
+    const void *fn = dev::kernel_for(fin, postnorm, tpt, tiny, err);
     if (!fn) return 0;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];

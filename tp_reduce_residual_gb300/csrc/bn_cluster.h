@@ -39,7 +39,10 @@ inline size_t cluster_smem_bytes(int R, int slice) { return (size_t)R * (size_t)
 cudaError_t launch_cluster_fin(const ClusterArgs &c, bool fin, bool postnorm, int tpt, int cs,
                                bool pdl, cudaStream_t st);
 
-// Clusters of this shape the device holds at once (0 if none), for the planner.
-int cluster_fin_resident(bool fin, bool postnorm, int tpt, int cs, size_t smem, cudaError_t *err);
+// Clusters of this shape the device holds at once (0 if none), for the planner;
+// tiny selects the kernel with the second pass over rows of tiny values
+// (Args::tiny), which launch_cluster_fin takes from c.a.tiny.
+int cluster_fin_resident(bool fin, bool postnorm, int tpt, bool tiny, int cs, size_t smem,
+                         cudaError_t *err);
 
 }  // namespace bn

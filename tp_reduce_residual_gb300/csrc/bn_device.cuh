@@ -427,6 +427,28 @@ __device__ __forceinline__ void acc_square2(f2 &S, f2 &E, f2 x)
     E = add2(E, add2(e, pe));
 }
 
+// One compensated accumulator: (S, E) += x*x, as acc_square2 lane by lane.
+__device__ __forceinline__ void acc_square1(float &S, float &E, float x)
+{
+    const float p = mul_sep(x, x);
+    const float pe = fmaf(x, x, -p);
+    float s, e;
+    two_sum(S, p, s, e);
+    S = s;
+    E = E + (e + pe);
+}
+
+// (S, E) += (lo * up)^2 + (hi * up)^2 for the two values of v, scaled by a
+// power of two (exact); the second pass of a row of tiny values, kept scalar
+// so that the rare path holds few registers.
+__device__ __forceinline__ void acc_square_scaled(float &S, float &E, f2 v, float up)
+{
+    float lo, hi;
+    f2_split(v, lo, hi);
+    acc_square1(S, E, mul_sep(lo, up));
+    acc_square1(S, E, mul_sep(hi, up));
+}
+
 __device__ __forceinline__ void combine(float &S, float &E, float S2, float E2)
 {
     float s, e;
@@ -454,6 +476,25 @@ __device__ __forceinline__ float pair_value(float S, float E)
 {
     return S < __int_as_float(0x7f800000) ? S + E : S;
 }
+
+// A compensated sum of squares is exact only while the squares stay in FP32's
+// normal range: below it a square's rounding error cannot be represented.  A
+// row whose sum is below 2^-80 (every value below 2^-40) is therefore summed
+// again with each value scaled by 2^k, exactly (a power of two); the scaled
+// sum lands in [0.5, 2), and the result is scaled back by 2^-k twice.  A sum
+// that is zero or subnormal (every value below 2^-63) takes k = 100, which
+// lifts every nonzero FP32 value's square above 2^-100.  In the scaled pass
+// only a value over 2^51 times smaller than the row's largest can lose its
+// square's error term, an error below 2^-148 of the scaled sum.
+__device__ __forceinline__ bool needs_rescale(float ss) { return ss < __int_as_float(0x17800000); }
+
+__device__ __forceinline__ int rescale_exp(float ss)
+{
+    const int e = (int)((__float_as_uint(ss) >> 23) & 0xffu);  // biased exponent, ss >= 0
+    return e == 0 ? 100 : (127 - e) >> 1;
+}
+
+__device__ __forceinline__ float pow2f(int k) { return __int_as_float((127 + k) << 23); }
 
 __device__ __forceinline__ void warp_tree(float &S, float &E)
 {
@@ -539,7 +580,7 @@ __device__ __forceinline__ float row_sum_squares(f2 S2, f2 E2, int &nred, const 
 // CTAs), so the per-chunk bounds checks drop out of the loops.  In the shard
 // split it covers the finalize over the whole row (nchunks == CPT *
 // consumers); the epilogue slice there stays checked.
-template <int MODE, int CPT, bool SPLITR, bool FULL>
+template <int MODE, int CPT, bool SPLITR, bool FULL, bool TINY>
 __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
 {
     constexpr bool FIN = (MODE & F_FIN) != 0;
@@ -1093,6 +1134,22 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                         }
                     }
                     ss1 = row_sum_squares(S1, E1, nred, sm, cs, q, NT, NW, warp, lane, tid, ctl, live);
+                    if (TINY && needs_rescale(ss1)) {  // the same on every thread of the cluster
+                        const int kx = rescale_exp(ss1);
+                        const float up = pow2f(kx);
+                        float Sb = 0.f, Eb = 0.f;
+#pragma unroll
+                        for (int i = 0; i < CPT; ++i) {
+                            const int lc = tid + i * NT;
+                            if ((FULL && !SPLITR) || lc < nch) {
+#pragma unroll
+                                for (int m = 0; m < 4; ++m) acc_square_scaled(Sb, Eb, s[i][m], up);
+                            }
+                        }
+                        const float r = row_sum_squares(f2_make(Sb, 0.f), f2_make(Eb, 0.f), nred, sm, cs, q,
+                                                        NT, NW, warp, lane, tid, ctl, live);
+                        ss1 = mul_sep(mul_sep(r, pow2f(-kx)), pow2f(-kx));
+                    }
                     const float r1 = rms_factor(ss1, a.H, a.eps);
                     const f2 r1x2 = f2_make(r1, r1);
 #pragma unroll
@@ -1124,7 +1181,23 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                     }
                     release();
                 }
-                const float ss2 = row_sum_squares(S2, E2, nred, sm, cs, q, NT, NW, warp, lane, tid, ctl, live);
+                float ss2 = row_sum_squares(S2, E2, nred, sm, cs, q, NT, NW, warp, lane, tid, ctl, live);
+                if (TINY && needs_rescale(ss2)) {  // the same on every thread of the cluster
+                    const int kx = rescale_exp(ss2);
+                    const float up = pow2f(kx);
+                    float Sb = 0.f, Eb = 0.f;
+#pragma unroll
+                    for (int i = 0; i < CPT; ++i) {
+                        const int lc = tid + i * NT;
+                        if ((FULL && !SPLITR) || lc < nch) {
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) acc_square_scaled(Sb, Eb, s[i][m], up);
+                        }
+                    }
+                    const float r = row_sum_squares(f2_make(Sb, 0.f), f2_make(Eb, 0.f), nred, sm, cs, q,
+                                                    NT, NW, warp, lane, tid, ctl, live);
+                    ss2 = mul_sep(mul_sep(r, pow2f(-kx)), pow2f(-kx));
+                }
                 const float r2 = rms_factor(ss2, a.H, a.eps);
                 const f2 r2x2 = f2_make(r2, r2);
 #pragma unroll

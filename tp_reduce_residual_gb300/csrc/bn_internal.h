@@ -66,8 +66,20 @@ struct Args {
     int zbuf_bytes;           // shard split: shared-memory bytes of one full z row
     int spin_wait;            // 1: poll barriers with test_wait; 0: try_wait
     int wait_polls;           // polls after which a pipeline wait gives up (0: the default)
+    int tiny;                 // 1: the kernel with the second pass over rows of tiny values
     float eps;
 };
+
+// A row whose sum of squares is below 2^-80 has squares in or near FP32's
+// subnormal range, where the compensated sum is inexact (an error below
+// H * 2^-150); the kernels built with a second, rescaled pass over such rows
+// (TINY) restore the exactly accumulated sum rounded once.  The pass can
+// change an output only when eps < 2^-50: for any larger eps the RMS factor's
+// sum fl(fl(ss / H) + eps) is eps itself for both sums (ss / H < 2^-79, below
+// half the FP32 spacing at eps, which is at least eps * 2^-24 >= 2^-74).  The
+// planner takes the TINY kernels for eps < 2^-50 (or NaN) only; elsewhere
+// the pass would change nothing but the debug sums of squares.
+constexpr float kTinyPassEps = 0x1p-50f;
 
 // Launch shape chosen on the host.
 struct Launch {
@@ -79,6 +91,7 @@ struct Launch {
     size_t smem;     // dynamic shared memory bytes
     int pdl;         // 1: programmatic dependent launch (setup overlaps the previous kernel)
     int full;        // 1: every slice is exactly cpt * consumers chunks (unchecked kernel)
+    int tiny;        // 1: the kernel with the second pass over rows of tiny values (Args::tiny)
 };
 
 // Dynamic shared-memory layout, identical on host and device.

@@ -23,48 +23,64 @@ namespace {
 constexpr int kMode = BN_MODE_VALUE;
 constexpr int kMaxDevices = 64;
 
-template <bool SPLIT, bool FULL>
+template <bool SPLIT, bool FULL, bool TINY>
 const void *kernel_by_cpt(int cpt)
 {
     switch (cpt) {
-    case 1: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 1, SPLIT, FULL>);
-    case 2: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 2, SPLIT, FULL>);
+    case 1: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 1, SPLIT, FULL, TINY>);
+    case 2: return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 2, SPLIT, FULL, TINY>);
     case 4:
         // the planner takes at most kMaxCptFin chunks per thread in the finalize modes
-        if constexpr ((kMode & F_FIN) == 0) return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 4, SPLIT, FULL>);
+        if constexpr ((kMode & F_FIN) == 0)
+            return reinterpret_cast<const void *>(&dev::bn_kernel<kMode, 4, SPLIT, FULL, TINY>);
         return nullptr;
     default: return nullptr;
     }
+}
+
+// The second pass over rows of tiny values exists only where there are sums
+// of squares (the modes with the norms).
+constexpr bool kHasTiny = (kMode & F_RESNORM) != 0;
+
+template <bool SPLIT, bool FULL>
+const void *kernel_by_tiny(int cpt, int tiny)
+{
+    if (tiny) {
+        if constexpr (kHasTiny) return kernel_by_cpt<SPLIT, FULL, true>(cpt);
+        return nullptr;
+    }
+    return kernel_by_cpt<SPLIT, FULL, false>(cpt);
 }
 
 // The shard split exists for the finalize modes with an epilogue or the
 // finalize alone; other modes have no such kernel.
 constexpr bool kHasSplit = (kMode & F_FIN) && (kMode & (F_RESNORM | F_Z_OUT));
 
-const void *kernel_for(int cpt, int split, int full)
+const void *kernel_for(const Launch &l)
 {
-    if (split) {
-        if constexpr (kHasSplit) return full ? kernel_by_cpt<true, true>(cpt) : kernel_by_cpt<true, false>(cpt);
+    if (l.split) {
+        if constexpr (kHasSplit)
+            return l.full ? kernel_by_tiny<true, true>(l.cpt, l.tiny) : kernel_by_tiny<true, false>(l.cpt, l.tiny);
         return nullptr;
     }
-    return full ? kernel_by_cpt<false, true>(cpt) : kernel_by_cpt<false, false>(cpt);
+    return l.full ? kernel_by_tiny<false, true>(l.cpt, l.tiny) : kernel_by_tiny<false, false>(l.cpt, l.tiny);
 }
 
-int cpt_index(int cpt, int split, int full)
+int cpt_index(const Launch &l)
 {
-    return (cpt == 1 ? 0 : cpt == 2 ? 1 : 2) + (split ? 4 : 0) + (full ? 8 : 0);
+    return (l.cpt == 1 ? 0 : l.cpt == 2 ? 1 : 2) + (l.split ? 4 : 0) + (l.full ? 8 : 0) + (l.tiny ? 16 : 0);
 }
 
-// Function attributes are per device: set them once per (device, cpt).
+// Function attributes are per device: set them once per (device, kernel).
 std::atomic<unsigned> g_prepared[kMaxDevices];
 
-cudaError_t prepare(const void *fn, int cpt, int split, int full)
+cudaError_t prepare(const void *fn, const Launch &l)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    const unsigned bit = 1u << cpt_index(cpt, split, full);
+    const unsigned bit = 1u << cpt_index(l);
     if (g_prepared[dev].load(std::memory_order_acquire) & bit) return cudaSuccess;
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
@@ -110,9 +126,9 @@ void fill_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, const Launc
 
 cudaError_t BN_CAT(launch_, BN_MODE_NAME)(const Args &a, const Launch &l, cudaStream_t st)
 {
-    const void *fn = kernel_for(l.cpt, l.split, l.full);
+    const void *fn = kernel_for(l);
     if (!fn) return cudaErrorInvalidValue;
-    cudaError_t e = prepare(fn, l.cpt, l.split, l.full);
+    cudaError_t e = prepare(fn, l);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
@@ -123,12 +139,12 @@ cudaError_t BN_CAT(launch_, BN_MODE_NAME)(const Args &a, const Launch &l, cudaSt
 
 int BN_CAT(occupancy_, BN_MODE_NAME)(const Launch &l, cudaError_t *err)
 {
-    const void *fn = kernel_for(l.cpt, l.split, l.full);
+    const void *fn = kernel_for(l);
     if (!fn) {
         *err = cudaErrorInvalidValue;
         return 0;
     }
-    cudaError_t e = prepare(fn, l.cpt, l.split, l.full);
+    cudaError_t e = prepare(fn, l);
     if (e != cudaSuccess) {
         *err = e;
         return 0;

@@ -75,12 +75,12 @@ __device__ __forceinline__ void gamma8_smem(const float4 *g, int lc, f2 *out)
 // Grid: T * parts CTAs; CTA b works on token row b / parts.  Its first
 // w.tasks threads take the tasks q = (b % parts) * w.tasks + tid < R * nchunks
 // of that row, task q being chunk q % nchunks of shard q / nchunks.
-template <bool POSTNORM, int CPT>
+template <bool POSTNORM, int CPT, bool TINY>
 __global__ void __launch_bounds__(kWideThreads, 1) bn_wide_kernel(const WideArgs w)
 {
     const Args &a = w.a;
     extern __shared__ __align__(16) float4 gsm[];  // epilogue gammas: [post,] pre, 2 per chunk
-    __shared__ float2 red[2][kWideWarps];
+    __shared__ float2 red[4][kWideWarps];  // ss1, its rescale, ss2, its rescale
     __shared__ int s_last;
     const int tid = (int)threadIdx.x;
     const int lane = tid & 31;
@@ -245,6 +245,21 @@ __global__ void __launch_bounds__(kWideThreads, 1) bn_wide_kernel(const WideArgs
             }
         }
         ss1 = cta_sum_squares(S1, E1, red[0], warp, lane);
+        if (TINY && needs_rescale(ss1)) {  // the same on every thread of the CTA
+            const int kx = rescale_exp(ss1);
+            const float up = pow2f(kx);
+            float Sb = 0.f, Eb = 0.f;
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) {
+                const int lc = tid + i * kWideThreads;
+                if (lc < nch) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) acc_square_scaled(Sb, Eb, s[i][m], up);
+                }
+            }
+            const float r = cta_sum_squares(f2_make(Sb, 0.f), f2_make(Eb, 0.f), red[1], warp, lane);
+            ss1 = mul_sep(mul_sep(r, pow2f(-kx)), pow2f(-kx));
+        }
         const float r1 = rms_factor(ss1, a.H, a.eps);
         const f2 r1x2 = f2_make(r1, r1);
 #pragma unroll
@@ -270,7 +285,22 @@ __global__ void __launch_bounds__(kWideThreads, 1) bn_wide_kernel(const WideArgs
             reinterpret_cast<uint4 *>(a.residual + (size_t)t * H)[lc] = round8(s[i]);
         }
     }
-    const float ss2 = cta_sum_squares(S2, E2, red[1], warp, lane);
+    float ss2 = cta_sum_squares(S2, E2, red[2], warp, lane);
+    if (TINY && needs_rescale(ss2)) {  // the same on every thread of the CTA
+        const int kx = rescale_exp(ss2);
+        const float up = pow2f(kx);
+        float Sb = 0.f, Eb = 0.f;
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            const int lc = tid + i * kWideThreads;
+            if (lc < nch) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) acc_square_scaled(Sb, Eb, s[i][m], up);
+            }
+        }
+        const float r = cta_sum_squares(f2_make(Sb, 0.f), f2_make(Eb, 0.f), red[3], warp, lane);
+        ss2 = mul_sep(mul_sep(r, pow2f(-kx)), pow2f(-kx));
+    }
     const float r2 = rms_factor(ss2, a.H, a.eps);
     const f2 r2x2 = f2_make(r2, r2);
 #pragma unroll
@@ -291,12 +321,12 @@ __global__ void __launch_bounds__(kWideThreads, 1) bn_wide_kernel(const WideArgs
     griddep_launch_dependents();
 }
 
-template <bool POSTNORM>
+template <bool POSTNORM, bool TINY>
 const void *wide_kernel(int cpt)
 {
     switch (cpt) {
-    case 1: return reinterpret_cast<const void *>(&bn_wide_kernel<POSTNORM, 1>);
-    case 2: return reinterpret_cast<const void *>(&bn_wide_kernel<POSTNORM, 2>);
+    case 1: return reinterpret_cast<const void *>(&bn_wide_kernel<POSTNORM, 1, TINY>);
+    case 2: return reinterpret_cast<const void *>(&bn_wide_kernel<POSTNORM, 2, TINY>);
     default: return nullptr;
     }
 }
@@ -324,11 +354,12 @@ cudaError_t prepare_wide(const void *fn, int bit)
 
 cudaError_t launch_wide(const WideArgs &w, bool postnorm, int cpt, bool pdl, cudaStream_t st)
 {
-    const void *fn = postnorm ? dev::wide_kernel<true>(cpt) : dev::wide_kernel<false>(cpt);
+    const void *fn = w.a.tiny ? (postnorm ? dev::wide_kernel<true, true>(cpt) : dev::wide_kernel<false, true>(cpt))
+                              : (postnorm ? dev::wide_kernel<true, false>(cpt) : dev::wide_kernel<false, false>(cpt));
     if (!fn || w.parts < 1 || w.a.T < 1 || w.a.H > kWideThreads * kWideMaxCpt * 8 ||
         w.tasks < 1 || w.tasks > kWideThreads)
         return cudaErrorInvalidValue;
-    const cudaError_t e = dev::prepare_wide(fn, (postnorm ? 2 : 0) + (cpt == 2 ? 1 : 0));
+    const cudaError_t e = dev::prepare_wide(fn, (w.a.tiny ? 4 : 0) + (postnorm ? 2 : 0) + (cpt == 2 ? 1 : 0));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)w.a.T * (unsigned)w.parts, 1, 1);

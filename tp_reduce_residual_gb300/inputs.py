@@ -210,7 +210,14 @@ def algorithmic_bytes(op: str, R: int, T: int, H: int, k: int = 0, split: bool =
 # edge cases of the method: special values and exactly known sums, one kind per token row
 
 EDGE_KINDS = ("normal", "neg_zero", "neg_pairs", "witness", "subnormal", "constant",
-              "overflow_post", "overflow_pre", "inf_nan", "cancel")
+              "overflow_post", "overflow_pre", "inf_nan", "cancel", "tiny", "tiny_sub")
+
+# value scales of the rows of tiny values: their squares are FP32 subnormals
+# (about 2^-134 and 2^-154), and the row sums of squares, about R*H*2^-134 and
+# R*H*2^-154, are normal ("tiny", R*H >= 2^8) or subnormal but nonzero
+# ("tiny_sub", 2^5 <= R*H < 2^28)
+TINY_SCALE = 2.0 ** -66
+TINY_SUB_SCALE = 2.0 ** -76
 
 
 def _bf16_exact(x: np.ndarray) -> np.ndarray:
@@ -270,6 +277,11 @@ def _edge_row(kind: str, R: int, H: int, rng: np.random.Generator):
         p[r, 3 % H] = np.inf
         p[r, 7 % H] = -np.inf
         p[r, 11 % H] = np.nan
+    elif kind in ("tiny", "tiny_sub"):
+        # shards and residual N(0, 0.5^2) times a power of two (exact in BF16)
+        sc = np.float32(TINY_SCALE if kind == "tiny" else TINY_SUB_SCALE)
+        p[:] = _bf16_exact(0.5 * rng.standard_normal((R, H)).astype(np.float32)) * sc
+        res = _bf16_exact(0.5 * rng.standard_normal(H).astype(np.float32)) * sc
     elif kind == "zero":
         pass
     else:
