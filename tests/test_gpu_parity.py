@@ -414,6 +414,45 @@ def test_reduce_planner_balances_rows_per_sm():
 
 
 @pytest.mark.gpu
+def test_finalize_planner_shares_sms_between_narrow_rows():
+    """Narrow finalize rows take two chunks a thread and several CTAs per SM,
+    with the stage bytes split between those CTAs; rows of 1024 chunks and
+    more keep one 512-thread CTA per SM (the headline shape)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms != 152:
+        pytest.skip("expected shapes are those of a 152-SM GB300")
+    expect = {  # H: (threads, chunks per thread, CTAs per SM)
+        1024: (160, 1, 4), 2048: (160, 2, 4), 3072: (224, 2, 2), 4096: (288, 2, 2),
+        8192: (544, 2, 1),
+    }
+    for H, (threads, cpt, per_sm) in expect.items():
+        i = bn.launch_info("finalize_reduce_norm", 8, 1024, H, 8)
+        got = (i["threads"], i["chunks_per_thread"], i["grid"] // sms)
+        assert got == (threads, cpt, per_sm), (H, got)
+        assert i["split"] == 0 and i["cluster_size"] == 1
+        # about 48 KB of stages per SM, split between its CTAs (copies of 2H bytes)
+        per_cta = 48 * 1024 // per_sm
+        assert i["stage_bytes"] == max(1, per_cta // (2 * H)) * 2 * H, (H, i["stage_bytes"])
+
+
+NARROW_FIN = [
+    # (R, T, k, H): two chunks a thread, several CTAs per SM; ragged slices too
+    (8, 300, 8, 2048), (8, 200, 8, 3072), (4, 333, 8, 4096), (8, 160, 2, 4096),
+    (8, 157, 8, 2056), (3, 170, 5, 3000),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("single", [False, True])
+@pytest.mark.parametrize("R,T,k,H", NARROW_FIN)
+def test_narrow_finalize_rows_match_oracle(R, T, k, H, single):
+    wl = inputs.custom("finalize_reduce_norm", R, H, k, partial_std=0.3, shared_std=0.3)
+    d = parity.gpu_inputs(wl, T, seed=3000 + R * 13 + T + H)
+    g = parity.run_fused(d, single=single)
+    parity.compare(g, parity.run_oracle(d, single=single), what=f"narrow finalize R={R} T={T} k={k} H={H}")
+
+
+@pytest.mark.gpu
 def test_every_piece_has_a_launch_up_to_its_maximum():
     """The unfused pieces serve rows the fused entry points decline: the
     planner finds a launch (clusters of up to 16 CTAs) wherever

@@ -337,6 +337,10 @@ int loads_per_row(int mode, const Args &a, bool split, int cs)
 //             but no more than the rows put on one SM when one CTA takes a row;
 //   stages    the SM's shared memory split over those CTAs, capped at two rows
 //             of copies ahead.
+// Narrow finalize rows take two chunks per thread down to this many consumer
+// threads per CTA (see shape_for).
+constexpr int kNarrowFinMinConsumers = 128;
+
 // One launch shape for a given row split.  Sets *resident to the clusters the
 // device holds at once (0: this shape cannot be resident).
 bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, int cap_in,
@@ -366,34 +370,25 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     const int max_cpt = fin ? kMaxCptFin : kMaxCpt;
     int cpt = 1;
     while (cpt < max_cpt && (nch_max + cpt - 1) / cpt > cap) cpt *= 2;
+    // Narrow finalize rows (column split, threads automatic): two chunks per
+    // thread as soon as a CTA still has 4 consumer warps, so that 2 to 4 CTAs
+    // share an SM instead of one wide CTA.  Measured on GB300 (R=8, k=8,
+    // T=1024, us per call; one CTA of 1 chunk a thread / CTAs of 2):
+    // H=4096 143.3 / 110.0 (T=4096 542 / 385), H=3072 135.4 / 89.4,
+    // H=2048 129.2 / 66.0 (3 CTAs of 128 threads).
+    if (fin && !split && cpt == 1 && max_cpt >= 2 && cap_in == 0 && g_tune_threads.load() == 0 &&
+        nch_max >= 2 * kNarrowFinMinConsumers)
+        cpt = 2;
     const int consumers = round_up((nch_max + cpt - 1) / cpt, 32);
     if (consumers > kMaxConsumers)
         return fail(BN_ERR_UNSUPPORTED, "row of %d chunks needs %d consumer threads", nch_max, consumers);
-    // one stage holds `group` row copies of item_bytes each.  Measured on
-    // GB300: the finalize modes gain from ~48 KB stages (fewer handshakes
-    // over their many gathered copies), the reduce modes run best with one
-    // copy per stage, and their kernels assume it (no item cursor).
     const int item_bytes = round_up(nch_max * 16 * (sum_in ? 2 : 1), 128);
-    int group = g_tune_group.load() > 0 ? g_tune_group.load() : (fin ? (48 * 1024) / item_bytes : 1);
-    if (!fin) group = 1;
-    if (group > per_row) group = per_row;
-    if (group < 1) group = 1;
     const int slice = (nchunks + cs - 1) / cs;  // the largest column slice of the epilogue
     const int gamma_bytes = gamma_slot_bytes(mode, slice);
     // shard split: each CTA's z buffer holds R rows of its column slice
     const int zbuf_bytes =
         (split && !(mode & F_Z_OUT)) ? round_up(a->R * ((nchunks + cs - 1) / cs) * 16, 128) : 0;
     const int cta_max = d->smem_optin - 1024;  // room for the kernel's static shared memory
-    // A group is shrunk until two stages fit one CTA, or three when the group
-    // is automatic (measured, shard split of C4 at T=64: 2 stages of 3 copies
-    // 27.9 us, 3 stages of 2 copies 26.1 us).
-    const int min_stages = g_tune_group.load() > 0 ? 2 : 3;
-    while (group > 1 && (int)SmemLayout::make(min_stages, group * item_bytes, gamma_bytes, zbuf_bytes,
-                                              fin).total > cta_max)
-        --group;
-    const int stage_bytes = group * item_bytes;
-    const int stages_per_row = (per_row + group - 1) / group;
-    const int overhead = (int)SmemLayout::make(0, stage_bytes, gamma_bytes, zbuf_bytes, fin).total;
 
     Launch L;
     L.split = split ? 1 : 0;
@@ -406,10 +401,11 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     L.full = split ? (nchunks == cpt * consumers ? 1 : 0)
                    : (nchunks % cs == 0 && nchunks / cs == cpt * consumers ? 1 : 0);
     L.tiny = a->tiny;
-    // CTAs per SM that registers and threads allow (probe with a 2-stage ring)
+    // CTAs per SM that registers and threads allow (probe with the smallest
+    // ring: two stages of one copy)
     Launch probe = L;
     probe.cluster = 1;
-    probe.smem = SmemLayout::make(2, stage_bytes, gamma_bytes, zbuf_bytes, fin).total;
+    probe.smem = SmemLayout::make(2, item_bytes, gamma_bytes, zbuf_bytes, fin).total;
     int resident_probe = 0;
     BN_TRY(resident_clusters(mode, probe, &resident_probe));
     int by_regs = resident_probe / (d->sms > 0 ? d->sms : 1);
@@ -423,6 +419,29 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
         const int fill = (a->T + d->sms - 1) / d->sms;
         if (fill >= 1 && fill < ctas) ctas = fill;
     }
+
+    // One stage holds `group` row copies of item_bytes each.  Measured on
+    // GB300: the finalize modes gain from about 48 KB of stages per SM (fewer
+    // handshakes over their many gathered copies), split between the CTAs
+    // that share it (R=8, k=8, H=4096, 2 CTAs: stages of 16, 24 and 32 KB
+    // 111.2, 110.0 and 115.0 us); the reduce modes run best with one copy per
+    // stage, and their kernels assume it (no item cursor).
+    int group = g_tune_group.load() > 0 ? g_tune_group.load()
+                                        : (fin ? (48 * 1024) / (ctas * item_bytes) : 1);
+    if (!fin) group = 1;
+    if (group > per_row) group = per_row;
+    if (group < 1) group = 1;
+    // A group is shrunk until two stages fit one CTA, or three when the group
+    // is automatic (measured, shard split of C4 at T=64: 2 stages of 3 copies
+    // 27.9 us, 3 stages of 2 copies 26.1 us).
+    const int min_stages = g_tune_group.load() > 0 ? 2 : 3;
+    while (group > 1 && (int)SmemLayout::make(min_stages, group * item_bytes, gamma_bytes, zbuf_bytes,
+                                              fin).total > cta_max)
+        --group;
+    const int stage_bytes = group * item_bytes;
+    const int stages_per_row = (per_row + group - 1) / group;
+    const int overhead = (int)SmemLayout::make(0, stage_bytes, gamma_bytes, zbuf_bytes, fin).total;
+
     // the kernel's own static shared memory is 128 bytes; the occupancy check
     // below drops a stage if the estimate was one too many
     int per_cta = d->smem_per_sm / ctas - d->smem_reserved - 128;
