@@ -383,12 +383,14 @@ def test_launch_query_is_coherent(op, R, T, k, H):
 
 @pytest.mark.gpu
 def test_reduce_planner_balances_rows_per_sm():
-    """One CTA per reduce row: the planner takes 512-thread CTAs when an SM then
-    runs at least as many consumer threads and takes no more rows, with a gain
-    in one (R=8, H=8192 at T=1024 and 4096; R=4, H=12288), keeps the default
-    where both tie (T=256), where the wide CTA runs fewer threads (R=4,
-    H=5120) or would hold one chunk per thread (H=4096), and sizes the ring
-    for the CTAs that actually share an SM when rows are fewer than CTA slots."""
+    """One CTA per reduce row: the planner takes 512-thread CTAs for heavy rows
+    (R=8, H=8192 at T=1024 and 4096) when an SM then runs at least as many
+    consumer threads and takes no more rows, with a gain in one; keeps the
+    default where both tie (T=256), where the wide CTA runs fewer threads
+    (R=4, H=5120) or would hold one chunk per thread (H=4096); gives light
+    rows (R <= 4) 128-thread CTAs with up to 4 chunks each; and sizes the
+    ring for the CTAs that actually share an SM when rows are fewer than CTA
+    slots."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     if sms != 152:
         pytest.skip("expected shapes are those of a 152-SM GB300")
@@ -411,6 +413,19 @@ def test_reduce_planner_balances_rows_per_sm():
         assert (i["threads"], i["chunks_per_thread"], i["resident_ctas"]) == (192, 4, 3 * sms)
     i = bn.launch_info("reduce_norm", 4, 256, 5120)
     assert i["threads"] == 192 and i["resident_ctas"] == 2 * sms and i["grid"] == 256
+    # light rows (R <= 4) with more rows than SMs: 128 consumer threads, up to
+    # 4 chunks each, up to 4 CTAs per SM; the wider CTA only for heavy rows
+    for R, H, want in ((2, 2048, (160, 2)), (4, 4096, (160, 4)), (2, 7168, (256, 4)),
+                       (4, 8192, (288, 4))):
+        i = bn.launch_info("reduce_norm", R, 4096, H)
+        assert (i["threads"], i["chunks_per_thread"], i["cluster_size"]) == (*want, 1), (R, H, i)
+    i = bn.launch_info("reduce_norm", 8, 4096, 7168)
+    assert (i["threads"], i["chunks_per_thread"]) == (256, 4)
+    i = bn.launch_info("reduce_norm", 8, 4096, 2048)
+    assert (i["threads"], i["chunks_per_thread"]) == (160, 2)
+    # a row with an SM to itself keeps the wider CTA
+    i = bn.launch_info("reduce_norm", 4, 64, 5120)
+    assert (i["threads"], i["chunks_per_thread"]) == (352, 2)
 
 
 @pytest.mark.gpu

@@ -337,9 +337,11 @@ int loads_per_row(int mode, const Args &a, bool split, int cs)
 //             but no more than the rows put on one SM when one CTA takes a row;
 //   stages    the SM's shared memory split over those CTAs, capped at two rows
 //             of copies ahead.
-// Narrow finalize rows take two chunks per thread down to this many consumer
-// threads per CTA (see shape_for).
+// Narrow rows take two chunks per thread down to this many consumer threads
+// per CTA, and light reduce rows (at most kLightReduceMaxR shards) cap their
+// CTAs at it (see shape_for).
 constexpr int kNarrowFinMinConsumers = 128;
+constexpr int kLightReduceMaxR = 4;
 
 // One launch shape for a given row split.  Sets *resident to the clusters the
 // device holds at once (0: this shape cannot be resident).
@@ -352,10 +354,20 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     const int nchunks = H / 8;
     const int per_row = loads_per_row(mode, *a, split, cs);
     // measured on GB300: the finalize modes run best with 512 consumer threads
-    // (one CTA per SM), the reduce modes with 256 and several CTAs per SM
+    // (one CTA per SM), the reduce modes with 256 and several CTAs per SM, and
+    // the light reduce rows (R <= 4 shards summed, one CTA a row, more rows
+    // than SMs) with 128 and up to 4 chunks a thread, which puts more rows in
+    // flight per SM.  Light rows (us per call, T=4096, default / 128
+    // threads): R=2 H=4096 38.9 / 32.6, R=4 H=4096 46.1 / 41.4, R=4 H=2048
+    // 31.3 / 24.1; R=8 H=4096 is slower with 128 (56.6 / 61.2), and so is a
+    // row that has an SM to itself (R=4 H=5120 T=64: 4.49 / 4.88).
+    const bool light = !fin && !sum_in && (mode & F_RESNORM) && a->R <= kLightReduceMaxR &&
+                       cs == 1 && a->T > d->sms;
     const int cap = g_tune_threads.load() > 0 ? g_tune_threads.load()
                     : cap_in > 0               ? cap_in
-                                               : (fin ? kMaxConsumers : 256);
+                    : fin                      ? kMaxConsumers
+                    : light                    ? kNarrowFinMinConsumers
+                                               : 256;
     const int want_stages = g_tune_stages.load();
     const int want_ctas = g_tune_ctas.load();
     *resident = 0;
@@ -370,14 +382,17 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     const int max_cpt = fin ? kMaxCptFin : kMaxCpt;
     int cpt = 1;
     while (cpt < max_cpt && (nch_max + cpt - 1) / cpt > cap) cpt *= 2;
-    // Narrow finalize rows (column split, threads automatic): two chunks per
-    // thread as soon as a CTA still has 4 consumer warps, so that 2 to 4 CTAs
-    // share an SM instead of one wide CTA.  Measured on GB300 (R=8, k=8,
-    // T=1024, us per call; one CTA of 1 chunk a thread / CTAs of 2):
-    // H=4096 143.3 / 110.0 (T=4096 542 / 385), H=3072 135.4 / 89.4,
-    // H=2048 129.2 / 66.0 (3 CTAs of 128 threads).
-    if (fin && !split && cpt == 1 && max_cpt >= 2 && cap_in == 0 && g_tune_threads.load() == 0 &&
-        nch_max >= 2 * kNarrowFinMinConsumers)
+    // Narrow rows (column split, threads automatic): two chunks per thread as
+    // soon as a CTA still has 4 consumer warps, so that 2 to 4 CTAs share an
+    // SM instead of one wide CTA.  Measured on GB300 (us per call; one CTA of
+    // 1 chunk a thread / CTAs of 2): finalize R=8, k=8, T=1024 H=4096 143.3 /
+    // 110.0 (T=4096 542 / 385), H=3072 135.4 / 89.4, H=2048 129.2 / 66.0
+    // (3 CTAs of 128 threads); reduce R=8, H=2048, T=4096 38.9 / 30.8.  Reduce
+    // rows split over a cluster, or with an SM each, keep one chunk a thread
+    // (R=2, H=4096, T=16 over 2-CTA clusters: 3.38 / 3.54).
+    const bool sums_rows = !sum_in && (fin || ((mode & F_RESNORM) != 0 && cs == 1 && a->T > d->sms));
+    if (sums_rows && !split && cpt == 1 && max_cpt >= 2 && cap_in == 0 &&
+        g_tune_threads.load() == 0 && nch_max >= 2 * kNarrowFinMinConsumers)
         cpt = 2;
     const int consumers = round_up((nch_max + cpt - 1) / cpt, 32);
     if (consumers > kMaxConsumers)
@@ -518,6 +533,16 @@ void sm_load(const Launch &l, int resident, int T, int sms, long long *threads, 
 //   R=4, H=5120 keeps 3 CTAs x 160 threads against 1 x 320 (T=1024 18.0 /
 //     20.4); R=8, H=4096 keeps 256 threads (512 would take 1 chunk each:
 //     T=1024 19.1 / 24.2).
+// With more rows than SMs, only heavy rows (at least kWideMinR shards) of at
+// least kWideMinChunks chunks are offered the wider shape: elsewhere one CTA
+// per SM left the row-wide reductions without a second CTA to overlap them,
+// whatever the two figures said.  Measured (T=4096, default / wide): R=8
+// H=7168 96.7 / 101.5, R=4 H=8192 78.5 / 88.2, R=4 H=7168 66.4 / 82.1, R=2
+// H=8192 61.1 / 77.2.  A row with an SM to itself keeps the wider CTA
+// (R=4, H=5120, T=64: 4.49 against 4.88 with 160 threads).
+constexpr int kWideMinR = 8;
+constexpr int kWideMinChunks = 1024;
+
 bn_status wider_ctas(int mode, Args *a, const DeviceInfo *d, Launch *l, int resident)
 {
     Args wa = *a;
@@ -591,7 +616,8 @@ bn_status plan(int mode, Args *a, Launch *l)
     for (int tried = 0; tried < 2 * kMaxCluster; ++tried) {
         const bn_status st = shape_for(mode, a, d, false, cs, 0, l, &resident);
         if (st == BN_OK && resident > 0) {
-            if (!(mode & F_FIN) && cs == 1 && g_tune_threads.load() == 0)
+            if (!(mode & F_FIN) && cs == 1 && g_tune_threads.load() == 0 &&
+                ((a->R >= kWideMinR && nchunks >= kWideMinChunks) || T <= d->sms))
                 return wider_ctas(mode, a, d, l, resident);
             return BN_OK;
         }
