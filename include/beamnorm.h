@@ -39,10 +39,14 @@
  * the final rounding it is off the exact sum by at most about (n * 2^-24)^2
  * relative and typically by about sqrt(n) * 2^-48, so it is the FP32 rounding
  * of the exact sum unless that lies within such a distance of a rounding
- * boundary (or squares fall below the FP32 normal range, |s| < 2^-63, where a
- * product's error is itself rounded).  So results practically never depend on
- * how a row is split across threads.  A sum beyond the FP32 range is +inf,
- * as the exact sum rounded.
+ * boundary.  So results practically never depend on how a row is split
+ * across threads.  Where squares fall below the FP32 normal range a
+ * product's error is itself rounded and one pass is off by up to H * 2^-150;
+ * for eps < 2^-50 a row whose sum is below 2^-80 is therefore summed again
+ * with its values scaled by a power of two, which restores the exact sum
+ * rounded once.  For larger eps that pass cannot change an output, since
+ * fl(ss / H) + eps rounds to eps, so it is skipped there (bn_tuning.tiny_pass
+ * overrides).  A sum beyond the FP32 range is +inf, as the exact sum rounded.
  *
  * Conventions for every entry point:
  *   - BF16 tensors are passed as uint16_t bit patterns.  All tensors are dense,
