@@ -105,3 +105,70 @@ def test_random_shape_matches_oracle(case):
         bn.set_tuning()
     assert bn.check_device_error() == 0
     parity.compare(g, parity.run_oracle(d, single=c["single"]), what=_id(c))
+
+
+# ---- the unfused pieces (the fallback of a declined fused call) -------------------------
+
+N_PIECE_CASES = 40
+MAX_PIECE_H = 131072
+
+
+def _draw_piece(i: int) -> dict:
+    rng = np.random.default_rng(95_000 + i)
+    fin = bool(rng.integers(0, 2))
+    single = bool(rng.integers(0, 3) == 0)
+    R = int(rng.choice([1, 2, 4, 8, 16]))
+    k = int(rng.choice([1, 2, 4, 8])) if fin else 0
+    # H log-uniform over [8, 131072]: a third of the draws above the fused maximum
+    H = 8 * int(np.clip(np.exp(rng.uniform(0.0, np.log(MAX_PIECE_H / 8))), 1, MAX_PIECE_H // 8))
+    per_row = H * 2 * (R * (k + 1) + 2 if fin else R + 2) + 8 * H
+    T_max = max(1, min(64, MAX_BYTES // per_row))
+    T = int(np.clip(np.exp(rng.uniform(0.0, np.log(T_max + 1.0))), 1, T_max))
+    with_shared = fin and bool(rng.integers(0, 2))
+    return dict(fin=fin, single=single, R=R, k=k, H=H, T=T, with_shared=with_shared)
+
+
+PIECE_CASES = [_draw_piece(i) for i in range(N_PIECE_CASES)]
+
+
+def _piece_id(c: dict) -> str:
+    return (f"{'fin' if c['fin'] else 'red'}{'-single' if c['single'] else ''}-R{c['R']}-k{c['k']}"
+            f"-H{c['H']}-T{c['T']}{'-shared' if c['with_shared'] else ''}")
+
+
+def test_piece_draws_reach_beyond_the_fused_maximum():
+    assert any(c["H"] > 32768 for c in PIECE_CASES) and any(c["H"] <= 32768 for c in PIECE_CASES)
+    assert {(c["fin"], c["single"]) for c in PIECE_CASES} == {(False, False), (False, True),
+                                                               (True, False), (True, True)}
+
+
+@pytest.mark.parametrize("case", PIECE_CASES, ids=[_piece_id(c) for c in PIECE_CASES])
+def test_random_shape_through_the_pieces_matches_oracle(case):
+    """The unfused chain on a random shape: the materialised finalize (z), the
+    rank-ordered FP32 sum, then the epilogue on that sum; each against the
+    oracle's fused results (z and the sum bit for bit)."""
+    c = case
+    op = "finalize_reduce_norm" if c["fin"] else "reduce_norm"
+    wl = inputs.custom(op, c["R"], c["H"], c["k"], partial_std=0.3, shared_std=0.3)
+    d = parity.gpu_inputs(wl, c["T"], seed=8_000 + c["R"] * 7 + c["T"] * 3 + c["H"],
+                          with_shared=c["with_shared"])
+    for piece in ((["finalize_only", "finalize_reduce_only"] if c["fin"] else ["reduce_only"]) +
+                  ["residual_norm_only" if c["single"] else "norm_only"]):
+        assert bn.supports_op(piece, c["R"], c["T"], c["H"], c["k"]), piece
+    ref = parity.run_oracle(d, single=c["single"])
+    g = {}
+    if c["fin"]:
+        z = bn.finalize_only(d["expert_out"], d["perm"], d["w"], d["shared"])
+        s = bn.finalize_reduce_only(d["expert_out"], d["perm"], d["w"], d["shared"])
+        g["z"] = inputs.u16(z)
+    else:
+        s = bn.reduce_only(d["partials"])
+    res = d["residual"].clone()
+    if c["single"]:
+        out = bn.residual_norm_only(s, res, d["gamma_pre"], d["eps"])
+    else:
+        out = bn.norm_only(s, res, d["gamma_post"], d["gamma_pre"], d["eps"])
+    torch.cuda.synchronize()
+    assert bn.check_device_error() == 0
+    g.update({"sum": s.cpu().numpy(), "out": inputs.u16(out), "residual_out": inputs.u16(res)})
+    parity.compare(g, ref, what=_piece_id(c))
