@@ -340,7 +340,7 @@ int loads_per_row(int mode, const Args &a, bool split, int cs)
 // Narrow rows take two chunks per thread down to this many consumer threads
 // per CTA, and light reduce rows (at most kLightReduceMaxR shards) cap their
 // CTAs at it (see shape_for).
-constexpr int kNarrowFinMinConsumers = 128;
+constexpr int kNarrowMinConsumers = 128;
 constexpr int kLightReduceMaxR = 4;
 
 // One launch shape for a given row split.  Sets *resident to the clusters the
@@ -366,7 +366,7 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     const int cap = g_tune_threads.load() > 0 ? g_tune_threads.load()
                     : cap_in > 0               ? cap_in
                     : fin                      ? kMaxConsumers
-                    : light                    ? kNarrowFinMinConsumers
+                    : light                    ? kNarrowMinConsumers
                                                : 256;
     const int want_stages = g_tune_stages.load();
     const int want_ctas = g_tune_ctas.load();
@@ -392,7 +392,7 @@ bn_status shape_for(int mode, Args *a, const DeviceInfo *d, bool split, int cs, 
     // (R=2, H=4096, T=16 over 2-CTA clusters: 3.38 / 3.54).
     const bool sums_rows = !sum_in && (fin || ((mode & F_RESNORM) != 0 && cs == 1 && a->T > d->sms));
     if (sums_rows && !split && cpt == 1 && max_cpt >= 2 && cap_in == 0 &&
-        g_tune_threads.load() == 0 && nch_max >= 2 * kNarrowFinMinConsumers)
+        g_tune_threads.load() == 0 && nch_max >= 2 * kNarrowMinConsumers)
         cpt = 2;
     const int consumers = round_up((nch_max + cpt - 1) / cpt, 32);
     if (consumers > kMaxConsumers)
