@@ -577,6 +577,37 @@ def test_cluster_task_split_matches_oracle(R, T, k, H, with_shared, single, cs):
     parity.compare(g, parity.run_oracle(d, single=single), what=f"cluster tasks R={R} T={T} H={H}")
 
 
+@pytest.mark.parametrize("R,T,k,H,cs", [
+    (8, 16, 8, 2048, 4), (8, 32, 8, 2048, 4), (8, 64, 8, 2048, 2), (4, 32, 8, 4096, 4),
+    (2, 32, 8, 7168, 4), (8, 16, 10, 8192, 0), (8, 64, 8, 4096, 0), (8, 16, 8, 6144, 0),
+    (2, 37, 8, 7168, 2),   # 37 clusters of 4 are more than the device holds at once
+])
+def test_narrow_finalize_rows_keep_the_cluster_path_past_15_rows(R, T, k, H, cs):
+    """Past 15 token rows the finalize keeps the cluster path for narrow rows
+    (clusters of at most 4 CTAs, at most two tasks a thread, all T * cs CTAs on
+    distinct SMs); wider rows go to the main kernel (cs = 0 here).  The
+    cluster path's bits equal the forced column split's, and the oracle's."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms != 152:
+        pytest.skip("expected shapes are those of a 152-SM GB300")
+    info = bn.launch_info("finalize_reduce_norm", R, T, H, k)
+    if cs:
+        assert info["split"] == 2 and info["cluster_size"] == cs and info["grid"] == T * cs, info
+    else:
+        assert info["split"] != 2, info
+    wl = inputs.custom("finalize_reduce_norm", R, H, k, partial_std=0.3, shared_std=0.3)
+    d = parity.gpu_inputs(wl, T, seed=860 + R * 7 + T + H)
+    g = parity.run_fused(d)
+    try:
+        bn.set_tuning(split=1)
+        base = parity.run_fused(d)
+    finally:
+        bn.set_tuning()
+    for key in ("sum", "z"):
+        assert_bits_equal(g[key], base[key], key)
+    parity.compare(g, parity.run_oracle(d), what=f"mid-T finalize R={R} T={T} k={k} H={H}")
+
+
 CLUSTER_REDUCE = [
     # (R, T, H, single, cluster size)
     (4, 1, 5120, False, 16),

@@ -652,6 +652,15 @@ constexpr int kClusterFinMaxT = 15;
 // R=2, H=256 at T=8 2.60 / 2.83 (4); every case slower at T=64.
 constexpr int kClusterReduceMaxT = 8;
 constexpr int kClusterReduceMinTasks = 256;
+// Past kClusterFinMaxT rows the fused finalize entries keep the cluster path
+// for narrow rows only: clusters of at most kClusterMidMaxCs CTAs whose
+// CTAs, one per SM, hold all T rows at once with at most two tasks a thread.
+// Measured on GB300 (us per call, CUDA graph, L2-cold; R=8, k=8; cluster
+// path / the main kernel's shard or column split): H=2048 T=16 5.66 / 8.70,
+// T=32 6.28 / 9.77 (4 CTAs a row), T=64 9.06 / 11.91 (2); H=4096 T=16 8.40
+// / 11.33, T=32 9.27 / 12.32 (4).  Larger clusters lost (H=2048 T=16 with 8:
+// 10.18), and so did wider rows (H=8192 T=16 with 8: 19.4 / 14.3).
+constexpr int kClusterMidMaxCs = 4;
 
 struct ClusterPlan {
     int cs, tpt, resident;
@@ -661,7 +670,8 @@ struct ClusterPlan {
 // The largest cluster (16, 8, 4 or 2 CTAs) whose CTAs take at most two
 // (shard, chunk) tasks per thread (reduce rows: at least 256 tasks a CTA) and
 // whose clusters the device holds at once for the T rows (on request, any
-// cluster that is resident at all).
+// cluster that is resident at all); past kClusterFinMaxT finalize rows, a
+// cluster of at most kClusterMidMaxCs CTAs with T * cs CTAs on distinct SMs.
 bool plan_cluster_fin(int mode, const Args &a, const DeviceInfo *d, ClusterPlan *p)
 {
     const bool fin = (mode & F_FIN) != 0;
@@ -670,11 +680,14 @@ bool plan_cluster_fin(int mode, const Args &a, const DeviceInfo *d, ClusterPlan 
         return false;
     const int pref = g_tune_split.load();
     if (pref != 0 && pref != 3) return false;
-    if (pref == 0 && a.T > (fin ? kClusterFinMaxT : kClusterReduceMaxT)) return false;
+    const bool mid = fin && pref == 0 && a.T > kClusterFinMaxT;
+    if (pref == 0 && !fin && a.T > kClusterReduceMaxT) return false;
+    if (mid && (long long)a.T * 2 > d->sms) return false;
     const int want_cs = g_tune_cluster.load();
     const int nch = a.H / 8;
-    for (int cs = kMaxCluster; cs >= 2; cs /= 2) {
+    for (int cs = mid ? kClusterMidMaxCs : kMaxCluster; cs >= 2; cs /= 2) {
         if (want_cs > 0 && cs != want_cs) continue;
+        if (mid && (long long)a.T * cs > d->sms) continue;
         const int slice = (nch + cs - 1) / cs;
         if (nch < cs || slice > kClusterThreads) continue;
         const int tasks = a.R * slice;
