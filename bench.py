@@ -302,60 +302,77 @@ def time_headline(bn, wl, T, steps, warmup, dev_index, use_workspace=False):
 
 def time_e2e(bn, wl, T, steps, copy_streams=4):
     """The same call through the public API with host buffers: every step copies
-    the inputs from pinned host memory and reads the outputs back.  The input
-    copies of a step are split by leading dimension over `copy_streams` side
-    streams (several copy engines), which the compute stream then waits for;
-    a step's copies start only after the previous step's call is enqueued
-    behind them, so no step overlaps another."""
+    the inputs from pinned host memory and reads both outputs back.  Two
+    device input sets alternate, so that one step's uploads (split by leading
+    dimension over `copy_streams` side streams, several copy engines) overlap
+    the previous step's call and downloads, as a serving loop would pipeline
+    them; a set is overwritten only after the downloads of the step that last
+    used it.  Every step still moves all of its bytes inside the timed region."""
     dd = inputs.make_inputs(wl, T, device="cuda")
     host = {k: (v.cpu().pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in dd.items()}
-    dev = {k: (torch.empty_like(v) if isinstance(v, torch.Tensor) else v) for k, v in dd.items()}
+    devs = [{k: (torch.empty_like(v) if isinstance(v, torch.Tensor) else v) for k, v in dd.items()}
+            for _ in range(2)]
     del dd
-    out = torch.empty_like(dev["residual"])
-    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    res_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    outs = [torch.empty_like(devs[0]["residual"]) for _ in range(2)]
+    out_h = [torch.empty(outs[0].shape, dtype=outs[0].dtype, pin_memory=True) for _ in range(2)]
+    res_h = [torch.empty(outs[0].shape, dtype=outs[0].dtype, pin_memory=True) for _ in range(2)]
     names = [k for k, v in host.items() if isinstance(v, torch.Tensor)]
     h2d = sum(host[k].numel() * host[k].element_size() for k in names)
-    d2h = 2 * out.numel() * out.element_size()
+    d2h = 2 * outs[0].numel() * outs[0].element_size()
 
     main = torch.cuda.current_stream()
     side = [torch.cuda.Stream() for _ in range(max(1, copy_streams))]
-    pieces = []
-    for k in names:
-        nparts = min(len(side), host[k].shape[0]) if host[k].dim() > 0 else 1
-        for hp, dp in zip(host[k].chunk(nparts), dev[k].chunk(nparts)):
-            pieces.append((hp, dp))
-    pieces.sort(key=lambda x: -x[0].numel() * x[0].element_size())
+    down = torch.cuda.Stream()
+    pieces = []  # per set: (host piece, device piece), largest first
+    for dev in devs:
+        ps = []
+        for k in names:
+            nparts = min(len(side), host[k].shape[0]) if host[k].dim() > 0 else 1
+            for hp, dp in zip(host[k].chunk(nparts), dev[k].chunk(nparts)):
+                ps.append((hp, dp))
+        ps.sort(key=lambda x: -x[0].numel() * x[0].element_size())
+        pieces.append(ps)
+    freed = [torch.cuda.Event() for _ in range(2)]  # set b's downloads are done
+    for ev in freed:
+        ev.record(down)
 
-    def step():
-        for s_ in side:
-            s_.wait_stream(main)
+    def step(i):
+        b = i & 1
         load = [0] * len(side)
-        for hp, dp in pieces:   # largest first onto the least loaded stream
-            i = load.index(min(load))
-            with torch.cuda.stream(side[i]):
+        for s_ in side:
+            s_.wait_event(freed[b])
+        for hp, dp in pieces[b]:   # largest first onto the least loaded stream
+            j = load.index(min(load))
+            with torch.cuda.stream(side[j]):
                 dp.copy_(hp, non_blocking=True)
-            load[i] += hp.numel() * hp.element_size()
+            load[j] += hp.numel() * hp.element_size()
         for s_ in side:
             main.wait_stream(s_)
-        call_fused(bn, dev, dev["residual"], out)
-        out_h.copy_(out, non_blocking=True)
-        res_h.copy_(dev["residual"], non_blocking=True)
+        call_fused(bn, devs[b], devs[b]["residual"], outs[b])
+        down.wait_stream(main)
+        with torch.cuda.stream(down):
+            out_h[b].copy_(outs[b], non_blocking=True)
+            res_h[b].copy_(devs[b]["residual"], non_blocking=True)
+            freed[b].record(down)
 
-    step()
+    step(0)
+    step(1)
     torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
-    start.record(stream)
-    for _ in range(steps):
-        step()
-    end.record(stream)
+    start.record(main)
+    for s_ in side + [down]:
+        s_.wait_stream(main)
+    for i in range(steps):
+        step(i)
+    for s_ in side + [down]:
+        main.wait_stream(s_)
+    end.record(main)
     torch.cuda.synchronize()
     barrier()
     ms = start.elapsed_time(end)
-    del host, dev, out
+    del host, devs, outs
     torch.cuda.empty_cache()
     return ms, h2d, d2h
 
