@@ -273,3 +273,23 @@ def test_tiny_pass_changes_no_output_for_eps_from_2_pow_minus_50(eps, path):
     g = parity.run_fused(d, prefill="sentinel", **kw)
     for key in ("out", "residual_out", "ss"):
         assert np.array_equal(g[key].view(np.uint8), runs[1][key].view(np.uint8)), key
+
+
+@pytest.mark.parametrize("single", [False, True])
+def test_tiny_rows_with_eps_zero_through_the_pieces(single):
+    """The epilogue pieces (norm_only, residual_norm_only) on the FP32 sum of
+    rows of tiny values at eps = 0: their kernels with the second pass meet the
+    oracle within one subnormal step, as the fused entry points do."""
+    d = inputs.edge_inputs("reduce_norm", 4, 5120, TINY_KINDS, seed=730, eps=0.0)
+    ref = parity.run_oracle(d, single=single)
+    s = bn.reduce_only(d["partials"])
+    res = d["residual"].clone()
+    ss = parity._sentinel_like((d["T"], 2), torch.float32)
+    if single:
+        out = bn.residual_norm_only(s, res, d["gamma_pre"], d["eps"], debug=bn.Debug(ss=ss))
+    else:
+        out = bn.norm_only(s, res, d["gamma_post"], d["gamma_pre"], d["eps"], debug=bn.Debug(ss=ss))
+    assert bn.check_device_error() == 0
+    g = {"sum": s.cpu().numpy(), "ss": ss.cpu().numpy(), "out": inputs.u16(out),
+         "residual_out": inputs.u16(res)}
+    parity.compare(g, ref, what=f"tiny eps=0 pieces single={single}", ss_floor=SUBNORMAL_STEP)
