@@ -265,8 +265,18 @@ __global__ void __launch_bounds__(kClusterThreads, 1) bn_cluster_fin_kernel(cons
         }
     }
     griddep_launch_dependents();
-    // no CTA leaves while a remote store of the exchanges may still target it
-    if (cs > 1) cluster_sync_all();
+    // The only accesses to another CTA's shared memory are remote stores (and
+    // their byte counts) into the exchange slots, and every CTA waits for all
+    // of those addressed to it before it gets here.  So a CTA leaves without a
+    // cluster barrier (measured: 0.2 to 0.3 us less per call at few rows).
+    // If one of its exchange waits gave up, stores from the other CTAs may
+    // still be on their way: the threads that see it stay for the bounded
+    // wait limit before leaving, and the CTA's shared memory lives as long as
+    // they do.
+    if (cs > 1 && (*(volatile int *)&s_abort & kAbortDsmem)) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < kWaitLimitCycles) __nanosleep(1000);
+    }
 }
 
 template <bool FIN, bool POSTNORM, bool TINY>
