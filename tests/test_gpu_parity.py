@@ -467,6 +467,24 @@ def test_narrow_finalize_rows_match_oracle(R, T, k, H, single):
     parity.compare(g, parity.run_oracle(d, single=single), what=f"narrow finalize R={R} T={T} k={k} H={H}")
 
 
+LIGHT_REDUCE = [
+    # (R, T, H): light rows with more rows than SMs take 128-thread CTAs with up
+    # to 4 chunks each; ragged widths leave the last thread's chunks short
+    (2, 300, 2048), (4, 333, 4096), (2, 200, 7168), (3, 400, 2056), (4, 170, 3000),
+    (1, 257, 8192),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("single", [False, True])
+@pytest.mark.parametrize("R,T,H", LIGHT_REDUCE)
+def test_light_reduce_rows_match_oracle(R, T, H, single):
+    wl = inputs.custom("reduce_norm", R, H, partial_std=0.5, row_scale=True)
+    d = parity.gpu_inputs(wl, T, seed=3100 + R * 17 + T + H)
+    g = parity.run_fused(d, single=single)
+    parity.compare(g, parity.run_oracle(d, single=single), what=f"light reduce R={R} T={T} H={H}")
+
+
 @pytest.mark.gpu
 def test_every_piece_has_a_launch_up_to_its_maximum():
     """The unfused pieces serve rows the fused entry points decline: the
