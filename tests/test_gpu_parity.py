@@ -467,6 +467,21 @@ def test_narrow_finalize_rows_match_oracle(R, T, k, H, single):
     parity.compare(g, parity.run_oracle(d, single=single), what=f"narrow finalize R={R} T={T} k={k} H={H}")
 
 
+@pytest.mark.gpu
+@pytest.mark.parametrize("op,R,T,k,H", [
+    ("reduce_norm", 2, 200_000, 0, 64),            # about 1300 rows per CTA
+    ("finalize_reduce_norm", 2, 100_000, 2, 64),   # T * k = 200000 gathered rows per shard
+    ("reduce_norm", 3, 50_000, 0, 1000),           # ragged rows, several hundred per CTA
+])
+def test_many_token_rows_match_oracle(op, R, T, k, H):
+    """Long grid-stride loops: every CTA of the persistent grid walks hundreds
+    of rows, and the finalize's gather indices reach 200000 rows per shard."""
+    wl = inputs.custom(op, R, H, k, partial_std=0.5, shared_std=0.3)
+    d = parity.gpu_inputs(wl, T, seed=3200 + R + T)
+    g = parity.run_fused(d)
+    parity.compare(g, parity.run_oracle(d), what=f"{op} R={R} T={T} H={H}")
+
+
 LIGHT_REDUCE = [
     # (R, T, H): light rows with more rows than SMs take 128-thread CTAs with up
     # to 4 chunks each; ragged widths leave the last thread's chunks short
