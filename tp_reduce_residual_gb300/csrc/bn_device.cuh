@@ -343,7 +343,15 @@ __device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c)
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
     return r;
 }
-__device__ __forceinline__ f2 neg2(f2 a) { return a ^ 0x8000000080000000ull; }
+// -(a * b) rounded once (round to nearest even is symmetric, so this is the
+// negated product exactly); the negation is an operand modifier of the scalar
+// multiply, not an instruction of its own.
+__device__ __forceinline__ float mul_neg(float a, float b)
+{
+    float r;
+    asm("{\n\t.reg .f32 t;\n\tneg.f32 t, %2;\n\tmul.rn.f32 %0, %1, t;\n\t}" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
 
 // Exact widening of a word holding two BF16 values (low half -> low lane).
 __device__ __forceinline__ f2 widen2(uint32_t w)
@@ -415,14 +423,19 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
 // Two independent compensated accumulators (one per lane): (S, E) += x*x.
 // The product's rounding error comes from one explicit fma (it only measures
 // the error of the rounded product; no result value is contracted) and the
-// addition's error from two-sum; both are carried in E.
+// addition's error from two-sum; both are carried in E.  The product is
+// formed negated, np = -p, which the fma needs as its addend: the two-sum is
+// then written with np, S - np = S + p and -(np + bb) = p - bb, the same
+// roundings of the same values.
 __device__ __forceinline__ void acc_square2(f2 &S, f2 &E, f2 x)
 {
-    const f2 p = mul_sep2(x, x);
-    const f2 pe = fma2(x, x, neg2(p));
-    const f2 s = add2(S, p);
+    float x0, x1;
+    f2_split(x, x0, x1);
+    const f2 np = f2_make(mul_neg(x0, x0), mul_neg(x1, x1));
+    const f2 pe = fma2(x, x, np);
+    const f2 s = sub2(S, np);
     const f2 bb = sub2(s, S);
-    const f2 e = add2(sub2(S, sub2(s, bb)), sub2(p, bb));
+    const f2 e = sub2(sub2(S, sub2(s, bb)), add2(np, bb));
     S = s;
     E = add2(E, add2(e, pe));
 }
