@@ -252,28 +252,50 @@ __device__ __forceinline__ bool phase_done(uint32_t bar, uint32_t parity, bool s
 // abort bits.  The clock is read only after 1024 unsuccessful polls: a wait
 // that ends quickly costs nothing but the polls themselves.
 template <bool CLUSTER_ACQUIRE, int KIND>
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl &c)
+__device__ __forceinline__ bool wait_phase_loop(uint32_t bar, uint32_t parity, volatile int *abort,
+                                                unsigned *err, bool spin, uint32_t pipe_polls)
 {
     constexpr int kSkipOn = KIND == kPipe ? kAbortPipe : KIND == kDsmem ? kAbortDsmem : 0;
-    // a completed phase returns at once (its data is valid even in a CTA that
-    // is aborting); the abort bits are read only when the wait must poll
-    if (phase_done<CLUSTER_ACQUIRE>(bar, parity, c.spin)) return true;
-    if (kSkipOn != 0 && (*c.abort & kSkipOn)) return false;
-    const uint32_t limit = KIND == kPipe ? c.pipe_polls : kMaxSpins;
+    if (kSkipOn != 0 && (*abort & kSkipOn)) return false;
+    const uint32_t limit = KIND == kPipe ? pipe_polls : kMaxSpins;
     long long t0 = 0;
     for (uint32_t i = 1; i < limit; ++i) {
-        if (phase_done<CLUSTER_ACQUIRE>(bar, parity, c.spin)) return true;
+        if (phase_done<CLUSTER_ACQUIRE>(bar, parity, spin)) return true;
         if ((i & 1023u) == 0u) {
-            if (kSkipOn != 0 && (*c.abort & kSkipOn)) return false;
+            if (kSkipOn != 0 && (*abort & kSkipOn)) return false;
             if (i == 1024u)
                 t0 = clock64();
             else if (clock64() - t0 > kWaitLimitCycles)
                 break;
         }
     }
-    atomicOr(c.err, kErrTimeout);
-    atomicOr(const_cast<int *>(c.abort), KIND == kDsmem ? (kAbortPipe | kAbortDsmem) : kAbortPipe);
+    atomicOr(err, kErrTimeout);
+    atomicOr(const_cast<int *>(abort), KIND == kDsmem ? (kAbortPipe | kAbortDsmem) : kAbortPipe);
     return false;
+}
+
+// The polling loop as a function of its own.  Inlined at every wait it makes
+// a kernel's code several times larger than the SM's first-level instruction
+// cache; a call costs nothing while the phase is already complete, but the
+// call's register convention made the 4-chunk reduce kernels spill, so they
+// keep it inline (OUTLINE below).
+template <bool CLUSTER_ACQUIRE, int KIND>
+__device__ __noinline__ bool wait_phase_poll(uint32_t bar, uint32_t parity, volatile int *abort,
+                                             unsigned *err, bool spin, uint32_t pipe_polls)
+{
+    return wait_phase_loop<CLUSTER_ACQUIRE, KIND>(bar, parity, abort, err, spin, pipe_polls);
+}
+
+template <bool CLUSTER_ACQUIRE, int KIND, bool OUTLINE = true>
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl &c)
+{
+    // a completed phase returns at once (its data is valid even in a CTA that
+    // is aborting); the abort bits are read only when the wait must poll
+    if (phase_done<CLUSTER_ACQUIRE>(bar, parity, c.spin)) return true;
+    if constexpr (OUTLINE)
+        return wait_phase_poll<CLUSTER_ACQUIRE, KIND>(bar, parity, c.abort, c.err, c.spin, c.pipe_polls);
+    else
+        return wait_phase_loop<CLUSTER_ACQUIRE, KIND>(bar, parity, c.abort, c.err, c.spin, c.pipe_polls);
 }
 
 // ---- arithmetic helpers ----------------------------------------------------------
@@ -542,6 +564,7 @@ struct Smem {
 // Row-wide sum of squares: compensated pairs reduced over the warp, the
 // consumer warps of the CTA, then the CTAs of the cluster, in a fixed order;
 // every consumer thread of every CTA of the cluster gets the same value.
+template <bool OUTLINE>
 __device__ __forceinline__ float row_sum_squares(f2 S2, f2 E2, int &nred, const Smem &sm,
                                                  uint32_t cs, uint32_t q, int NT, int NW,
                                                  int warp, int lane, int tid, const Ctl &ctl,
@@ -572,7 +595,7 @@ __device__ __forceinline__ float row_sum_squares(f2 S2, f2 E2, int &nred, const 
             const uint32_t d = (uint32_t)tid;
             st_async_f2(mapa(smem_addr(slots + q), d), S, E, mapa(bar, d));
         }
-        if (!wait_phase<true, kDsmem>(bar, (uint32_t)(nred >> 1) & 1u, ctl)) live = false;
+        if (!wait_phase<true, kDsmem, OUTLINE>(bar, (uint32_t)(nred >> 1) & 1u, ctl)) live = false;
         S = slots[0].x;
         E = slots[0].y;
         for (uint32_t c = 1; c < cs; ++c) combine(S, E, slots[c].x, slots[c].y);
@@ -603,6 +626,9 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
     constexpr bool SUM_OUT = (MODE & F_SUM_OUT) != 0;
     constexpr bool Z_OUT = (MODE & F_Z_OUT) != 0;
     constexpr bool REDUCE = !Z_OUT;
+    // the waits' polling loops out of line, except in the 4-chunk kernels,
+    // whose registers the call's convention would spill
+    constexpr bool kOutline = CPT < 4;
 
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
@@ -723,7 +749,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                 // publish this row's gather indices and weights (all lanes)
                 bool got = true;
                 if (lane == 0)
-                    got = wait_phase<false, kPipe>(sm.mempty0 + 8u * slot,
+                    got = wait_phase<false, kPipe, kOutline>(sm.mempty0 + 8u * slot,
                                                   (((uint32_t)it >> 1) & 1u) ^ 1u, ctl);
                 got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
                 if (!got) {
@@ -758,7 +784,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                     const uint32_t fb = sm.full0 + 8u * stage;
                     if (pos == 0) {
                         n_in = items_in_stage(left);
-                        if (!wait_phase<false, kPipe>(sm.empty0 + 8u * stage, phase ^ 1u, ctl)) return false;
+                        if (!wait_phase<false, kPipe, kOutline>(sm.empty0 + 8u * stage, phase ^ 1u, ctl)) return false;
                         mbar_arrive_expect_tx(fb, bytes * (uint32_t)n_in);
                         ++issued;
                     }
@@ -816,7 +842,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
             if (pos != 0) {
                 // the armed stage never completes its byte count: give its
                 // issued copies the bounded time to land
-                wait_phase<false, kDrain>(sm.full0 + 8u * st, ph, ctl);
+                wait_phase<false, kDrain, kOutline>(sm.full0 + 8u * st, ph, ctl);
             }
             const uint32_t done_n = pos != 0 ? n - 1 : n;
             for (uint32_t i = 0; i < done_n; ++i) {
@@ -826,7 +852,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                 } else {
                     --st;
                 }
-                wait_phase<false, kDrain>(sm.full0 + 8u * st, ph, ctl);
+                wait_phase<false, kDrain, kOutline>(sm.full0 + 8u * st, ph, ctl);
             }
         }
     } else {
@@ -842,7 +868,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
         auto take = [&]() -> const uint8_t * {
             if (!FIN || cpos == 0) {
                 cn = items_in_stage(cleft);
-                if (!wait_phase<false, kPipe>(sm.full0 + 8u * stage, phase, ctl)) live = false;
+                if (!wait_phase<false, kPipe, kOutline>(sm.full0 + 8u * stage, phase, ctl)) live = false;
                 cbase = sm.stages + (size_t)stage * (size_t)a.stage_bytes;
             }
             return cbase + (size_t)cpos * item_bytes;
@@ -925,7 +951,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                 }
                 release();
             } else if constexpr (FIN && SPLITR) {
-                if (!wait_phase<false, kPipe>(sm.mfull0 + 8u * slot, ((uint32_t)it >> 1) & 1u, ctl))
+                if (!wait_phase<false, kPipe, kOutline>(sm.mfull0 + 8u * slot, ((uint32_t)it >> 1) & 1u, ctl))
                     live = false;
                 const float *wrow = sm.mw + slot * kMaxMeta;
                 // Each 16-byte chunk of every z_r this CTA finalizes goes
@@ -1012,7 +1038,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sm.mempty0 + 8u * slot);
                 if constexpr (REDUCE) {
-                    if (!wait_phase<true, kDsmem>(zready, (uint32_t)it & 1u, ctl)) live = false;
+                    if (!wait_phase<true, kDsmem, kOutline>(zready, (uint32_t)it & 1u, ctl)) live = false;
                     // rank-ordered sum of the R z rows over this CTA's slice,
                     // all from its own shared memory
 #pragma unroll
@@ -1025,7 +1051,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                     }
                 }
             } else if constexpr (FIN) {
-                if (!wait_phase<false, kPipe>(sm.mfull0 + 8u * slot, ((uint32_t)it >> 1) & 1u, ctl))
+                if (!wait_phase<false, kPipe, kOutline>(sm.mfull0 + 8u * slot, ((uint32_t)it >> 1) & 1u, ctl))
                     live = false;
                 const float *wrow = sm.mw + slot * kMaxMeta;
                 for (int r = 0; r < a.R; ++r) {
@@ -1146,7 +1172,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                             for (int m = 0; m < 4; ++m) acc_square2(S1, E1, s[i][m]);
                         }
                     }
-                    ss1 = row_sum_squares(S1, E1, nred, sm, cs, q, NT, NW, warp, lane, tid, ctl, live);
+                    ss1 = row_sum_squares<kOutline>(S1, E1, nred, sm, cs, q, NT, NW, warp, lane, tid, ctl, live);
                     if (TINY && needs_rescale(ss1)) {  // the same on every thread of the cluster
                         const int kx = rescale_exp(ss1);
                         const float up = pow2f(kx);
@@ -1159,7 +1185,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                                 for (int m = 0; m < 4; ++m) acc_square_scaled(Sb, Eb, s[i][m], up);
                             }
                         }
-                        const float r = row_sum_squares(f2_make(Sb, 0.f), f2_make(Eb, 0.f), nred, sm, cs, q,
+                        const float r = row_sum_squares<kOutline>(f2_make(Sb, 0.f), f2_make(Eb, 0.f), nred, sm, cs, q,
                                                         NT, NW, warp, lane, tid, ctl, live);
                         ss1 = mul_sep(mul_sep(r, pow2f(-kx)), pow2f(-kx));
                     }
@@ -1194,7 +1220,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                     }
                     release();
                 }
-                float ss2 = row_sum_squares(S2, E2, nred, sm, cs, q, NT, NW, warp, lane, tid, ctl, live);
+                float ss2 = row_sum_squares<kOutline>(S2, E2, nred, sm, cs, q, NT, NW, warp, lane, tid, ctl, live);
                 if (TINY && needs_rescale(ss2)) {  // the same on every thread of the cluster
                     const int kx = rescale_exp(ss2);
                     const float up = pow2f(kx);
@@ -1207,7 +1233,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                             for (int m = 0; m < 4; ++m) acc_square_scaled(Sb, Eb, s[i][m], up);
                         }
                     }
-                    const float r = row_sum_squares(f2_make(Sb, 0.f), f2_make(Eb, 0.f), nred, sm, cs, q,
+                    const float r = row_sum_squares<kOutline>(f2_make(Sb, 0.f), f2_make(Eb, 0.f), nred, sm, cs, q,
                                                     NT, NW, warp, lane, tid, ctl, live);
                     ss2 = mul_sep(mul_sep(r, pow2f(-kx)), pow2f(-kx));
                 }
