@@ -82,7 +82,9 @@ def _guarded_outputs(op, d):
 
 
 # Rings of two stages (one copy each where rows are few) make the consumers
-# wait for copies in flight, so that a one-poll limit certainly expires.
+# wait for copies in flight, and the waits probe with the non-suspending
+# test_wait (wait_mode 2): a suspending first probe may sleep until the copy
+# lands, so that a one-poll limit would expire only when the copies are slow.
 CASES = [
     # (id, op, R, T, k, H, tuning)
     ("finalize-columns", "finalize_reduce_norm", 8, 40, 10, 8192, dict(split=1, cluster_size=1)),
@@ -124,7 +126,7 @@ def test_expired_waits_report_a_timeout_and_leave_the_context_usable(case):
     torch.cuda.synchronize()
     bits = 0
     try:
-        bn.set_tuning(wait_limit_polls=1, **tuning)
+        bn.set_tuning(wait_limit_polls=1, wait_mode=2, **tuning)
         for _ in range(ATTEMPTS):
             bufs, guards = _guarded_outputs(op, d)
             _call(op, d, bufs)
