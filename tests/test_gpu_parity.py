@@ -610,6 +610,28 @@ def test_cluster_task_split_matches_oracle(R, T, k, H, with_shared, single, cs):
     parity.compare(g, parity.run_oracle(d, single=single), what=f"cluster tasks R={R} T={T} H={H}")
 
 
+@pytest.mark.parametrize("k", [1, 3, 4, 5, 7, 8, 9, 10, 11, 15, 16])
+def test_cluster_task_unroll_widths_match_oracle(k):
+    """The cluster path's finalize tasks are compiled for 4, 8, 10 and 16
+    expert slots, and a call takes the smallest that holds k: every k at and
+    on either side of those widths gives the finalize and sum bits of the
+    forced column split, and the oracle's results."""
+    R, T, H = 4, 3, 2048
+    wl = inputs.custom("finalize_reduce_norm", R, H, k, partial_std=0.3, shared_std=0.3)
+    d = parity.gpu_inputs(wl, T, seed=1200 + k, with_shared=True)
+    try:
+        bn.set_tuning(split=3, cluster_size=4)
+        assert bn.launch_info("finalize_reduce_norm", R, T, H, k)["split"] == 2
+        g = parity.run_fused(d)
+        bn.set_tuning(split=1)
+        base = parity.run_fused(d)
+    finally:
+        bn.set_tuning()
+    for key in ("sum", "z"):  # the row reductions' trees differ between the splits
+        assert_bits_equal(g[key], base[key], f"k={k} {key}")
+    parity.compare(g, parity.run_oracle(d), what=f"cluster tasks k={k}")
+
+
 @pytest.mark.parametrize("R,T,k,H,cs", [
     (8, 16, 8, 2048, 4), (8, 32, 8, 2048, 4), (8, 64, 8, 2048, 2), (4, 32, 8, 4096, 4),
     (2, 32, 8, 7168, 4), (8, 16, 10, 8192, 0), (8, 64, 8, 4096, 0), (8, 16, 8, 6144, 0),

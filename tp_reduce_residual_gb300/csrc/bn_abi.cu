@@ -697,7 +697,7 @@ bool plan_cluster_fin(int mode, const Args &a, const DeviceInfo *d, ClusterPlan 
         const size_t smem = cluster_smem_bytes(a.R, slice);
         if ((long long)smem > (long long)d->smem_optin - 2048) continue;
         cudaError_t e = cudaSuccess;
-        const int res = cluster_fin_resident(fin, (mode & F_POSTNORM) != 0, tpt,
+        const int res = cluster_fin_resident(fin, a.k, (mode & F_POSTNORM) != 0, tpt,
                                              tiny_for(mode, a.eps) != 0, cs, smem, &e);
         if (e != cudaSuccess) {
             cudaGetLastError();

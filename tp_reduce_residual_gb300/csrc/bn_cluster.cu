@@ -82,9 +82,12 @@ __device__ __forceinline__ void gamma8_regs(const float *g, f2 *out)
 // task % slice.  A task finalizes that chunk of that shard (FIN), or copies the
 // shard's partial chunk (the reduce entry points).  The first `slice` threads
 // then run the epilogue, one chunk each.
-template <bool FIN, bool POSTNORM, int TPT, bool TINY>
+// KU: the expert slots a finalize task unrolls (k <= KU), 0 for the reduce
+// entry points (cluster_slots).
+template <int KU, bool POSTNORM, int TPT, bool TINY>
 __global__ void __launch_bounds__(kClusterThreads, 1) bn_cluster_fin_kernel(const ClusterArgs ca)
 {
+    constexpr bool FIN = KU > 0;
     const Args &a = ca.a;
     extern __shared__ __align__(16) uint4 zsm[];  // [R][slice] BF16 finalize results
     // four row reductions at most: ss1, its rescale, ss2, its rescale; each
@@ -106,6 +109,13 @@ __global__ void __launch_bounds__(kClusterThreads, 1) bn_cluster_fin_kernel(cons
     const size_t H = (size_t)a.H;
     const uint32_t xb[4] = {smem_addr(&xbar[0]), smem_addr(&xbar[1]), smem_addr(&xbar[2]),
                             smem_addr(&xbar[3])};
+    // A kernel unrolled for fewer slots than k (the host never launches one)
+    // returns at once, before any barrier, with the error bit set.
+    if (FIN && a.k > KU) {
+        griddep_wait();
+        if (tid == 0) atomicOr(a.err, kErrTimeout);
+        return;
+    }
 
     if (tid == 0) {
         for (int i = 0; i < 4; ++i) mbar_init(xb[i], 1u);
@@ -145,10 +155,10 @@ __global__ void __launch_bounds__(kClusterThreads, 1) bn_cluster_fin_kernel(cons
             const int r = task / slice;
             const int lc = task - r * slice;
             const size_t meta = ((size_t)r * a.T + t) * (size_t)a.k;
-            uint4 x[kMaxK];
-            float wj[kMaxK];
+            uint4 x[KU > 0 ? KU : 1];
+            float wj[KU > 0 ? KU : 1];
 #pragma unroll
-            for (int j = 0; j < kMaxK; ++j) {
+            for (int j = 0; j < KU; ++j) {
                 if (j < a.k) {
                     int p = __ldg(a.perm + meta + j);
                     if (p < 0 || (long long)p >= rows) {
@@ -173,7 +183,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1) bn_cluster_fin_kernel(cons
                 for (int m = 0; m < 4; ++m) acc[m] = mul_sep2(w2, v[m]);
             }
 #pragma unroll
-            for (int j = 1; j < kMaxK; ++j) {
+            for (int j = 1; j < KU; ++j) {
                 if (j < a.k) {
                     f2 v[4];
                     widen8(x[j], v);
@@ -279,26 +289,41 @@ __global__ void __launch_bounds__(kClusterThreads, 1) bn_cluster_fin_kernel(cons
     }
 }
 
-template <bool FIN, bool POSTNORM, bool TINY>
+template <int KU, bool POSTNORM, bool TINY>
 const void *cluster_kernel(int tpt)
 {
     switch (tpt) {
-    case 1: return reinterpret_cast<const void *>(&bn_cluster_fin_kernel<FIN, POSTNORM, 1, TINY>);
-    case 2: return reinterpret_cast<const void *>(&bn_cluster_fin_kernel<FIN, POSTNORM, 2, TINY>);
+    case 1: return reinterpret_cast<const void *>(&bn_cluster_fin_kernel<KU, POSTNORM, 1, TINY>);
+    case 2: return reinterpret_cast<const void *>(&bn_cluster_fin_kernel<KU, POSTNORM, 2, TINY>);
     default: return nullptr;
     }
 }
 
-template <bool TINY>
-const void *cluster_kernel(bool fin, bool postnorm, int tpt)
+template <int KU, bool TINY>
+const void *cluster_kernel(bool postnorm, int tpt)
 {
-    return fin ? (postnorm ? cluster_kernel<true, true, TINY>(tpt) : cluster_kernel<true, false, TINY>(tpt))
-               : (postnorm ? cluster_kernel<false, true, TINY>(tpt) : cluster_kernel<false, false, TINY>(tpt));
+    return postnorm ? cluster_kernel<KU, true, TINY>(tpt) : cluster_kernel<KU, false, TINY>(tpt);
 }
+
+template <bool TINY>
+const void *cluster_kernel(int ku, bool postnorm, int tpt)
+{
+    switch (ku) {
+    case 0: return cluster_kernel<0, TINY>(postnorm, tpt);
+    case 4: return cluster_kernel<4, TINY>(postnorm, tpt);
+    case 8: return cluster_kernel<8, TINY>(postnorm, tpt);
+    case 10: return cluster_kernel<10, TINY>(postnorm, tpt);
+    case kMaxK: return cluster_kernel<kMaxK, TINY>(postnorm, tpt);
+    default: return nullptr;
+    }
+}
+
+// position of a slot count in the table above
+int slots_index(int ku) { return ku == 0 ? 0 : ku == 4 ? 1 : ku == 8 ? 2 : ku == 10 ? 3 : 4; }
 
 // Function attributes are per device: dynamic shared memory above the 48 KB
 // default and cluster sizes above 8, set once per kernel and device.
-std::atomic<unsigned> g_cluster_ready[64];
+std::atomic<unsigned long long> g_cluster_ready[64];
 
 cudaError_t prepare_cluster(const void *fn, int bit)
 {
@@ -306,7 +331,7 @@ cudaError_t prepare_cluster(const void *fn, int bit)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (g_cluster_ready[dev].load(std::memory_order_acquire) & (1u << bit)) return cudaSuccess;
+    if (g_cluster_ready[dev].load(std::memory_order_acquire) & (1ull << bit)) return cudaSuccess;
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
@@ -318,18 +343,19 @@ cudaError_t prepare_cluster(const void *fn, int bit)
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    g_cluster_ready[dev].fetch_or(1u << bit, std::memory_order_acq_rel);
+    g_cluster_ready[dev].fetch_or(1ull << bit, std::memory_order_acq_rel);
     return cudaSuccess;
 }
 
-const void *kernel_for(bool fin, bool postnorm, int tpt, bool tiny, cudaError_t *e)
+const void *kernel_for(int ku, bool postnorm, int tpt, bool tiny, cudaError_t *e)
 {
-    const void *fn = tiny ? cluster_kernel<true>(fin, postnorm, tpt) : cluster_kernel<false>(fin, postnorm, tpt);
+    const void *fn = tiny ? cluster_kernel<true>(ku, postnorm, tpt) : cluster_kernel<false>(ku, postnorm, tpt);
     if (!fn) {
         *e = cudaErrorInvalidValue;
         return nullptr;
     }
-    *e = prepare_cluster(fn, (tiny ? 8 : 0) + (fin ? 4 : 0) + (postnorm ? 2 : 0) + (tpt == 2 ? 1 : 0));
+    *e = prepare_cluster(fn, ((slots_index(ku) * 2 + (tiny ? 1 : 0)) * 2 + (postnorm ? 1 : 0)) * 2 +
+                                 (tpt == 2 ? 1 : 0));
     return *e == cudaSuccess ? fn : nullptr;
 }
 
@@ -362,10 +388,11 @@ cudaError_t launch_cluster_fin(const ClusterArgs &c, bool fin, bool postnorm, in
                                bool pdl, cudaStream_t st)
 {
     if (cs < 1 || cs > kMaxCluster || c.a.T < 1 || c.a.nchunks < cs ||
-        c.tasks > kClusterThreads * tpt || (c.a.nchunks + cs - 1) / cs > kClusterThreads)
+        c.tasks > kClusterThreads * tpt || (c.a.nchunks + cs - 1) / cs > kClusterThreads ||
+        (fin && (c.a.k < 1 || c.a.k > kMaxK)))
         return cudaErrorInvalidValue;
     cudaError_t e;
-    const void *fn = dev::kernel_for(fin, postnorm, tpt, c.a.tiny != 0, &e);
+    const void *fn = dev::kernel_for(cluster_slots(fin, c.a.k), postnorm, tpt, c.a.tiny != 0, &e);
     if (!fn) return e;
     const int slice = (c.a.nchunks + cs - 1) / cs;
     cudaLaunchConfig_t cfg;
@@ -375,10 +402,10 @@ cudaError_t launch_cluster_fin(const ClusterArgs &c, bool fin, bool postnorm, in
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-int cluster_fin_resident(bool fin, bool postnorm, int tpt, bool tiny, int cs, size_t smem,
+int cluster_fin_resident(bool fin, int k, bool postnorm, int tpt, bool tiny, int cs, size_t smem,
                          cudaError_t *err)
 {
-    const void *fn = dev::kernel_for(fin, postnorm, tpt, tiny, err);
+    const void *fn = dev::kernel_for(cluster_slots(fin, k), postnorm, tpt, tiny, err);
     if (!fn) return 0;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];

@@ -30,19 +30,30 @@ struct ClusterArgs {
     int tasks;     // R * largest slice: the finalize tasks of one CTA
 };
 
+// Expert slots a finalize task unrolls (its k gathers all in flight): the
+// smallest of 4, 8, 10 and 16 that holds k; 0 for the reduce entry points.  A
+// kernel unrolled for 16 slots was 11 to 28 % more code than one for 10, and
+// at a few rows, whose code runs once per call, the smaller kernels were 4 to
+// 10 % faster (C4 T=1 5.29 -> 5.07 us, R=4 k=8 T=1 4.02 -> 3.63).
+inline int cluster_slots(bool fin, int k)
+{
+    return !fin ? 0 : k <= 4 ? 4 : k <= 8 ? 8 : k <= 10 ? 10 : kMaxK;
+}
+
 // Dynamic shared memory: the slice's finalize results, [R][slice] 16-byte chunks.
 inline size_t cluster_smem_bytes(int R, int slice) { return (size_t)R * (size_t)slice * 16u; }
 
 // Enqueue one cluster of cs CTAs per token row (grid T * cs).  fin selects the
-// finalize tasks (expert rows) or the partial rows of the reduce entry points;
-// postnorm the sandwich or the single pre-RMSNorm; tpt is 1 or 2.
+// finalize tasks (expert rows, c.a.k of them a task) or the partial rows of the
+// reduce entry points; postnorm the sandwich or the single pre-RMSNorm; tpt is
+// 1 or 2.
 cudaError_t launch_cluster_fin(const ClusterArgs &c, bool fin, bool postnorm, int tpt, int cs,
                                bool pdl, cudaStream_t st);
 
 // Clusters of this shape the device holds at once (0 if none), for the planner;
 // tiny selects the kernel with the second pass over rows of tiny values
 // (Args::tiny), which launch_cluster_fin takes from c.a.tiny.
-int cluster_fin_resident(bool fin, bool postnorm, int tpt, bool tiny, int cs, size_t smem,
+int cluster_fin_resident(bool fin, int k, bool postnorm, int tpt, bool tiny, int cs, size_t smem,
                          cudaError_t *err);
 
 }  // namespace bn
