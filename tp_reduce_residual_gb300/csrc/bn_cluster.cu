@@ -39,7 +39,7 @@ __device__ __forceinline__ void epilogue_sync(int nthreads)
 // pairs exchanged across the cluster and combined by the same tree (lane d
 // holding CTA d's).  Every epilogue thread of every CTA gets the same value.
 // The trees pad with zero pairs, which two-sum adds exactly; they replace
-// loops over the pairs that the compiler unrolled into a third of the
+// loops over the pairs that the compiler unrolled into about a fifth of the
 // kernels' code.
 __device__ __forceinline__ float row_sum_squares_cl(f2 S2, f2 E2, float2 *red, float2 *xslot,
                                                     uint32_t xbar, uint32_t cs, uint32_t q,
