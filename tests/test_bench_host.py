@@ -94,3 +94,23 @@ def test_kernel_hash_ignores_comments_only():
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only(a) != bench._code_only(c)
     assert bench._code_only('const char *s = "a // b";') == 'const char *s = "a // b";'
+
+
+def test_headline_rotates_input_sets_below_twice_l2():
+    """The headline loop replays one input set only when a call's inputs are
+    at least twice L2; a smaller workload rotates over enough sets to pass 8x
+    L2 (at most 64), and the config says which."""
+    l2 = 136 * 1024 * 1024
+    wl, T = bench.parse_workload("C4:1024")
+    B = bench.workload_bytes(wl, T)
+    assert bench.headline_sets(B, l2) == 1
+    assert bench.l2_label(B, l2).endswith("no flush") and "> L2" in bench.l2_label(B, l2)
+    wl, T = bench.parse_workload("C2:256")
+    B = bench.workload_bytes(wl, T)
+    n = bench.headline_sets(B, l2)
+    assert n > 1 and n * B >= 8 * l2 and (n - 1) * B < 8 * l2
+    assert "rotate over" in bench.l2_label(B, l2) and "warm" not in bench.l2_label(B, l2)
+    wl, T = bench.parse_workload("C4:1")
+    B = bench.workload_bytes(wl, T)
+    assert bench.headline_sets(B, l2) == 64
+    assert "partly L2-warm" in bench.l2_label(B, l2)
