@@ -30,10 +30,18 @@ struct ClusterArgs {
     int tasks;     // R * largest slice: the finalize tasks of one CTA
 };
 
-// Expert slots a finalize task unrolls (unrolled_slots; measured here: C4 T=1
-// 5.29 -> 5.07 us, R=4 k=8 T=1 4.02 -> 3.63 against 16 slots); 0 for the
-// reduce entry points.
-inline int cluster_slots(bool fin, int k) { return fin ? unrolled_slots(k) : 0; }
+// Expert slots a finalize task unrolls so that all its k gathers are in
+// flight: the smallest of 4, 8, 10 and 16 that holds k; 0 for the reduce entry
+// points.  A kernel unrolled for 16 slots was 11 to 28 % more code than one
+// for 10, and at a few rows, where the kernel's code runs about once per call,
+// the smaller kernels were 4 to 10 % faster on GB300 (C4 T=1 5.29 -> 5.07 us,
+// R=4 k=8 T=1 4.02 -> 3.63).  (The many-CTA finalize with a workspace, its
+// time set by the hand-off of each row between CTAs through global memory,
+// showed no consistent gain and keeps 16.)
+inline int cluster_slots(bool fin, int k)
+{
+    return !fin ? 0 : k <= 4 ? 4 : k <= 8 ? 8 : k <= 10 ? 10 : kMaxK;
+}
 
 // Dynamic shared memory: the slice's finalize results, [R][slice] 16-byte chunks.
 inline size_t cluster_smem_bytes(int R, int slice) { return (size_t)R * (size_t)slice * 16u; }

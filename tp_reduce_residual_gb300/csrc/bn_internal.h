@@ -32,15 +32,6 @@ constexpr int kModeResNormOnly = F_SUM_IN | F_RESNORM;
 constexpr int kMaxR = 16;
 constexpr int kMaxK = 16;
 constexpr int kMaxMeta = 256;        // R * k slots staged per token row
-
-// Expert slots a cluster-path finalize task unrolls so that all its k gathers
-// are in flight: the smallest of 4, 8, 10 and 16 that holds k.  A kernel
-// unrolled for 16 slots was 11 to 28 % more code than one for 10, and at a
-// few rows, where the kernel's code runs about once per call, the smaller
-// kernels were 4 to 10 % faster on GB300.  (The many-CTA finalize with a
-// workspace, its time set by the hand-off of each row between CTAs through
-// global memory, showed no consistent gain and keeps 16.)
-inline int unrolled_slots(int k) { return k <= 4 ? 4 : k <= 8 ? 8 : k <= 10 ? 10 : kMaxK; }
 constexpr int kMaxH = 32768;         // fused entry points (whole-row epilogue in one launch)
 constexpr int kMaxPieceH = 131072;   // unfused pieces (the fallback when a fused call declines)
 constexpr int kMaxConsumers = 512;   // consumer threads per CTA
