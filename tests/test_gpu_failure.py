@@ -92,7 +92,7 @@ CASES = [
      dict(split=2, cluster_size=8, stages=2, group=1)),
     ("finalize-columns-x4", "finalize_reduce_norm", 8, 6, 8, 6144,
      dict(split=1, cluster_size=4, stages=2, group=1)),
-    ("reduce-columns-x8", "reduce_norm", 8, 16, 0, 8192, dict(cluster_size=8, stages=2)),
+    ("reduce-columns-x8", "reduce_norm", 8, 16, 0, 8192, dict(split=1, cluster_size=8, stages=2)),
     ("reduce-rows-per-cta", "reduce_norm", 4, 1024, 0, 5120, dict(stages=2)),
     ("finalize-only-shards-x4", "finalize_only", 8, 4, 10, 8192,
      dict(split=2, cluster_size=4, stages=2, group=1)),

@@ -652,6 +652,17 @@ constexpr int kClusterFinMaxT = 15;
 // R=2, H=256 at T=8 2.60 / 2.83 (4); every case slower at T=64.
 constexpr int kClusterReduceMaxT = 8;
 constexpr int kClusterReduceMinTasks = 256;
+// Past kClusterReduceMaxT rows, up to kClusterReduceMidMaxT, the reduce rows
+// keep the cluster path with clusters of at most kClusterReduceMidMaxCs CTAs,
+// all resident at once.  Measured on GB300 after the cluster kernels shrank
+// (us per call, CUDA graph, L2-cold; main kernel / clusters of 8): R=8,
+// H=8192 at T=16 5.52 / 4.61, T=24 5.37 / 4.88, T=32 5.90 / 4.96; R=4,
+// H=5120 at T=16 3.69 / 3.05, T=32 4.49 / 4.16; R=8, H=4096 at T=16 5.05 /
+// 3.44; R=2, H=8192 at T=16 3.40 / 3.11.  Clusters of 16 fell off between 192
+// and 256 CTAs (R=8, H=8192: T=12 4.15, T=16 7.83), and at T=48 the clusters
+// of 8 no longer fit at once (9.73 against 5.91).
+constexpr int kClusterReduceMidMaxT = 32;
+constexpr int kClusterReduceMidMaxCs = 8;
 // Past kClusterFinMaxT rows the fused finalize entries keep the cluster path
 // for narrow rows only: clusters of at most kClusterMidMaxCs CTAs whose
 // CTAs, one per SM, hold all T rows at once with at most two tasks a thread.
@@ -671,7 +682,8 @@ struct ClusterPlan {
 // (shard, chunk) tasks per thread (reduce rows: at least 256 tasks a CTA) and
 // whose clusters the device holds at once for the T rows (on request, any
 // cluster that is resident at all); past kClusterFinMaxT finalize rows, a
-// cluster of at most kClusterMidMaxCs CTAs with T * cs CTAs on distinct SMs.
+// cluster of at most kClusterMidMaxCs CTAs with T * cs CTAs on distinct SMs;
+// past kClusterReduceMaxT reduce rows, one of at most kClusterReduceMidMaxCs.
 bool plan_cluster_fin(int mode, const Args &a, const DeviceInfo *d, ClusterPlan *p)
 {
     const bool fin = (mode & F_FIN) != 0;
@@ -681,13 +693,15 @@ bool plan_cluster_fin(int mode, const Args &a, const DeviceInfo *d, ClusterPlan 
     const int pref = g_tune_split.load();
     if (pref != 0 && pref != 3) return false;
     const bool mid = fin && pref == 0 && a.T > kClusterFinMaxT;
-    if (pref == 0 && !fin && a.T > kClusterReduceMaxT) return false;
+    const bool mid_reduce = !fin && pref == 0 && a.T > kClusterReduceMaxT;
+    if (mid_reduce && a.T > kClusterReduceMidMaxT) return false;
     if (mid && (long long)a.T * 2 > d->sms) return false;
     const int want_cs = g_tune_cluster.load();
     const int nch = a.H / 8;
     for (int cs = mid ? kClusterMidMaxCs : kMaxCluster; cs >= 2; cs /= 2) {
         if (want_cs > 0 && cs != want_cs) continue;
         if (mid && (long long)a.T * cs > d->sms) continue;
+        if (mid_reduce && cs > kClusterReduceMidMaxCs) continue;
         const int slice = (nch + cs - 1) / cs;
         if (nch < cs || slice > kClusterThreads) continue;
         const int tasks = a.R * slice;
