@@ -694,6 +694,29 @@ def test_cluster_split_of_reduce_rows_matches_oracle(R, T, H, single, cs):
     parity.compare(g, parity.run_oracle(d, single=single), what=f"cluster reduce R={R} T={T} H={H}")
 
 
+@pytest.mark.parametrize("R,T,H", [(8, 9, 8192), (8, 16, 8192), (8, 32, 8192), (4, 24, 5120),
+                                   (8, 20, 4096), (2, 16, 8192)])
+def test_reduce_rows_keep_the_cluster_path_to_32_rows(R, T, H):
+    """Past 8 token rows the planner keeps heavy reduce rows on the cluster
+    path, with clusters of at most 8 CTAs all resident at once: the forced
+    column split's sum bits and the oracle's results."""
+    wl = inputs.custom("reduce_norm", R, H, partial_std=0.5, row_scale=True)
+    d = parity.gpu_inputs(wl, T, seed=870 + R * 7 + T + H)
+    info = bn.launch_info("reduce_norm", R, T, H)
+    assert info["split"] == 2 and info["cluster_size"] <= 8, info
+    assert info["resident_ctas"] >= info["grid"] == T * info["cluster_size"], info
+    g = parity.run_fused(d)
+    try:
+        bn.set_tuning(split=1)
+        base = parity.run_fused(d)
+    finally:
+        bn.set_tuning()
+    assert_bits_equal(g["sum"], base["sum"], "sum")
+    parity.compare(g, parity.run_oracle(d), what=f"cluster reduce R={R} T={T} H={H}")
+    # past 32 rows the main kernel again
+    assert bn.launch_info("reduce_norm", R, 33, H)["split"] != 2
+
+
 def test_cluster_task_split_flags_bad_perm_and_stays_in_bounds():
     R, T, k, H = 4, 5, 3, 1000
     wl = inputs.custom("finalize_reduce_norm", R, H, k, partial_std=0.3)
