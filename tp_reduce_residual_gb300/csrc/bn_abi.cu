@@ -660,7 +660,10 @@ constexpr int kClusterReduceMinTasks = 256;
 // H=5120 at T=16 3.69 / 3.05, T=32 4.49 / 4.16; R=8, H=4096 at T=16 5.05 /
 // 3.44; R=2, H=8192 at T=16 3.40 / 3.11.  Clusters of 16 fell off between 192
 // and 256 CTAs (R=8, H=8192: T=12 4.15, T=16 7.83), and at T=48 the clusters
-// of 8 no longer fit at once (9.73 against 5.91).
+// of 8 no longer fit at once (9.73 against 5.91).  Over R in {2, 4, 8}, H from
+// 2048 to 12288 and T in {9, 12, 16, 24, 32} the rule lost to the main
+// kernel by more than 3 % only at R=4, H=12288, T=24 and 32 (5.32 / 4.83,
+// 5.50 / 4.96).
 constexpr int kClusterReduceMidMaxT = 32;
 constexpr int kClusterReduceMidMaxCs = 8;
 // Past kClusterFinMaxT rows the fused finalize entries keep the cluster path
