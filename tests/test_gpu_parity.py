@@ -717,6 +717,27 @@ def test_reduce_rows_keep_the_cluster_path_to_32_rows(R, T, H):
     assert bn.launch_info("reduce_norm", R, 33, H)["split"] != 2
 
 
+@pytest.mark.parametrize("T", [1, 4, 12])
+def test_light_reduce_rows_take_clusters_of_8_to_12_rows(T):
+    """Rows of two shards of 5120 (640 chunks) take clusters of 8 CTAs at 160
+    tasks a CTA up to 12 token rows, and clusters of 4 past them: the forced
+    column split's sum bits and the oracle's results."""
+    R, H = 2, 5120
+    wl = inputs.custom("reduce_norm", R, H, partial_std=0.5, row_scale=True)
+    d = parity.gpu_inputs(wl, T, seed=910 + T)
+    info = bn.launch_info("reduce_norm", R, T, H)
+    assert info["split"] == 2 and info["cluster_size"] == 8 and info["grid"] == 8 * T, info
+    g = parity.run_fused(d)
+    try:
+        bn.set_tuning(split=1)
+        base = parity.run_fused(d)
+    finally:
+        bn.set_tuning()
+    assert_bits_equal(g["sum"], base["sum"], "sum")
+    parity.compare(g, parity.run_oracle(d), what=f"light cluster reduce R={R} T={T} H={H}")
+    assert bn.launch_info("reduce_norm", R, 13, H)["cluster_size"] == 4
+
+
 def test_cluster_task_split_flags_bad_perm_and_stays_in_bounds():
     R, T, k, H = 4, 5, 3, 1000
     wl = inputs.custom("finalize_reduce_norm", R, H, k, partial_std=0.3)

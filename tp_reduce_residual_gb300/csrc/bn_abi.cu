@@ -666,6 +666,16 @@ constexpr int kClusterReduceMinTasks = 256;
 // 5.50 / 4.96).
 constexpr int kClusterReduceMidMaxT = 32;
 constexpr int kClusterReduceMidMaxCs = 8;
+// Up to kClusterReduceMinTasks8MaxT rows, clusters of 8 take reduce rows down
+// to kClusterReduceMinTasks8 tasks a CTA: R=2 rows of 5120 and 7168 (160 and
+// 224 tasks) then take 8 CTAs instead of 4 (us per call: H=5120 T=1 2.90 ->
+// 2.73, T=4 2.93 -> 2.79, T=12 3.02 -> 2.92; H=7168 T=2 2.95 -> 2.79, T=8
+// 3.06 -> 2.89).  Past 12 rows the gain is gone (T=16: H=5120 3.04 -> 2.96,
+// H=7168 3.09 -> 3.15; T=32, H=7168: 4.12 -> 4.21), and a cluster of 16
+// below 256 tasks was slower from T=4 (R=4, H=5120, T=8: 3.16 against 2.96
+// with 8).
+constexpr int kClusterReduceMinTasks8 = 128;
+constexpr int kClusterReduceMinTasks8MaxT = 12;
 // Past kClusterFinMaxT rows the fused finalize entries keep the cluster path
 // for narrow rows only: clusters of at most kClusterMidMaxCs CTAs whose
 // CTAs, one per SM, hold all T rows at once with at most two tasks a thread.
@@ -682,7 +692,8 @@ struct ClusterPlan {
 };
 
 // The largest cluster (16, 8, 4 or 2 CTAs) whose CTAs take at most two
-// (shard, chunk) tasks per thread (reduce rows: at least 256 tasks a CTA) and
+// (shard, chunk) tasks per thread (reduce rows: at least 256 tasks a CTA, or
+// 128 in a cluster of 8 up to 12 rows) and
 // whose clusters the device holds at once for the T rows (on request, any
 // cluster that is resident at all); past kClusterFinMaxT finalize rows, a
 // cluster of at most kClusterMidMaxCs CTAs with T * cs CTAs on distinct SMs;
@@ -710,7 +721,10 @@ bool plan_cluster_fin(int mode, const Args &a, const DeviceInfo *d, ClusterPlan 
         const int tasks = a.R * slice;
         const int tpt = (tasks + kClusterThreads - 1) / kClusterThreads;
         if (tpt > kClusterMaxTpt) continue;
-        if (!fin && pref == 0 && tasks < kClusterReduceMinTasks) continue;
+        if (!fin && pref == 0 && tasks < kClusterReduceMinTasks &&
+            !(cs == kClusterReduceMidMaxCs && tasks >= kClusterReduceMinTasks8 &&
+              a.T <= kClusterReduceMinTasks8MaxT))
+            continue;
         const size_t smem = cluster_smem_bytes(a.R, slice);
         if ((long long)smem > (long long)d->smem_optin - 2048) continue;
         cudaError_t e = cudaSuccess;
