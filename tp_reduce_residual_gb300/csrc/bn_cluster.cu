@@ -35,12 +35,11 @@ __device__ __forceinline__ void epilogue_sync(int nthreads)
 }
 
 // Row-wide sum of squares: the epilogue warps' compensated pairs, combined by
-// a warp tree over the warps' pairs (lane w holding warp w's), then the CTAs'
-// pairs exchanged across the cluster and combined by the same tree (lane d
-// holding CTA d's).  Every epilogue thread of every CTA gets the same value.
-// The trees pad with zero pairs, which two-sum adds exactly; they replace
-// loops over the pairs that the compiler unrolled into about a fifth of the
-// kernels' code.
+// a tree over the warps' pairs (lane w holding warp w's), then the CTAs'
+// pairs exchanged across the cluster and combined by the same kind of tree
+// (lane d holding CTA d's).  Every epilogue thread of every CTA gets the same
+// value.  The trees replace loops over the pairs that the compiler unrolled
+// into about a fifth of the kernels' code.
 __device__ __forceinline__ float row_sum_squares_cl(f2 S2, f2 E2, float2 *red, float2 *xslot,
                                                     uint32_t xbar, uint32_t cs, uint32_t q,
                                                     int nwe, int warp, int lane, int tid,
@@ -51,14 +50,7 @@ __device__ __forceinline__ float row_sum_squares_cl(f2 S2, f2 E2, float2 *red, f
     warp_tree(S, E);
     if (lane == 0) red[warp] = make_float2(S, E);
     epilogue_sync(nwe * 32);
-    {
-        const float2 v = lane < nwe ? red[lane] : make_float2(0.f, 0.f);
-        S = v.x;
-        E = v.y;
-        warp_tree(S, E);
-        S = __shfl_sync(0xffffffffu, S, 0);
-        E = __shfl_sync(0xffffffffu, E, 0);
-    }
+    small_tree(red, nwe, lane, S, E);
     if (cs > 1) {
         // thread d sends this CTA's pair into slot q of CTA d, counted in bytes
         // on CTA d's barrier; each CTA's own arrive expects cs * 8 bytes
@@ -68,12 +60,7 @@ __device__ __forceinline__ float row_sum_squares_cl(f2 S2, f2 E2, float2 *red, f
             st_async_f2(mapa(smem_addr(xslot + q), d), S, E, mapa(xbar, d));
         }
         if (!wait_phase<true, kDsmem>(xbar, 0u, ctl)) live = false;
-        const float2 v = lane < (int)cs ? xslot[lane] : make_float2(0.f, 0.f);
-        S = v.x;
-        E = v.y;
-        warp_tree(S, E);
-        S = __shfl_sync(0xffffffffu, S, 0);
-        E = __shfl_sync(0xffffffffu, E, 0);
+        small_tree(xslot, (int)cs, lane, S, E);
     }
     return pair_value(S, E);
 }

@@ -543,6 +543,28 @@ __device__ __forceinline__ void warp_tree(float &S, float &E)
     }
 }
 
+// The pairs src[0..n-1] (1 <= n <= 32) combined as warp_tree combines them on
+// lane 0 with the lanes from n on holding zero pairs, then broadcast to every
+// lane.  A zero pair changes nothing under combine, and at a level whose
+// offset is n or more lane 0's partner holds only zeros, so those levels are
+// left out (a CTA of 5 consumer warps runs 3 of the 5).
+__device__ __forceinline__ void small_tree(const float2 *src, int n, int lane, float &S, float &E)
+{
+    const float2 v = lane < n ? src[lane] : make_float2(0.f, 0.f);
+    S = v.x;
+    E = v.y;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        if (off < n) {
+            const float S2 = __shfl_down_sync(0xffffffffu, S, off);
+            const float E2 = __shfl_down_sync(0xffffffffu, E, off);
+            combine(S, E, S2, E2);
+        }
+    }
+    S = __shfl_sync(0xffffffffu, S, 0);
+    E = __shfl_sync(0xffffffffu, E, 0);
+}
+
 // 1 / sqrt(ss / H + eps): three correctly rounded FP32 operations
 // (-prec-div and -prec-sqrt are left at their IEEE defaults).
 __device__ __forceinline__ float rms_factor(float ss, int H, float eps)
@@ -578,12 +600,7 @@ __device__ __forceinline__ float row_sum_squares(f2 S2, f2 E2, int &nred, const 
     const int b = nred & 1;
     if (lane == 0) sm.red[b * 32 + warp] = make_float2(S, E);
     consumer_sync(NT);
-    const float2 v = (lane < NW) ? sm.red[b * 32 + lane] : make_float2(0.f, 0.f);
-    S = v.x;
-    E = v.y;
-    warp_tree(S, E);
-    S = __shfl_sync(0xffffffffu, S, 0);
-    E = __shfl_sync(0xffffffffu, E, 0);
+    small_tree(sm.red + b * 32, NW, lane, S, E);
     if (cs > 1) {
         float2 *slots = sm.xslot + b * kMaxCluster;
         const uint32_t bar = sm.ex0 + 8u * (uint32_t)b;
