@@ -486,10 +486,18 @@ __device__ __forceinline__ void acc_square_scaled(float &S, float &E, f2 v, floa
     acc_square1(S, E, mul_sep(hi, up));
 }
 
+// (S, E) += (S2, E2) for two compensated sums of squares.  Both running parts
+// are non-negative, so the larger one is known without a branch and Dekker's
+// fast two-sum (the smaller part minus what the rounded sum kept of it) gives
+// the exact rounding error, the value two-sum gives, in a chain of three
+// dependent operations instead of five.  The sum itself is formed from S and
+// S2, so a NaN in either still reaches it.
 __device__ __forceinline__ void combine(float &S, float &E, float S2, float E2)
 {
-    float s, e;
-    two_sum(S, S2, s, e);
+    const float s = S + S2;
+    const float hi = fmaxf(S, S2);
+    const float lo = fminf(S, S2);
+    const float e = lo - (s - hi);
     S = s;
     E = (E + E2) + e;
 }
