@@ -596,7 +596,11 @@ struct Smem {
 // Row-wide sum of squares: compensated pairs reduced over the warp, the
 // consumer warps of the CTA, then the CTAs of the cluster, in a fixed order;
 // every consumer thread of every CTA of the cluster gets the same value.
-template <bool OUTLINE>
+// TREE: the CTAs' pairs are combined by a tree, not one after the other
+// (taken by the shard-split kernels: C4 at T=16 13.24 -> 12.88 us, C3 at
+// T=16 11.23 -> 10.79; the column-split kernels were 0.5-1 % slower with it,
+// their code being laid out differently at the register cap).
+template <bool OUTLINE, bool TREE>
 __device__ __forceinline__ float row_sum_squares(f2 S2, f2 E2, int &nred, const Smem &sm,
                                                  uint32_t cs, uint32_t q, int NT, int NW,
                                                  int warp, int lane, int tid, const Ctl &ctl,
@@ -623,9 +627,13 @@ __device__ __forceinline__ float row_sum_squares(f2 S2, f2 E2, int &nred, const 
             st_async_f2(mapa(smem_addr(slots + q), d), S, E, mapa(bar, d));
         }
         if (!wait_phase<true, kDsmem, OUTLINE>(bar, (uint32_t)(nred >> 1) & 1u, ctl)) live = false;
-        S = slots[0].x;
-        E = slots[0].y;
-        for (uint32_t c = 1; c < cs; ++c) combine(S, E, slots[c].x, slots[c].y);
+        if constexpr (TREE) {
+            small_tree(slots, (int)cs, lane, S, E);
+        } else {
+            S = slots[0].x;
+            E = slots[0].y;
+            for (uint32_t c = 1; c < cs; ++c) combine(S, E, slots[c].x, slots[c].y);
+        }
     }
     ++nred;
     return pair_value(S, E);
@@ -1203,7 +1211,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                             for (int m = 0; m < 4; ++m) acc_square2(S1, E1, s[i][m]);
                         }
                     }
-                    ss1 = row_sum_squares<kOutline>(S1, E1, nred, sm, cs, q, NT, NW, warp, lane, tid, ctl, live);
+                    ss1 = row_sum_squares<kOutline, SPLITR>(S1, E1, nred, sm, cs, q, NT, NW, warp, lane, tid, ctl, live);
                     if (TINY && needs_rescale(ss1)) {  // the same on every thread of the cluster
                         const int kx = rescale_exp(ss1);
                         const float up = pow2f(kx);
@@ -1216,7 +1224,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                                 for (int m = 0; m < 4; ++m) acc_square_scaled(Sb, Eb, s[i][m], up);
                             }
                         }
-                        const float r = row_sum_squares<kOutline>(f2_make(Sb, 0.f), f2_make(Eb, 0.f), nred, sm, cs, q,
+                        const float r = row_sum_squares<kOutline, SPLITR>(f2_make(Sb, 0.f), f2_make(Eb, 0.f), nred, sm, cs, q,
                                                         NT, NW, warp, lane, tid, ctl, live);
                         ss1 = mul_sep(mul_sep(r, pow2f(-kx)), pow2f(-kx));
                     }
@@ -1251,7 +1259,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                     }
                     release();
                 }
-                float ss2 = row_sum_squares<kOutline>(S2, E2, nred, sm, cs, q, NT, NW, warp, lane, tid, ctl, live);
+                float ss2 = row_sum_squares<kOutline, SPLITR>(S2, E2, nred, sm, cs, q, NT, NW, warp, lane, tid, ctl, live);
                 if (TINY && needs_rescale(ss2)) {  // the same on every thread of the cluster
                     const int kx = rescale_exp(ss2);
                     const float up = pow2f(kx);
@@ -1264,7 +1272,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 32, 1) bn_kernel(const Args a)
                             for (int m = 0; m < 4; ++m) acc_square_scaled(Sb, Eb, s[i][m], up);
                         }
                     }
-                    const float r = row_sum_squares<kOutline>(f2_make(Sb, 0.f), f2_make(Eb, 0.f), nred, sm, cs, q,
+                    const float r = row_sum_squares<kOutline, SPLITR>(f2_make(Sb, 0.f), f2_make(Eb, 0.f), nred, sm, cs, q,
                                                     NT, NW, warp, lane, tid, ctl, live);
                     ss2 = mul_sep(mul_sep(r, pow2f(-kx)), pow2f(-kx));
                 }
