@@ -695,15 +695,18 @@ def test_cluster_split_of_reduce_rows_matches_oracle(R, T, H, single, cs):
 
 
 @pytest.mark.parametrize("R,T,H", [(8, 9, 8192), (8, 16, 8192), (8, 32, 8192), (4, 24, 5120),
-                                   (8, 20, 4096), (2, 16, 8192)])
+                                   (8, 20, 4096), (2, 16, 8192), (8, 33, 8192), (16, 34, 4096)])
 def test_reduce_rows_keep_the_cluster_path_to_32_rows(R, T, H):
     """Past 8 token rows the planner keeps heavy reduce rows on the cluster
-    path, with clusters of at most 8 CTAs all resident at once: the forced
-    column split's sum bits and the oracle's results."""
+    path, with clusters of at most 8 CTAs all resident at once (from 33 to 36
+    rows, clusters of 8 only, for rows of 8 or more shards): the forced column
+    split's sum bits and the oracle's results."""
     wl = inputs.custom("reduce_norm", R, H, partial_std=0.5, row_scale=True)
     d = parity.gpu_inputs(wl, T, seed=870 + R * 7 + T + H)
     info = bn.launch_info("reduce_norm", R, T, H)
     assert info["split"] == 2 and info["cluster_size"] <= 8, info
+    if T > 32:
+        assert info["cluster_size"] == 8, info
     assert info["resident_ctas"] >= info["grid"] == T * info["cluster_size"], info
     g = parity.run_fused(d)
     try:
@@ -713,8 +716,12 @@ def test_reduce_rows_keep_the_cluster_path_to_32_rows(R, T, H):
         bn.set_tuning()
     assert_bits_equal(g["sum"], base["sum"], "sum")
     parity.compare(g, parity.run_oracle(d), what=f"cluster reduce R={R} T={T} H={H}")
-    # past 32 rows the main kernel again
-    assert bn.launch_info("reduce_norm", R, 33, H)["split"] != 2
+    # past 32 rows only clusters of 8, all resident, for 8 or more shards
+    i33 = bn.launch_info("reduce_norm", R, 33, H)
+    assert i33["split"] != 2 or (R >= 8 and i33["cluster_size"] == 8 and
+                                 i33["resident_ctas"] >= i33["grid"]), i33
+    # and past 36 rows the main kernel again
+    assert bn.launch_info("reduce_norm", R, 37, H)["split"] != 2
 
 
 @pytest.mark.parametrize("T", [1, 4, 12])

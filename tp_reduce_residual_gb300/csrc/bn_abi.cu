@@ -663,8 +663,19 @@ constexpr int kClusterReduceMinTasks = 256;
 // of 8 no longer fit at once (9.73 against 5.91).  Over R in {2, 4, 8}, H from
 // 2048 to 12288 and T in {9, 12, 16, 24, 32} the rule lost to the main
 // kernel by more than 3 % only at R=4, H=12288, T=24 and 32 (5.32 / 4.83,
-// 5.50 / 4.96).
+// 5.50 / 4.96).  From kClusterReduceMidMaxT + 1 to kClusterReduceWideMaxT
+// rows, rows of at least kClusterReduceWideMinR shards and at most 1024
+// chunks take clusters of kClusterReduceMidMaxCs only, all resident at once
+// (T=33: R=8, H=8192 5.48 / 5.00, R=8, H=4096 5.30 / 4.09; T=34, R=16,
+// H=4096 7.40 / 4.87; T=36, R=8: H=8192 5.57 / 5.43, H=4096 5.58 / 4.78,
+// H=2048 5.01 / 4.10).  Lighter rows lost at T=36 (R=4, H=5120 4.35 / 4.79;
+// R=2, H=8192 4.20 / 4.76), wider ones too (R=4, H=12288: 4.99 / 6.29), and
+// past 36 rows the clusters of 8 lost where they still fit (R=8, H=2048,
+// T=64: 4.98 / 5.36); clusters of 4 or 2 lost by 0-11 % from T=40 on.
 constexpr int kClusterReduceMidMaxT = 32;
+constexpr int kClusterReduceWideMaxT = 36;
+constexpr int kClusterReduceWideMinR = 8;
+constexpr int kClusterReduceWideMaxChunks = 1024;
 constexpr int kClusterReduceMidMaxCs = 8;
 // Up to kClusterReduceMinTasks8MaxT rows, clusters of 8 take reduce rows down
 // to kClusterReduceMinTasks8 tasks a CTA: R=2 rows of 5120 and 7168 (160 and
@@ -697,7 +708,10 @@ struct ClusterPlan {
 // whose clusters the device holds at once for the T rows (on request, any
 // cluster that is resident at all); past kClusterFinMaxT finalize rows, a
 // cluster of at most kClusterMidMaxCs CTAs with T * cs CTAs on distinct SMs;
-// past kClusterReduceMaxT reduce rows, one of at most kClusterReduceMidMaxCs.
+// past kClusterReduceMaxT reduce rows, one of at most kClusterReduceMidMaxCs
+// (past kClusterReduceMidMaxT rows, exactly that many, up to
+// kClusterReduceWideMaxT rows, for rows of at least kClusterReduceWideMinR
+// shards and at most kClusterReduceWideMaxChunks chunks).
 bool plan_cluster_fin(int mode, const Args &a, const DeviceInfo *d, ClusterPlan *p)
 {
     const bool fin = (mode & F_FIN) != 0;
@@ -708,7 +722,10 @@ bool plan_cluster_fin(int mode, const Args &a, const DeviceInfo *d, ClusterPlan 
     if (pref != 0 && pref != 3) return false;
     const bool mid = fin && pref == 0 && a.T > kClusterFinMaxT;
     const bool mid_reduce = !fin && pref == 0 && a.T > kClusterReduceMaxT;
-    if (mid_reduce && a.T > kClusterReduceMidMaxT) return false;
+    if (mid_reduce && a.T > kClusterReduceMidMaxT &&
+        (a.T > kClusterReduceWideMaxT || a.R < kClusterReduceWideMinR ||
+         a.H / 8 > kClusterReduceWideMaxChunks))
+        return false;
     if (mid && (long long)a.T * 2 > d->sms) return false;
     const int want_cs = g_tune_cluster.load();
     const int nch = a.H / 8;
@@ -716,6 +733,7 @@ bool plan_cluster_fin(int mode, const Args &a, const DeviceInfo *d, ClusterPlan 
         if (want_cs > 0 && cs != want_cs) continue;
         if (mid && (long long)a.T * cs > d->sms) continue;
         if (mid_reduce && cs > kClusterReduceMidMaxCs) continue;
+        if (mid_reduce && a.T > kClusterReduceMidMaxT && cs != kClusterReduceMidMaxCs) continue;
         const int slice = (nch + cs - 1) / cs;
         if (nch < cs || slice > kClusterThreads) continue;
         const int tasks = a.R * slice;
